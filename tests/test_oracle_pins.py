@@ -1,0 +1,480 @@
+"""Pins for the float64 oracle: each test checks it against something other
+than itself -- hand-derived closed forms (tests/golden), central-difference
+VJPs of the forward definitions, algebraic invariants, and brute force on
+tiny shapes.  The negative controls of Hesper's WrongBackwardTest (zero,
+identity, negated backward, wrong RoPE sign) must FAIL the same checks, and so
+must mistakes planted in copies of the oracle's functions.
+
+Pages: "Hesper.Training.VerifiedBackward" API documentation (Verification
+Strategy: Tier 1 algebraic identities, Tier 2 finite differences with
+eps 1e-4, tol 1e-3) and Hesper pull request #1 ("Tests/WrongBackwardTest.lean").
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+
+import oracle as O
+
+pytestmark = pytest.mark.filterwarnings("ignore::RuntimeWarning")
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "closed_forms.json")
+
+
+@pytest.fixture(scope="module")
+def golden():
+    with open(GOLDEN) as f:
+        return json.load(f)
+
+
+def rng(seed):
+    return np.random.default_rng(seed)
+
+
+# --------------------------------------------------------------------------
+# Closed forms (tests/golden)
+# --------------------------------------------------------------------------
+def test_golden_softmax(golden):
+    g = golden["softmax_forward"]
+    np.testing.assert_allclose(O.softmax_forward(g["x"]), g["s"], rtol=0, atol=1e-15)
+    g = golden["softmax_backward_2"]
+    np.testing.assert_allclose(O.softmax_backward_from_logits(g["x"], g["dy"]), g["dx"], atol=1e-15)
+
+
+def test_golden_rope(golden):
+    g = golden["rope_quarter_turn"]
+    t = g["theta"]
+    np.testing.assert_allclose(O.rope_forward_pair(*g["forward_in"], t), g["forward_out"], atol=1e-15)
+    np.testing.assert_allclose(O.rope_backward_pair(*g["backward_in_a"], t), g["backward_out_a"], atol=1e-15)
+    np.testing.assert_allclose(O.rope_backward_pair(*g["backward_in_b"], t), g["backward_out_b"], atol=1e-15)
+    g = golden["rope_angles"]
+    np.testing.assert_allclose(O.rope_angles(np.array(g["positions"]), g["D"], g["base"]), g["theta"],
+                               rtol=1e-14, atol=0)
+
+
+def test_golden_rmsnorm(golden):
+    g = golden["rmsnorm_backward_eps0"]
+    np.testing.assert_allclose(O.rmsnorm_backward(g["x"], g["gamma"], g["dy"], g["eps"]), g["dx"],
+                               rtol=1e-14)
+
+
+def test_golden_attention(golden):
+    g = golden["attention_two_keys"]
+    dq, dK, dV = O.attention_backward_single(g["q"], g["K"], g["V"], g["scale"], g["dout"])
+    np.testing.assert_allclose(dq, g["dq"], rtol=1e-14)
+    np.testing.assert_allclose(dK, g["dK"], rtol=1e-14)
+    np.testing.assert_allclose(dV, g["dV"], rtol=1e-14)
+    g = golden["attention_single_key"]
+    dq, dK, dV = O.attention_backward_single(g["q"], g["K"], g["V"], g["scale"], g["dout"])
+    assert np.all(dq == 0) and np.all(dK == 0)
+    np.testing.assert_allclose(dV[0], g["dout"], rtol=0, atol=0)
+
+
+# --------------------------------------------------------------------------
+# Softmax: VJP, sum to zero
+# --------------------------------------------------------------------------
+@pytest.mark.parametrize("n,seed", [(1, 0), (2, 1), (5, 2), (16, 3)])
+def test_softmax_backward_vjp(n, seed):
+    r = rng(seed)
+    x, dy = r.normal(size=n), r.normal(size=n)
+    num = O.numerical_grad(lambda z: float(np.dot(dy, O.softmax_forward(z))), x)
+    assert O.check_gradient(O.softmax_backward_from_logits(x, dy), num)
+    # and more tightly than the page's tolerance
+    np.testing.assert_allclose(O.softmax_backward_from_logits(x, dy), num, atol=1e-8)
+
+
+def test_softmax_sums_to_zero():
+    r = rng(7)
+    for n in (1, 3, 16, 1000):
+        x, dy = r.normal(size=n) * 3, r.normal(size=n)
+        assert abs(O.softmax_backward_sums_to_zero(x, dy)) < 1e-12
+    # shift invariance of the forward and the rowwise (batched) form
+    x = r.normal(size=(4, 9))
+    np.testing.assert_allclose(O.softmax_forward(x + 5.0), O.softmax_forward(x), atol=1e-15)
+    np.testing.assert_allclose(O.softmax_forward(x).sum(-1), 1.0, atol=1e-15)
+    dy = r.normal(size=(4, 9))
+    rows = np.stack([O.softmax_backward_from_logits(x[i], dy[i]) for i in range(4)])
+    np.testing.assert_allclose(O.softmax_backward_from_logits(x, dy), rows, atol=1e-15)
+
+
+# --------------------------------------------------------------------------
+# RoPE: VJP, round trip, norm, closed forms, tensor layouts
+# --------------------------------------------------------------------------
+def test_rope_pair_vjp_and_roundtrip():
+    r = rng(11)
+    for _ in range(20):
+        x = r.normal(size=2)
+        theta = r.uniform(-math.pi, math.pi)
+        dy = r.normal(size=2)
+        f = lambda z: float(np.dot(dy, O.rope_forward_pair(z[0], z[1], theta)))
+        num = O.numerical_grad(f, x)
+        assert O.check_gradient(np.array(O.rope_backward_pair(dy[0], dy[1], theta)), num)
+        assert O.rope_roundtrip_check(x[0], x[1], theta, tol=1e-6)
+        # rotation preserves the pair norm
+        y = O.rope_forward_pair(x[0], x[1], theta)
+        assert abs(math.hypot(*y) - math.hypot(*x)) < 1e-13
+        z = O.rope_backward_pair(dy[0], dy[1], theta)
+        assert abs(math.hypot(*z) - math.hypot(*dy)) < 1e-13
+    # theta = 0 is the identity
+    assert O.rope_backward_pair(0.3, -0.7, 0.0) == (0.3, -0.7)
+
+
+@pytest.mark.parametrize("interleaved", [True, False])
+def test_rope_tensor_matches_pairs(interleaved):
+    r = rng(12)
+    B, T, H, D = 2, 3, 2, 8
+    dy = r.normal(size=(B, T, H, D))
+    theta = O.rope_angles(np.arange(T)[None, :].repeat(B, 0) + 5, D, 10000.0)
+    out = O.rope_backward(dy, theta, interleaved)
+    for b in range(B):
+        for t in range(T):
+            for h in range(H):
+                for i in range(D // 2):
+                    a, c = (2 * i, 2 * i + 1) if interleaved else (i, i + D // 2)
+                    z0, z1 = O.rope_backward_pair(dy[b, t, h, a], dy[b, t, h, c], theta[b, t, i])
+                    assert out[b, t, h, a] == z0 and out[b, t, h, c] == z1
+    back = O.rope_forward(out, theta, interleaved)
+    np.testing.assert_allclose(back, dy, atol=1e-12)
+
+
+def test_rope_tensor_vjp():
+    r = rng(13)
+    B, T, H, D = 1, 2, 2, 4
+    theta = r.uniform(-3, 3, size=(B, T, D // 2))
+    x = r.normal(size=(B, T, H, D))
+    dy = r.normal(size=(B, T, H, D))
+    for inter in (True, False):
+        num = O.numerical_grad(lambda z: float(np.sum(dy * O.rope_forward(z, theta, inter))), x)
+        assert O.check_gradient(O.rope_backward(dy, theta, inter), num)
+
+
+# --------------------------------------------------------------------------
+# RMSNorm: VJP, scale-invariance identity
+# --------------------------------------------------------------------------
+@pytest.mark.parametrize("n,eps,seed", [(1, 1e-6, 0), (8, 1e-6, 1), (33, 1e-6, 2), (8, 0.5, 3)])
+def test_rmsnorm_backward_vjp(n, eps, seed):
+    r = rng(seed)
+    x, dy = r.normal(size=n), r.normal(size=n)
+    gamma = 1.0 + 0.1 * r.normal(size=n)
+    num = O.numerical_grad(lambda z: float(np.dot(dy, O.rmsnorm_forward(z, gamma, eps))), x)
+    assert O.check_gradient(O.rmsnorm_backward(x, gamma, dy, eps), num)
+    np.testing.assert_allclose(O.rmsnorm_backward(x, gamma, dy, eps), num, atol=1e-7)
+
+
+def test_rmsnorm_scale_identity():
+    """y(c x) with eps -> the same y: d/dc <dy, y(c x)> at c = 1 equals
+    <dx, x>.  With eps, y(c x) = g x / sqrt(ms + eps/c^2), which gives
+    <dx, x> = (eps / (ms + eps)) <dy g, x> / rms."""
+    r = rng(21)
+    for eps in (1e-6, 0.3, 2.0):
+        x, dy = r.normal(size=17), r.normal(size=17)
+        gamma = 1 + 0.1 * r.normal(size=17)
+        ms = np.mean(x * x)
+        rms = math.sqrt(ms + eps)
+        lhs = float(np.dot(O.rmsnorm_backward(x, gamma, dy, eps), x))
+        rhs = eps / (ms + eps) * float(np.dot(dy * gamma, x)) / rms
+        assert abs(lhs - rhs) < 1e-12 * max(1.0, abs(rhs))
+    # forward: with gamma = 1 and eps = 0 the output has unit mean square
+    y = O.rmsnorm_forward(x, np.ones_like(x), 0.0)
+    assert abs(np.mean(y * y) - 1.0) < 1e-14
+
+
+# --------------------------------------------------------------------------
+# Scaled dot product and single-query attention
+# --------------------------------------------------------------------------
+def test_scaled_dot_vjp():
+    r = rng(31)
+    q, k = r.normal(size=6), r.normal(size=6)
+    scale, ds = 0.37, 1.7
+    nq = O.numerical_grad(lambda z: ds * O.scaled_dot_forward(z, k, scale), q)
+    nk = O.numerical_grad(lambda z: ds * O.scaled_dot_forward(q, z, scale), k)
+    assert O.check_gradient(O.scaled_dot_backward_q(k, scale, ds), nq)
+    assert O.check_gradient(O.scaled_dot_backward_k(q, scale, ds), nk)
+
+
+@pytest.mark.parametrize("S,D,seed", [(1, 4, 0), (3, 2, 1), (16, 8, 2)])
+def test_attention_single_vjp(S, D, seed):
+    """Brute force: numerical gradients of <dOut, attentionForward(q, K, V)>."""
+    r = rng(seed)
+    q, K, V, dout = r.normal(size=D), r.normal(size=(S, D)), r.normal(size=(S, D)), r.normal(size=D)
+    scale = 1 / math.sqrt(D)
+    dq, dK, dV = O.attention_backward_single(q, K, V, scale, dout)
+    f = lambda q_, K_, V_: float(np.dot(dout, O.attention_forward_single(q_, K_, V_, scale)))
+    assert O.check_gradient(dq, O.numerical_grad(lambda z: f(z, K, V), q))
+    assert O.check_gradient(dK, O.numerical_grad(lambda z: f(q, z, V), K))
+    assert O.check_gradient(dV, O.numerical_grad(lambda z: f(q, K, z), V))
+
+
+def test_matrix_form_equals_single_query_loop():
+    r = rng(41)
+    T, S, D = 5, 7, 3
+    Q, K, V, dO = r.normal(size=(T, D)), r.normal(size=(S, D)), r.normal(size=(S, D)), r.normal(size=(T, D))
+    scale = 0.6
+    dQ, dK, dV = O.attention_head_backward(Q, K, V, dO, scale, causal=False)
+    sK = np.zeros_like(K)
+    sV = np.zeros_like(V)
+    for i in range(T):
+        dq, dk, dv = O.attention_backward_single(Q[i], K, V, scale, dO[i])
+        np.testing.assert_allclose(dQ[i], dq, atol=1e-13)
+        sK += dk
+        sV += dv
+    np.testing.assert_allclose(dK, sK, atol=1e-13)
+    np.testing.assert_allclose(dV, sV, atol=1e-13)
+    # forward matrix form equals the single-query forward
+    Om, _, _ = O.attention_head_forward(Q, K, V, scale, causal=False)
+    for i in range(T):
+        np.testing.assert_allclose(Om[i], O.attention_forward_single(Q[i], K, V, scale), atol=1e-14)
+
+
+def test_causal_rows_are_prefix_attention():
+    """Causal row i equals full attention over keys 0..i (transformer.js mask)."""
+    r = rng(42)
+    T, D = 6, 3
+    Q, K, V, dO = (r.normal(size=(T, D)) for _ in range(4))
+    Om, lse, _ = O.attention_head_forward(Q, K, V, 0.5, causal=True)
+    dQ, _, _ = O.attention_head_backward(Q, K, V, dO, 0.5, causal=True)
+    for i in range(T):
+        np.testing.assert_allclose(Om[i], O.attention_forward_single(Q[i], K[: i + 1], V[: i + 1], 0.5), atol=1e-14)
+        dq, _, _ = O.attention_backward_single(Q[i], K[: i + 1], V[: i + 1], 0.5, dO[i])
+        np.testing.assert_allclose(dQ[i], dq, atol=1e-13)
+        s = 0.5 * (K[: i + 1] @ Q[i])
+        assert abs(lse[i] - math.log(np.sum(np.exp(s)))) < 1e-13
+
+
+# --------------------------------------------------------------------------
+# Whole decode / causal paths: brute force VJPs including GQA and RoPE
+# --------------------------------------------------------------------------
+def _decode_forward(q_pre, k, v, scale, theta_q, G):
+    """Decode forward with RoPE on the query: q = R(theta) q_pre."""
+    B, Hq, D = q_pre.shape
+    q = O.rope_forward(q_pre[:, None], theta_q)[:, 0]
+    out = np.zeros_like(q)
+    for b in range(B):
+        for h in range(Hq):
+            out[b, h] = O.attention_forward_single(q[b, h], k[b, :, h // G], v[b, :, h // G], scale)
+    return out
+
+
+def test_decode_backward_vjp_gqa_rope():
+    r = rng(51)
+    B, Hq, Hkv, S, D = 1, 4, 2, 5, 4
+    G = Hq // Hkv
+    q_pre = r.normal(size=(B, Hq, D))
+    k, v = r.normal(size=(B, S, Hkv, D)), r.normal(size=(B, S, Hkv, D))
+    dout = r.normal(size=(B, Hq, D))
+    scale, base, pos = 0.5, 10000.0, 3
+    theta = O.rope_angles(np.full((B, 1), pos), D, base)
+    q = O.rope_forward(q_pre[:, None], theta)[:, 0]
+    dq, dk, dv = O.decode_backward(q, k, v, dout, scale, base, pos)
+    f = lambda qp, k_, v_: float(np.sum(dout * _decode_forward(qp, k_, v_, scale, theta, G)))
+    assert O.check_gradient(dq, O.numerical_grad(lambda z: f(z, k, v), q_pre))
+    assert O.check_gradient(dk, O.numerical_grad(lambda z: f(q_pre, z, v), k))
+    assert O.check_gradient(dv, O.numerical_grad(lambda z: f(q_pre, k, z), v))
+
+
+def _causal_forward_rope(q_pre, k_pre, v, scale, theta):
+    q = O.rope_forward(q_pre, theta)
+    k = O.rope_forward(k_pre, theta)
+    o, _ = O.causal_forward(q, k, v, scale)
+    return o
+
+
+def test_causal_backward_vjp_gqa_rope():
+    r = rng(52)
+    B, T, Hq, Hkv, D = 1, 5, 4, 2, 4
+    q_pre, k_pre = r.normal(size=(B, T, Hq, D)), r.normal(size=(B, T, Hkv, D))
+    v, dout = r.normal(size=(B, T, Hkv, D)), r.normal(size=(B, T, Hq, D))
+    scale, base = 0.5, 100.0
+    theta = O.rope_angles(np.arange(T)[None, :], D, base)
+    q, k = O.rope_forward(q_pre, theta), O.rope_forward(k_pre, theta)
+    dq, dk, dv = O.causal_backward(q, k, v, dout, scale, base, 0)
+    f = lambda a, b_, c: float(np.sum(dout * _causal_forward_rope(a, b_, c, scale, theta)))
+    assert O.check_gradient(dq, O.numerical_grad(lambda z: f(z, k_pre, v), q_pre))
+    assert O.check_gradient(dk, O.numerical_grad(lambda z: f(q_pre, z, v), k_pre))
+    assert O.check_gradient(dv, O.numerical_grad(lambda z: f(q_pre, k_pre, z), v))
+
+
+def test_causal_directional_derivative_medium():
+    """At a size too large for entry-by-entry brute force: the derivative of
+    <dO, Attn> along random directions equals <grad, direction>."""
+    r = rng(53)
+    B, T, Hq, Hkv, D = 1, 40, 2, 1, 8
+    q, k, v, dout = (r.normal(size=s) for s in [(B, T, Hq, D), (B, T, Hkv, D), (B, T, Hkv, D), (B, T, Hq, D)])
+    scale = 1 / math.sqrt(D)
+    dq, dk, dv = O.causal_backward(q, k, v, dout, scale)
+    f = lambda a, b_, c: float(np.sum(dout * O.causal_forward(a, b_, c, scale)[0]))
+    eps = 1e-5
+    for grad, which in ((dq, 0), (dk, 1), (dv, 2)):
+        u = r.normal(size=grad.shape)
+        args_p = [q, k, v]
+        args_m = [q, k, v]
+        args_p = [a + eps * u if i == which else a for i, a in enumerate(args_p)]
+        args_m = [a - eps * u if i == which else a for i, a in enumerate(args_m)]
+        num = (f(*args_p) - f(*args_m)) / (2 * eps)
+        assert abs(num - float(np.sum(grad * u))) < 1e-6 * max(1.0, abs(num))
+
+
+def test_chain_layer_vjp():
+    """Tiny chain layer with a consistent forward: y = RMSNorm(Attn(R q, R k, v));
+    numerical gradients of <dHidden, y> match chain_layer_backward fed with
+    x = the attention output."""
+    r = rng(54)
+    B, T, Hq, Hkv, D = 1, 3, 2, 1, 4
+    n = Hq * D
+    q_pre, k_pre = r.normal(size=(B, T, Hq, D)), r.normal(size=(B, T, Hkv, D))
+    v = r.normal(size=(B, T, Hkv, D))
+    gamma = 1 + 0.1 * r.normal(size=n)
+    dh = r.normal(size=(B * T, n))
+    scale, base, eps = 0.5, 50.0, 1e-6
+    theta = O.rope_angles(np.arange(T)[None, :], D, base)
+    q, k = O.rope_forward(q_pre, theta), O.rope_forward(k_pre, theta)
+    x = O.causal_forward(q, k, v, scale)[0].reshape(B * T, n)
+    _, dq, dk, dv = O.chain_layer_backward(x, gamma, dh, q, k, v, eps, scale, base)
+
+    def f(a, b_, c):
+        o = _causal_forward_rope(a, b_, c, scale, theta).reshape(B * T, n)
+        return float(np.sum(dh * O.rmsnorm_forward(o, gamma, eps)))
+    assert O.check_gradient(dq, O.numerical_grad(lambda z: f(z, k_pre, v), q_pre))
+    assert O.check_gradient(dk, O.numerical_grad(lambda z: f(q_pre, z, v), k_pre))
+    assert O.check_gradient(dv, O.numerical_grad(lambda z: f(q_pre, k_pre, z), v))
+
+
+# --------------------------------------------------------------------------
+# Invariants and special cases
+# --------------------------------------------------------------------------
+def test_attention_invariants():
+    r = rng(61)
+    B, T, Hq, Hkv, D = 2, 9, 4, 2, 5
+    q, k, v, dout = (r.normal(size=s) for s in [(B, T, Hq, D), (B, T, Hkv, D), (B, T, Hkv, D), (B, T, Hq, D)])
+    dq, dk, dv = O.causal_backward(q, k, v, dout, 0.4)
+    G = Hq // Hkv
+    for b in range(B):
+        for j in range(Hkv):
+            # sum_j dS_ij = 0 for every row i, so sum over keys of dK vanishes
+            np.testing.assert_allclose(dk[b, :, j].sum(0), 0.0, atol=1e-12)
+            # every P row sums to 1, so sum over keys of dV equals sum of dO
+            np.testing.assert_allclose(dv[b, :, j].sum(0), dout[b, :, j * G:(j + 1) * G].sum((0, 1)), atol=1e-12)
+    # delta_i = sum_j P_ij dP_ij equals dO_i . O_i
+    Om, _, P = O.attention_head_forward(q[0, :, 0], k[0, :, 0], v[0, :, 0], 0.4, True)
+    dP = dout[0, :, 0] @ v[0, :, 0].T
+    np.testing.assert_allclose(np.sum(P * dP, -1), np.sum(dout[0, :, 0] * Om, -1), atol=1e-12)
+
+
+def test_decode_is_last_causal_row():
+    r = rng(62)
+    B, S, Hq, Hkv, D = 2, 7, 4, 2, 3
+    q, k, v, dout = (r.normal(size=s) for s in [(B, S, Hq, D), (B, S, Hkv, D), (B, S, Hkv, D), (B, S, Hq, D)])
+    dq_c, _, _ = O.causal_backward(q, k, v, dout, 0.3)
+    dq_d, dk_d, dv_d = O.decode_backward(q[:, -1], k, v, dout[:, -1], 0.3)
+    np.testing.assert_allclose(dq_d, dq_c[:, -1], atol=1e-13)
+    # the decode dK/dV equal the causal ones with only the last query's dO
+    dmask = np.zeros_like(dout)
+    dmask[:, -1] = dout[:, -1]
+    _, dk_c, dv_c = O.causal_backward(q, k, v, dmask, 0.3)
+    np.testing.assert_allclose(dk_d, dk_c, atol=1e-13)
+    np.testing.assert_allclose(dv_d, dv_c, atol=1e-13)
+
+
+def test_gqa_equals_repeated_mha():
+    r = rng(63)
+    B, T, Hq, Hkv, D = 1, 6, 6, 2, 4
+    G = Hq // Hkv
+    q, k, v, dout = (r.normal(size=s) for s in [(B, T, Hq, D), (B, T, Hkv, D), (B, T, Hkv, D), (B, T, Hq, D)])
+    dq, dk, dv = O.causal_backward(q, k, v, dout, 0.5, 1000.0)
+    kr, vr = np.repeat(k, G, axis=2), np.repeat(v, G, axis=2)
+    dq2, dk2, dv2 = O.causal_backward(q, kr, vr, dout, 0.5, 1000.0)
+    np.testing.assert_allclose(dq, dq2, atol=1e-13)
+    np.testing.assert_allclose(dk, dk2.reshape(B, T, Hkv, G, D).sum(3), atol=1e-13)
+    np.testing.assert_allclose(dv, dv2.reshape(B, T, Hkv, G, D).sum(3), atol=1e-13)
+
+
+def test_single_key_and_zero_query():
+    r = rng(64)
+    q, k, v, dout = r.normal(size=(1, 2, 3)), r.normal(size=(1, 1, 1, 3)), r.normal(size=(1, 1, 1, 3)), r.normal(size=(1, 2, 3))
+    dq, dk, dv = O.decode_backward(q, k, v, dout, 0.7)
+    assert np.all(dq == 0) and np.all(dk == 0)
+    np.testing.assert_allclose(dv[0, 0, 0], dout[0].sum(0), atol=1e-15)
+    # q = 0: uniform attention, dV[j] = dOut / S
+    S = 5
+    k, v = r.normal(size=(1, S, 1, 3)), r.normal(size=(1, S, 1, 3))
+    _, _, dv = O.decode_backward(np.zeros((1, 1, 3)), k, v, dout[:, :1], 0.7)
+    np.testing.assert_allclose(dv[0, :, 0], np.repeat(dout[:, :1] / S, S, 0)[:, 0], atol=1e-15)
+
+
+# --------------------------------------------------------------------------
+# Negative controls (Hesper's WrongBackwardTest) and planted mistakes
+# --------------------------------------------------------------------------
+def _vjp_cases():
+    r = rng(71)
+    x, dy = r.normal(size=6), r.normal(size=6)
+    gamma = 1 + 0.1 * r.normal(size=6)
+    theta = 1.1   # sin(theta) far from 0 so identity and wrong sign differ
+    return x, dy, gamma, theta
+
+
+def test_negative_controls_fail():
+    x, dy, gamma, theta = _vjp_cases()
+    # softmax
+    num = O.numerical_grad(lambda z: float(np.dot(dy, O.softmax_forward(z))), x)
+    good = O.softmax_backward_from_logits(x, dy)
+    assert O.check_gradient(good, num)
+    assert not O.check_gradient(np.zeros_like(good), num)       # zero backward
+    assert not O.check_gradient(dy, num)                        # identity backward
+    assert not O.check_gradient(-good, num)                     # negated backward
+    # RMSNorm
+    num = O.numerical_grad(lambda z: float(np.dot(dy, O.rmsnorm_forward(z, gamma))), x)
+    good = O.rmsnorm_backward(x, gamma, dy)
+    assert O.check_gradient(good, num)
+    for bad in (np.zeros_like(good), dy, -good):
+        assert not O.check_gradient(bad, num)
+    # RoPE, including the wrong rotation sign R(+theta)
+    p = x[:2]
+    num = O.numerical_grad(lambda z: float(np.dot(dy[:2], O.rope_forward_pair(z[0], z[1], theta))), p)
+    good = np.array(O.rope_backward_pair(dy[0], dy[1], theta))
+    wrong_sign = np.array(O.rope_forward_pair(dy[0], dy[1], theta))
+    assert O.check_gradient(good, num)
+    for bad in (np.zeros(2), dy[:2], -good, wrong_sign):
+        assert not O.check_gradient(bad, num)
+    # attention dQ := dOut is the identity control for a shape-preserving map
+    r = rng(72)
+    q, K, V, dout = r.normal(size=4), r.normal(size=(6, 4)), r.normal(size=(6, 4)), r.normal(size=4)
+    dq, _, _ = O.attention_backward_single(q, K, V, 0.5, dout)
+    num = O.numerical_grad(lambda z: float(np.dot(dout, O.attention_forward_single(z, K, V, 0.5))), q)
+    assert O.check_gradient(dq, num)
+    for bad in (np.zeros(4), dout, -dq):
+        assert not O.check_gradient(bad, num)
+
+
+def test_planted_mistakes_fail():
+    """Plausible slips in the oracle's own formulas are caught by the pins."""
+    r = rng(73)
+    x, dy = r.normal(size=7), r.normal(size=7)
+    gamma = 1 + 0.1 * r.normal(size=7)
+    s = O.softmax_forward(x)
+    num_sm = O.numerical_grad(lambda z: float(np.dot(dy, O.softmax_forward(z))), x)
+    assert not O.check_gradient(s * dy, num_sm)                                 # dropped sum term
+    assert not O.check_gradient(s * (dy + np.sum(s * dy)), num_sm)              # wrong sign
+    num_rn = O.numerical_grad(lambda z: float(np.dot(dy, O.rmsnorm_forward(z, gamma))), x)
+    n = x.size
+    rms = math.sqrt(np.mean(x * x) + 1e-6)
+    c = np.sum(dy * gamma * x)
+    assert not O.check_gradient(dy * gamma / rms, num_rn)                       # dropped c term
+    assert not O.check_gradient((dy * gamma - x * c / (n * rms)) / rms, num_rn)  # rms instead of rms^2
+    # attention: transposed operand in dK (dS Q instead of dS^T Q) and P for dP
+    T, D = 5, 5
+    Q, K, V, dO = (r.normal(size=(T, D)) for _ in range(4))
+    _, _, P = O.attention_head_forward(Q, K, V, 0.5, True)
+    dP = dO @ V.T
+    dS = O.softmax_backward(P, dP)
+    f = lambda kk: float(np.sum(dO * O.attention_head_forward(Q, kk, V, 0.5, True)[0]))
+    num_k = O.numerical_grad(f, K)
+    assert O.check_gradient(0.5 * dS.T @ Q, num_k)
+    assert not O.check_gradient(0.5 * dS @ Q, num_k)
+    fv = lambda vv: float(np.sum(dO * O.attention_head_forward(Q, K, vv, 0.5, True)[0]))
+    num_v = O.numerical_grad(fv, V)
+    assert not O.check_gradient(P @ dO, num_v)
+    # RoPE angle with the wrong exponent (-i/D instead of -2i/D) breaks the closed form
+    wrong = np.arange(4)[:, None] * np.power(10000.0, -np.arange(2) / 4.0)
+    assert not np.allclose(wrong, O.rope_angles(np.arange(4), 4, 10000.0))
