@@ -1,0 +1,454 @@
+#!/usr/bin/env python3
+"""Benchmark of the attention backward chain on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl native|reference]
+
+One step is one pass of the decode-style backward path over the GQA decode
+batch (64 sequences, 20 query heads over 5 KV heads, head dim 128, 1024 cached
+keys in bf16): attention backward with RoPE backward fused on dq, plus the
+RMSNorm backward of the 64 x 2560 hidden rows.  `value` is algorithmic HBM
+bytes per step / device time per step (GB/s), whole job over N GPUs (every
+rank runs its own replica; no data crosses ranks).  The same line carries the
+causal T = 2048 backward (B=4, H=20, D=128, bf16) as TFLOP/s, the 30-layer
+chain time, the roofline fraction of the dominant kernels against the
+measured peaks, the end-to-end number through host buffers, and the float64
+oracle timed on the host cores.
+
+`--impl reference` times the float64 CPU oracle (the slow plain definition)
+on the same workload and metric on the host cores, rank 0 only.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+DECODE_WORKLOAD = "decode_gqa_b64_hq20_hkv5_d128_s1024_bf16kv+rmsnorm_64x2560"
+
+
+# ----------------------------------------------------------------------------
+# algorithmic work
+# ----------------------------------------------------------------------------
+def decode_bytes(B=64, Hq=20, Hkv=5, S=1024, D=128, kv_es=2):
+    kv_read = 2 * B * S * Hkv * D * kv_es
+    grad_write = 2 * B * S * Hkv * D * 4
+    q_io = 3 * B * Hq * D * 4          # q, dout read; dq written
+    return kv_read + grad_write + q_io
+
+
+def rmsnorm_bytes(rows, n, x_es=4, dx_es=4):
+    return rows * n * (x_es + 4 + dx_es) + n * 4
+
+
+def causal_flops(B, T, H, D):
+    """Five matrix products over the causal (lower-triangular) half:
+    5 * 2 * D * B * H * T^2 / 2."""
+    return 5.0 * B * H * T * T * D
+
+
+# ----------------------------------------------------------------------------
+# clocks sampled during the timed region
+# ----------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.thread.join(timeout=2)
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[4:8]):
+                if val.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------
+# float64 oracle timing (CPU baseline / reference arm)
+# ----------------------------------------------------------------------------
+def _oracle_decode_units(args):
+    """Worker: the oracle on a list of (b, kv head) units of the decode batch
+    plus its share of RMSNorm rows.  Runs in a spawned process."""
+    units, rows = args
+    import numpy as np
+    import oracle as O
+    from transformer_attention_backward_gb300 import workloads as W
+    shape = W.DECODE_GQA
+    inp = W.decode_inputs(shape, seed=W.SEED_BASE + 2)
+    q, k, v, do = (inp[n].double().numpy() for n in ("q", "k", "v", "dout"))
+    rn = W.rmsnorm_inputs(*W.RMSNORM_DECODE, seed=W.SEED_BASE + 20)
+    x, g, dy = (rn[n].double().numpy() for n in ("x", "gamma", "dy"))
+    G = shape.Hq // shape.Hkv
+    t0 = time.perf_counter()
+    for b, j in units:
+        hs = slice(j * G, (j + 1) * G)
+        O.decode_backward(q[b:b + 1, hs], k[b:b + 1, :, j:j + 1], v[b:b + 1, :, j:j + 1], do[b:b + 1, hs],
+                          shape.scale, shape.rope_base, shape.q_pos)
+    if rows:
+        O.rmsnorm_backward(x[rows[0]:rows[1]], g, dy[rows[0]:rows[1]], rn["eps"])
+    return time.perf_counter() - t0
+
+
+def oracle_decode_time(n_units: int, workers: int):
+    """Seconds for the oracle to process `n_units` (b, kv head) units of the
+    decode batch and the matching RMSNorm rows, over `workers` processes."""
+    import multiprocessing as mp
+    units = [(b, j) for b in range(64) for j in range(5)][:n_units]
+    rows_total = 64 * n_units // 320
+    chunks = [units[i::workers] for i in range(workers)]
+    row_bounds = []
+    per = max(1, (rows_total + workers - 1) // workers)
+    for i in range(workers):
+        lo, hi = i * per, min(rows_total, (i + 1) * per)
+        row_bounds.append((lo, hi) if lo < hi else None)
+    env_keep = os.environ.get("OPENBLAS_NUM_THREADS")
+    os.environ["OPENBLAS_NUM_THREADS"] = "1"
+    os.environ["OMP_NUM_THREADS"] = "1"
+    try:
+        ctx = mp.get_context("spawn")
+        with ctx.Pool(workers) as pool:
+            pool.map(_oracle_decode_units, [([], None)] * workers)       # warm the workers (imports, inputs)
+            t0 = time.perf_counter()
+            pool.map(_oracle_decode_units, list(zip(chunks, row_bounds)))
+            wall = time.perf_counter() - t0
+    finally:
+        if env_keep is None:
+            os.environ.pop("OPENBLAS_NUM_THREADS", None)
+        else:
+            os.environ["OPENBLAS_NUM_THREADS"] = env_keep
+    frac = n_units / 320.0
+    return wall, frac
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+# ----------------------------------------------------------------------------
+# reference arm
+# ----------------------------------------------------------------------------
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    cores = cpu_cores()
+    n_units = 320
+    step_bytes = decode_bytes() + rmsnorm_bytes(64, 2560)
+    times = []
+    for i in range(args.warmup + args.steps):
+        wall, frac = oracle_decode_time(n_units, cores)
+        if i >= args.warmup:
+            times.append(wall / frac)
+    ms = 1e3 * statistics.median(times)
+    value = step_bytes / (ms * 1e-3) / 1e9
+    line = {
+        "impl": "reference", "metric": "attn_bwd_decode_gbps", "value": round(value, 4), "unit": "GB/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": DECODE_WORKLOAD, "global_batch": 64, "seq_len": 1024, "parallelism": "replicas"},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                         "sample": "full decode batch (320 (batch, KV head) units) + 64 RMSNorm rows per step, "
+                                   "float64 numpy oracle, spawned processes with 1 BLAS thread each"},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ----------------------------------------------------------------------------
+# native arm
+# ----------------------------------------------------------------------------
+def load_peaks():
+    for p in (os.path.join(ROOT, "MEASURED_PEAKS.json"),):
+        if os.path.exists(p):
+            with open(p) as f:
+                d = json.load(f)
+            return d, "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+def source_hash(*names):
+    h = hashlib.sha256()
+    for n in names:
+        with open(os.path.join(ROOT, "transformer_attention_backward_gb300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel_key, src_files):
+    """DRAM bytes per launch from the committed ncu summary, or None when the
+    kernel source changed since the counters were taken."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    e = d.get(kernel_key)
+    if not e or e.get("source_hash") != source_hash(*src_files):
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+def run_native(args):
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl", init_method="env://")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    import transformer_attention_backward_gb300 as abw
+    from transformer_attention_backward_gb300 import saved_forward
+    from transformer_attention_backward_gb300 import workloads as W
+    lib = abw.library()
+    stream = torch.cuda.current_stream()
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    def max_over_ranks(x):
+        if world == 1:
+            return x
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    # ------------------------------------------------------------ decode step
+    shape = W.DECODE_GQA
+    dinp = W.decode_inputs(shape, seed=W.SEED_BASE + 2)
+    rn = W.rmsnorm_inputs(*W.RMSNORM_DECODE, seed=W.SEED_BASE + 20)
+    host = {k: v.pin_memory() for k, v in dinp.items()}
+    host.update({"x": rn["x"].pin_memory(), "gamma": rn["gamma"].pin_memory(), "dy": rn["dy"].pin_memory()})
+    g = {k: v.to(dev) for k, v in host.items()}
+    dq = torch.empty_like(g["q"])
+    dk = torch.empty(g["k"].shape, dtype=torch.float32, device=dev)
+    dv = torch.empty_like(dk)
+    dx = torch.empty_like(g["x"])
+    step_bytes = decode_bytes() + rmsnorm_bytes(64, 2560)
+    dec_bytes = decode_bytes()
+
+    def step(evs=None):
+        if evs is not None:
+            evs[0].record(stream)
+        abw.attn_bwd_decode(g["q"], g["k"], g["v"], g["dout"], shape.scale, shape.rope_base, shape.q_pos,
+                            dq=dq, dk=dk, dv=dv, stream=stream)
+        if evs is not None:
+            evs[1].record(stream)
+        abw.rmsnorm_bwd(g["x"], g["gamma"], g["dy"], eps=rn["eps"], dx=dx, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    abw.device_check(stream)
+    barrier()
+    step_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    kern_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clocks:
+        t_start.record(stream)
+        for i in range(args.steps):
+            step_ev[i][0].record(stream)
+            step(kern_ev[i])
+            step_ev[i][1].record(stream)
+        t_end.record(stream)
+        torch.cuda.synchronize()
+    barrier()
+    abw.device_check(stream)
+    total_ms = max_over_ranks(t_start.elapsed_time(t_end))
+    ms_step = total_ms / args.steps
+    kern_ms = statistics.mean(a.elapsed_time(b) for a, b in kern_ev)
+    value = world * step_bytes / (ms_step * 1e-3) / 1e9
+    launches = 2 * args.steps
+
+    # ------------------------------------------------------------ end to end (host buffers)
+    hout = {"dq": torch.empty(dq.shape, dtype=dq.dtype, pin_memory=True),
+            "dk": torch.empty(dk.shape, dtype=dk.dtype, pin_memory=True),
+            "dv": torch.empty(dv.shape, dtype=dv.dtype, pin_memory=True),
+            "dx": torch.empty(dx.shape, dtype=dx.dtype, pin_memory=True)}
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = sum(t.numel() * t.element_size() for t in hout.values())
+
+    def e2e_step():
+        for k_ in host:
+            g[k_].copy_(host[k_], non_blocking=True)
+        step()
+        hout["dq"].copy_(dq, non_blocking=True)
+        hout["dk"].copy_(dk, non_blocking=True)
+        hout["dv"].copy_(dv, non_blocking=True)
+        hout["dx"].copy_(dx, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        e2e_step()
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1)) / args.steps
+    e2e_value = world * step_bytes / (e2e_ms * 1e-3) / 1e9
+    del g, dq, dk, dv, dx, hout
+    torch.cuda.empty_cache()
+
+    # ------------------------------------------------------------ causal T = 2048
+    causal = None
+    if not args.skip_causal:
+        cs = W.CAUSAL_2K
+        cin = {k: v.to(dev) for k, v in W.causal_inputs(cs, seed=W.SEED_BASE + 3).items()}
+        o, lse = saved_forward.causal_forward(cin["q"], cin["k"], cin["v"], cs.scale)
+        cq = torch.empty(cin["q"].shape, dtype=torch.float32, device=dev)
+        ck = torch.empty(cin["k"].shape, dtype=torch.float32, device=dev)
+        cv = torch.empty_like(ck)
+        ws = torch.empty(abw.attn_bwd_causal_workspace_bytes(cs.B, cs.T, cs.Hq, cs.D), dtype=torch.uint8, device=dev)
+
+        def cstep():
+            abw.attn_bwd_causal(cin["q"], cin["k"], cin["v"], o, cin["dout"], lse, cs.scale, cs.rope_base, 0,
+                                dq=cq, dk=ck, dv=cv, workspace=ws, stream=stream)
+
+        for _ in range(args.warmup):
+            cstep()
+        abw.device_check(stream)
+        barrier()
+        c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        csteps = max(1, args.steps)
+        with ClockSampler(local) as cclocks:
+            c0.record(stream)
+            for _ in range(csteps):
+                cstep()
+            c1.record(stream)
+            torch.cuda.synchronize()
+        barrier()
+        abw.device_check(stream)
+        cms = max_over_ranks(c0.elapsed_time(c1)) / csteps
+        flops = causal_flops(cs.B, cs.T, cs.Hq, cs.D)
+        ctf = world * flops / (cms * 1e-3) / 1e12
+        peaks, kind = load_peaks()
+        causal = {"workload": "causal_b4_h20_d128_t2048_bf16_rope1e4", "value": round(ctf, 3), "unit": "TFLOP/s",
+                  "ms_per_call": round(cms, 4), "flops_per_call": flops,
+                  "roofline": {"bound": "tensor", "achieved": round(ctf / world, 3),
+                               "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                               "frac": round(ctf / world / peaks["bf16_tflops"], 4), "traffic": None,
+                               "peak_kind": kind + " (burst)", "scope": "whole call"},
+                  "clocks": cclocks.summary()}
+        del cin, o, lse, cq, ck, cv, ws
+        torch.cuda.empty_cache()
+
+    peaks, kind = load_peaks()
+    achieved = dec_bytes / (kern_ms * 1e-3) / 1e9
+    roofline = {"bound": "hbm", "achieved": round(achieved, 2), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": round(achieved / peaks["hbm_gbs"], 4),
+                "traffic": recorded_traffic("decode_bwd_kernel", ["decode.cu", "abw_device.cuh"]),
+                "kernel": "decode_bwd_kernel", "bytes_per_launch": dec_bytes, "peak_kind": kind}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.skip_cpu:
+        n_units = 320
+        wall, frac = oracle_decode_time(n_units, cpu_cores())
+        cms = wall / frac * 1e3
+        cpu = {"value": round(step_bytes / (cms * 1e-3) / 1e9, 4), "unit": "GB/s", "cores": cpu_cores(),
+               "kind": "oracle",
+               "sample": "one full decode step (320 (batch, KV head) units + 64 RMSNorm rows), float64 numpy "
+                         f"oracle over {cpu_cores()} spawned processes, {wall:.2f} s"}
+
+    if rank == 0:
+        line = {
+            "metric": "attn_bwd_decode_gbps", "value": round(value, 3), "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": DECODE_WORKLOAD, "global_batch": 64 * world, "seq_len": 1024,
+                       "parallelism": f"replicas{world}", "l2": "inputs larger than L2 (505 MB per step)",
+                       "compute": "fp32 arithmetic on bf16 K/V, fp32 q/dout/gradients"},
+            "roofline": roofline,
+            "cpu_baseline": cpu,
+            "e2e": {"value": round(e2e_value, 3), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)},
+            "gpu_launches": launches,
+            "clocks": clocks.summary(),
+            "causal_t2048": causal,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["native", "reference"], default="native")
+    ap.add_argument("--skip-causal", action="store_true")
+    ap.add_argument("--skip-cpu", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "native":
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_native(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

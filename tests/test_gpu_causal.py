@@ -1,0 +1,114 @@
+"""GPU parity of attn_bwd_causal (and the 30-layer chain) against the float64
+oracle, through the C ABI.  bf16 inputs with fp32 accumulation: max relative
+error <= 2e-2 per output tensor.  At the full workload sizes the oracle
+recomputes a sample of whole (batch, KV head) units."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from tests.helpers import TOL_BF16, max_rel_err, to_np
+from transformer_attention_backward_gb300 import saved_forward
+from transformer_attention_backward_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def abw():
+    import transformer_attention_backward_gb300 as m
+    m.library()
+    return m
+
+
+def gpu_causal(abw, inp, shape):
+    g = {k: v.cuda() for k, v in inp.items()}
+    o, lse = saved_forward.causal_forward(g["q"], g["k"], g["v"], shape.scale)
+    dq, dk, dv = abw.attn_bwd_causal(g["q"], g["k"], g["v"], o, g["dout"], lse, shape.scale,
+                                     shape.rope_base, shape.pos0)
+    abw.device_check()
+    return dq, dk, dv
+
+
+def compare_units(inp, shape, dq, dk, dv, units):
+    q, k, v, do = (to_np(inp[n]) for n in ("q", "k", "v", "dout"))
+    rq, rk, rv = O.causal_backward(q, k, v, do, shape.scale, shape.rope_base, shape.pos0, kv_heads=units)
+    G = shape.Hq // shape.Hkv
+    errs = []
+    for b, j in units:
+        hs = slice(j * G, (j + 1) * G)
+        errs.append(max_rel_err(to_np(dq[b, :, hs]), rq[b, :, hs]))
+        errs.append(max_rel_err(to_np(dk[b, :, j]), rk[b, :, j]))
+        errs.append(max_rel_err(to_np(dv[b, :, j]), rv[b, :, j]))
+    return errs
+
+
+@pytest.mark.parametrize("shape", [
+    W.CausalShape(B=1, T=1, Hq=1, Hkv=1, D=128, rope_base=0.0),
+    W.CausalShape(B=2, T=130, Hq=4, Hkv=2, D=128, rope_base=10000.0),           # ragged tail, GQA
+    W.CausalShape(B=1, T=192, Hq=2, Hkv=2, D=128, rope_base=0.0),
+    W.CausalShape(B=1, T=300, Hq=3, Hkv=1, D=128, rope_base=500000.0, pos0=5),  # G = 3, offset positions
+    W.CausalShape(B=1, T=257, Hq=2, Hkv=1, D=128, rope_base=0.0, qk_mult=4.0),  # saturated softmax
+])
+def test_causal_small(abw, shape):
+    inp = W.causal_inputs(shape, seed=shape.T + shape.Hq)
+    dq, dk, dv = gpu_causal(abw, inp, shape)
+    units = [(b, j) for b in range(shape.B) for j in range(shape.Hkv)]
+    errs = compare_units(inp, shape, dq, dk, dv, units)
+    assert max(errs) <= TOL_BF16, errs
+
+
+def test_causal_t2048_sampled(abw):
+    """B = 4, H = 20, D = 128, T = 2048, RoPE base 1e4 on dq and dk."""
+    shape = W.CAUSAL_2K
+    inp = W.causal_inputs(shape, seed=W.SEED_BASE + 3)
+    dq, dk, dv = gpu_causal(abw, inp, shape)
+    errs = compare_units(inp, shape, dq, dk, dv, [(0, 0), (3, 19), (1, 7)])
+    assert max(errs) <= TOL_BF16, errs
+    assert all(torch.isfinite(t).all() for t in (dq, dk, dv))
+
+
+def test_causal_t8192_saturated_sampled(abw):
+    """B = 1, H = 32, T = 8192, Q and K x4 (softmax saturation), no RoPE."""
+    shape = W.CAUSAL_8K
+    inp = W.causal_inputs(shape, seed=W.SEED_BASE + 4)
+    dq, dk, dv = gpu_causal(abw, inp, shape)
+    errs = compare_units(inp, shape, dq, dk, dv, [(0, 0), (0, 31)])
+    assert max(errs) <= TOL_BF16, errs
+    # without RoPE, sum over keys of dK vanishes for every head
+    sk = dk.double().sum(1)
+    assert float(sk.abs().max()) <= 1e-3 * float(dk.double().abs().sum(1).max())
+
+
+def test_chain_30_layers_sampled(abw):
+    """30 layers in reverse: RMSNorm backward (bf16 dx becomes attention's
+    dOut), then causal attention backward with RoPE on dq/dk (GQA 20/5)."""
+    shape = W.CHAIN_LAYER
+    dh = W.chain_dhidden()
+    dh_g = dh.cuda()
+    results = {}
+    check_layers = (29, 13, 0)
+    for layer in reversed(range(W.CHAIN_LAYERS)):
+        inp = W.chain_layer_inputs(layer)
+        g = {k: v.cuda() for k, v in inp.items() if torch.is_tensor(v)}
+        dx = abw.rmsnorm_bwd(g["x"], g["gamma"], dh_g, eps=inp["eps"], dx_dtype=torch.bfloat16)
+        dout = dx.view(shape.B, shape.T, shape.Hq, shape.D)
+        o, lse = saved_forward.causal_forward(g["q"], g["k"], g["v"], shape.scale)
+        dq, dk, dv = abw.attn_bwd_causal(g["q"], g["k"], g["v"], o, dout, lse, shape.scale, shape.rope_base, 0)
+        if layer in check_layers:
+            results[layer] = (inp, dx.float().cpu(), dq.cpu(), dk.cpu(), dv.cpu())
+    abw.device_check()
+    for layer, (inp, dx, dq, dk, dv) in results.items():
+        units = [(0, 0), (1, 4)]
+        rdx, rq, rk, rv = O.chain_layer_backward(to_np(inp["x"]), to_np(inp["gamma"]), to_np(dh), to_np(inp["q"]),
+                                                 to_np(inp["k"]), to_np(inp["v"]), inp["eps"], shape.scale,
+                                                 shape.rope_base, kv_heads=units)
+        errs = [max_rel_err(to_np(dx), rdx)]
+        G = shape.Hq // shape.Hkv
+        for b, j in units:
+            hs = slice(j * G, (j + 1) * G)
+            errs += [max_rel_err(to_np(dq[b, :, hs]), rq[b, :, hs]), max_rel_err(to_np(dk[b, :, j]), rk[b, :, j]),
+                     max_rel_err(to_np(dv[b, :, j]), rv[b, :, j])]
+        assert max(errs) <= TOL_BF16, (layer, errs)

@@ -1,0 +1,48 @@
+// Internal host-side interface between the C ABI (api.cu) and the kernel
+// translation units.  Not installed; not part of the ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "abw_device.cuh"
+
+namespace abw {
+
+// Error word + wait limit for the current device (lazily resolved once per
+// device).  `err` is null if the symbol address could not be obtained.
+WaitCtl wait_ctl();
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no link
+// against libcuda).  Returns false and fills `why` on failure.
+bool encode_tiled(CUtensorMap *map, CUtensorMapDataType dt, uint32_t rank, const void *base,
+                  const uint64_t *dims, const uint64_t *strides_bytes, const uint32_t *box,
+                  CUtensorMapSwizzle swizzle, const char **why);
+
+// Launchers: validate nothing (api.cu has done it), enqueue, and return the
+// launch error.
+cudaError_t launch_softmax_bwd(const float *s, const float *dy, float *dx, int rows, int n,
+                               cudaStream_t st);
+cudaError_t launch_rope_bwd(const float *dy, float *dx, int B, int T, int H, int D, const float *theta,
+                            int pos0, double base, int interleaved, cudaStream_t st);
+cudaError_t launch_rmsnorm_bwd(const void *x, int x_bf16, const float *gamma, const float *dy, void *dx,
+                               int dx_bf16, int rows, int n, float eps, cudaStream_t st);
+
+// Returns cudaErrorNotSupported (and sets *why) when a shape has no kernel.
+cudaError_t launch_attn_bwd_decode(const float *q, const void *k, const void *v, const float *dout,
+                                   float *dq, float *dk, float *dv, int B, int Hq, int Hkv, int S, int D,
+                                   int kv_bf16, float scale, double rope_base, int q_pos,
+                                   const WaitCtl &w, cudaStream_t st, const char **why);
+
+size_t causal_workspace_bytes(int B, int T, int Hq, int D);
+cudaError_t launch_attn_bwd_causal(const void *q, const void *k, const void *v, const void *o,
+                                   const void *dout, const float *lse, float *dq, float *dk, float *dv,
+                                   int B, int T, int Hq, int Hkv, int D, float scale, double rope_base,
+                                   int pos0, void *ws, size_t ws_bytes, const WaitCtl &w,
+                                   cudaStream_t st, const char **why);
+
+cudaError_t launch_selftest_wait(const WaitCtl &w, cudaStream_t st);
+
+}  // namespace abw

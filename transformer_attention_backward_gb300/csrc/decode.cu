@@ -1,0 +1,519 @@
+// Decode-style attention backward: one query per sequence against a KV cache,
+// grouped KV heads, RoPE backward fused on dq.
+//
+// Spec: "Hesper.Training.VerifiedBackward", section Attention (full
+// single-head) -- attentionBackwardQ (dAttn = dOut V^T, softmax backward,
+// dQ = scale dScores K), attentionBackwardV (dV[s] = attn[s] dOut) -- and
+// section Scaled Dot-Product (dk = scale dScore q), summed over the query
+// heads that share a KV head; section RoPE (ropeBackward) on dq.
+//
+// Design (GB300): the work is bound by HBM -- K and V are read once (bf16) and
+// dK, dV are written once (fp32).  One (batch, KV head) unit is split over a
+// thread-block cluster of up to 8 CTAs, each owning a contiguous chunk of
+// keys.  K/V tiles of 64 rows arrive by TMA into a two-stage shared-memory
+// ring.  Per key the CTA keeps only two scalars per query head (the score and
+// dP) in shared memory; the softmax normaliser, delta = sum P dP and the dq
+// partial sums sum_j e_j dP_j K_j and sum_j e_j K_j are carried as running
+// (max-rescaled) partials, the same online-softmax merge Hesper's split-KV
+// flash attention uses for its tile partials (pull request #1, "Phase 2:
+// Merge partial results").  The cluster merges the per-CTA partials through
+// distributed shared memory; every CTA then writes its dK/dV rows straight
+// from the two scalars per head with streaming 16-byte stores, and rank 0
+// finishes dq (with the inverse rotation) -- so no byte of K/V is read twice
+// and nothing goes through a global scratch buffer.
+#include <cooperative_groups.h>
+#include <math.h>
+
+#include "abw_host.h"
+
+namespace cg = cooperative_groups;
+
+namespace abw {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+constexpr int kTile = 64;       // K/V rows per TMA tile
+constexpr int kStages = 2;      // TMA ring depth
+constexpr int kMaxCluster = 8;  // portable cluster size
+constexpr int kMaxG = 8;
+
+struct DecodeParams {
+  const float *q;
+  const float *dout;
+  float *dq;
+  float *dk;
+  float *dv;
+  int B, Hq, Hkv, S, D, G;
+  int chunk;      // keys per CTA (multiple of kTile)
+  int ncl;        // CTAs per (b, kv head) == cluster size
+  int lpr_log2;   // log2(lanes per K/V row), 16 bytes per lane
+  int rowbytes;   // D * sizeof(kv)
+  float scale;
+  int rope;
+  float rcos[128];
+  float rsin[128];
+  WaitCtl wait;
+};
+
+// Byte offsets of the dynamic shared-memory regions (same in every CTA).
+struct Layout {
+  int kv, sbuf, pbuf, etile, edp, xm, xl, xc, xa, xb, glob, alpha, runm, runl, runc, rsc, dqs, bars, total;
+  __host__ __device__ static int up(int x, int a) { return (x + a - 1) / a * a; }
+  __host__ __device__ Layout(int G, int D, int chunk, int rowbytes) {
+    int o = 0;
+    kv = o;    o += kStages * 2 * kTile * rowbytes;   o = up(o, 16);
+    sbuf = o;  o += G * chunk * 4;
+    pbuf = o;  o += G * chunk * 4;
+    etile = o; o += G * kTile * 4;
+    edp = o;   o += G * kTile * 4;
+    xm = o;    o += kMaxG * 4;
+    xl = o;    o += kMaxG * 4;
+    xc = o;    o += kMaxG * 4;
+    xa = o;    o += G * D * 4;
+    xb = o;    o += G * D * 4;    o = up(o, 16);
+    glob = o;  o += kMaxG * 16;
+    alpha = o; o += kMaxG * 4;
+    runm = o;  o += kMaxG * 4;
+    runl = o;  o += kMaxG * 4;
+    runc = o;  o += kMaxG * 4;
+    rsc = o;   o += kMaxCluster * kMaxG * 4;
+    dqs = o;   o += G * D * 4;    o = up(o, 16);
+    bars = o;  o += kStages * 8;
+    total = up(o, 16);
+  }
+};
+
+template <typename KV>
+__device__ __forceinline__ void load_row16(const unsigned char *p, float (&f)[16 / sizeof(KV)]);
+
+template <>
+__device__ __forceinline__ void load_row16<__nv_bfloat16>(const unsigned char *p, float (&f)[8]) {
+  const uint4 u = *reinterpret_cast<const uint4 *>(p);
+  f[0] = bf16_lo(u.x); f[1] = bf16_hi(u.x);
+  f[2] = bf16_lo(u.y); f[3] = bf16_hi(u.y);
+  f[4] = bf16_lo(u.z); f[5] = bf16_hi(u.z);
+  f[6] = bf16_lo(u.w); f[7] = bf16_hi(u.w);
+}
+
+template <>
+__device__ __forceinline__ void load_row16<float>(const unsigned char *p, float (&f)[4]) {
+  const float4 u = *reinterpret_cast<const float4 *>(p);
+  f[0] = u.x; f[1] = u.y; f[2] = u.z; f[3] = u.w;
+}
+
+template <typename KV>
+__device__ __forceinline__ float load_elem(const unsigned char *row, int d);
+template <>
+__device__ __forceinline__ float load_elem<__nv_bfloat16>(const unsigned char *row, int d) {
+  return __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(row)[d]);
+}
+template <>
+__device__ __forceinline__ float load_elem<float>(const unsigned char *row, int d) {
+  return reinterpret_cast<const float *>(row)[d];
+}
+
+template <typename KV, int GMAX>
+__global__ void __launch_bounds__(kThreads, 1)
+    decode_bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                      const __grid_constant__ DecodeParams p) {
+  constexpr int EPL = 16 / sizeof(KV);                           // elements per lane in the dot phase
+  constexpr int NACC = (GMAX * (512 / static_cast<int>(sizeof(KV))) + kThreads - 1) / kThreads;  // (h, d) pairs per thread
+  cg::cluster_group cluster = cg::this_cluster();
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char *smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+
+  const int G = p.G, D = p.D;
+  const Layout L(G, D, p.chunk, p.rowbytes);
+  const int rank = static_cast<int>(cluster.block_rank());
+  const int kvh = blockIdx.y, b = blockIdx.z;
+  const int key0 = rank * p.chunk;
+  const int nkeys = min(p.chunk, p.S - key0);   // >= 1 by construction of chunk / ncl
+  const int ntiles = (nkeys + kTile - 1) / kTile;
+  const uint32_t tile_bytes = static_cast<uint32_t>(kTile * p.rowbytes);
+
+  float *sbuf = reinterpret_cast<float *>(smem + L.sbuf);
+  float *pbuf = reinterpret_cast<float *>(smem + L.pbuf);
+  float *etile = reinterpret_cast<float *>(smem + L.etile);
+  float *edp = reinterpret_cast<float *>(smem + L.edp);
+  float *xm = reinterpret_cast<float *>(smem + L.xm);
+  float *xl = reinterpret_cast<float *>(smem + L.xl);
+  float *xc = reinterpret_cast<float *>(smem + L.xc);
+  float *xa = reinterpret_cast<float *>(smem + L.xa);
+  float *xb = reinterpret_cast<float *>(smem + L.xb);
+  float4 *glob = reinterpret_cast<float4 *>(smem + L.glob);
+  float *alph = reinterpret_cast<float *>(smem + L.alpha);
+  float *runm = reinterpret_cast<float *>(smem + L.runm);
+  float *runl = reinterpret_cast<float *>(smem + L.runl);
+  float *runc = reinterpret_cast<float *>(smem + L.runc);
+  float *rsc = reinterpret_cast<float *>(smem + L.rsc);
+  float *dqs = reinterpret_cast<float *>(smem + L.dqs);
+  const uint32_t bar0 = smem_u32(smem + L.bars);
+  const uint32_t kv0 = smem_u32(smem + L.kv);
+
+  auto kv_smem = [&](int stage, int which) -> unsigned char * {
+    return smem + L.kv + (stage * 2 + which) * kTile * p.rowbytes;
+  };
+  auto issue = [&](int t) {
+    const int st = t % kStages;
+    const uint32_t bar = bar0 + st * 8;
+    mbar_arrive_expect_tx(bar, 2 * tile_bytes);
+    tma_load_4d(kv0 + (st * 2 + 0) * tile_bytes, &tmK, 0, kvh, key0 + t * kTile, b, bar);
+    tma_load_4d(kv0 + (st * 2 + 1) * tile_bytes, &tmV, 0, kvh, key0 + t * kTile, b, bar);
+  };
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid == 0) {
+    prefetch_tensormap(&tmK);
+    prefetch_tensormap(&tmV);
+    for (int s = 0; s < kStages; ++s) mbar_init(bar0 + s * 8, 1);
+    fence_barrier_init();
+  }
+  if (tid < kMaxG) {
+    runm[tid] = -INFINITY;
+    runl[tid] = 0.f;
+    runc[tid] = 0.f;
+  }
+  __syncthreads();
+  if (tid == 0)
+    for (int t = 0; t < min(kStages, ntiles); ++t) issue(t);
+
+  // ---- per-lane slices of scale*q and dout for the dot products
+  const int lpr = 1 << p.lpr_log2;
+  const int sub = lane & (lpr - 1);
+  const int rgrp = lane >> p.lpr_log2;
+  const int rows_per_warp = 32 >> p.lpr_log2;
+  const int rows_per_step = kWarps * rows_per_warp;
+  const bool lane_on = sub * 16 < p.rowbytes;
+  const size_t qrow0 = (static_cast<size_t>(b) * p.Hq + static_cast<size_t>(kvh) * G) * D;
+  float qr[GMAX][EPL], dr[GMAX][EPL];
+#pragma unroll
+  for (int h = 0; h < GMAX; ++h)
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) {
+      const int d = sub * EPL + e;
+      const bool on = h < G && lane_on;
+      qr[h][e] = on ? p.q[qrow0 + static_cast<size_t>(h) * D + d] * p.scale : 0.f;
+      dr[h][e] = on ? p.dout[qrow0 + static_cast<size_t>(h) * D + d] : 0.f;
+    }
+
+  float accA[NACC], accB[NACC];
+#pragma unroll
+  for (int k = 0; k < NACC; ++k) accA[k] = accB[k] = 0.f;
+
+  // ======================= phase 1: stream the chunk =======================
+  for (int t = 0; t < ntiles; ++t) {
+    const int st = t % kStages;
+    mbar_wait_or_flag(bar0 + st * 8, (t / kStages) & 1, p.wait);
+    const unsigned char *Kt = kv_smem(st, 0);
+    const unsigned char *Vt = kv_smem(st, 1);
+    const int rows_valid = min(kTile, nkeys - t * kTile);
+    const int jt = t * kTile;
+
+    // (a) s_hj = (scale q_h) . K_j and dP_hj = dout_h . V_j
+    for (int r = warp * rows_per_warp + rgrp; r < kTile; r += rows_per_step) {
+      float kf[EPL], vf[EPL];
+      if (lane_on) {
+        load_row16<KV>(Kt + r * p.rowbytes + sub * 16, kf);
+        load_row16<KV>(Vt + r * p.rowbytes + sub * 16, vf);
+      } else {
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) kf[e] = vf[e] = 0.f;
+      }
+      float sp[GMAX], pp[GMAX];
+#pragma unroll
+      for (int h = 0; h < GMAX; ++h) {
+        float a = 0.f, c = 0.f;
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) {
+          a = fmaf(qr[h][e], kf[e], a);
+          c = fmaf(dr[h][e], vf[e], c);
+        }
+        sp[h] = a;
+        pp[h] = c;
+      }
+      for (int off = lpr >> 1; off > 0; off >>= 1) {
+#pragma unroll
+        for (int h = 0; h < GMAX; ++h) {
+          sp[h] += __shfl_xor_sync(0xffffffffu, sp[h], off);
+          pp[h] += __shfl_xor_sync(0xffffffffu, pp[h], off);
+        }
+      }
+      if (sub == 0 && r < rows_valid) {
+#pragma unroll
+        for (int h = 0; h < GMAX; ++h)
+          if (h < G) {
+            sbuf[h * p.chunk + jt + r] = sp[h];
+            pbuf[h * p.chunk + jt + r] = pp[h];
+          }
+      }
+    }
+    __syncthreads();
+
+    // (b) running max / normaliser / sum e dP per head (warp h)
+    if (warp < G) {
+      const int h = warp;
+      const float s0 = lane < rows_valid ? sbuf[h * p.chunk + jt + lane] : -INFINITY;
+      const float s1 = lane + 32 < rows_valid ? sbuf[h * p.chunk + jt + lane + 32] : -INFINITY;
+      const float d0 = lane < rows_valid ? pbuf[h * p.chunk + jt + lane] : 0.f;
+      const float d1 = lane + 32 < rows_valid ? pbuf[h * p.chunk + jt + lane + 32] : 0.f;
+      const float mt = warp_max(fmaxf(s0, s1));
+      const float m_old = runm[h];
+      const float m_new = fmaxf(m_old, mt);
+      const float a = expf(m_old - m_new);   // 0 on the first tile
+      const float e0 = lane < rows_valid ? expf(s0 - m_new) : 0.f;
+      const float e1 = lane + 32 < rows_valid ? expf(s1 - m_new) : 0.f;
+      etile[h * kTile + lane] = e0;
+      etile[h * kTile + lane + 32] = e1;
+      edp[h * kTile + lane] = e0 * d0;
+      edp[h * kTile + lane + 32] = e1 * d1;
+      const float ls = warp_sum(e0 + e1);
+      const float csum = warp_sum(e0 * d0 + e1 * d1);
+      if (lane == 0) {
+        runl[h] = runl[h] * a + ls;
+        runc[h] = runc[h] * a + csum;
+        runm[h] = m_new;
+        alph[h] = a;
+      }
+    }
+    __syncthreads();
+
+    // (c) dq partials: A_h[d] = sum_j e_hj dP_hj K_jd, B_h[d] = sum_j e_hj K_jd
+#pragma unroll
+    for (int k = 0; k < NACC; ++k) {
+      const int idx = tid + kThreads * k;
+      if (idx < G * D) {
+        const int h = idx / D, d = idx - h * D;
+        float a = accA[k] * alph[h], c = accB[k] * alph[h];
+        const float *et = etile + h * kTile;
+        const float *ed = edp + h * kTile;
+        for (int r = 0; r < rows_valid; ++r) {
+          const float kv = load_elem<KV>(Kt + r * p.rowbytes, d);
+          a = fmaf(ed[r], kv, a);
+          c = fmaf(et[r], kv, c);
+        }
+        accA[k] = a;
+        accB[k] = c;
+      }
+    }
+    __syncthreads();
+    if (tid == 0 && t + kStages < ntiles) {
+      fence_proxy_async_smem();
+      issue(t + kStages);
+    }
+  }
+
+  // ======================= publish partials, merge across the cluster ======
+  if (tid < G) {
+    xm[tid] = runm[tid];
+    xl[tid] = runl[tid];
+    xc[tid] = runc[tid];
+  }
+#pragma unroll
+  for (int k = 0; k < NACC; ++k) {
+    const int idx = tid + kThreads * k;
+    if (idx < G * D) {
+      xa[idx] = accA[k];
+      xb[idx] = accB[k];
+    }
+  }
+  cluster.sync();
+
+  if (tid < G) {
+    const int h = tid;
+    float M = -INFINITY;
+    for (int r = 0; r < p.ncl; ++r) M = fmaxf(M, cluster.map_shared_rank(xm, r)[h]);
+    float Ls = 0.f, Cs = 0.f;
+    for (int r = 0; r < p.ncl; ++r) {
+      const float w = expf(cluster.map_shared_rank(xm, r)[h] - M);
+      Ls += cluster.map_shared_rank(xl, r)[h] * w;
+      Cs += cluster.map_shared_rank(xc, r)[h] * w;
+      rsc[r * kMaxG + h] = w;
+    }
+    glob[h] = make_float4(M, 1.f / Ls, Cs / Ls, 0.f);
+  }
+  __syncthreads();
+
+  // P and dS of this CTA's keys, in place of the score and dP
+  for (int i = tid; i < G * nkeys; i += kThreads) {
+    const int h = i / nkeys, j = i - h * nkeys;
+    const float4 g = glob[h];
+    const float P = expf(sbuf[h * p.chunk + j] - g.x) * g.y;
+    sbuf[h * p.chunk + j] = P;
+    pbuf[h * p.chunk + j] = P * (pbuf[h * p.chunk + j] - g.z);
+  }
+  __syncthreads();
+
+  // ======================= phase 2: dK / dV rows ===========================
+  {
+    const int F4 = D >> 2;                                  // float4 per output row
+    int olog = 0;
+    while ((1 << olog) < F4 && olog < 5) ++olog;
+    const int olpr = 1 << olog;                             // lanes per row (<= 32)
+    const int osub = lane & (olpr - 1), ogrp = lane >> olog;
+    const int orows_w = 32 >> olog;
+    const int npass = (F4 + 31) / 32;
+    for (int pass = 0; pass < npass; ++pass) {
+      const int f = osub + 32 * pass;
+      const bool on = f < F4;
+      float4 qo[GMAX], go[GMAX];
+#pragma unroll
+      for (int h = 0; h < GMAX; ++h) {
+        if (on && h < G) {
+          qo[h] = *reinterpret_cast<const float4 *>(p.q + qrow0 + static_cast<size_t>(h) * D + 4 * f);
+          go[h] = *reinterpret_cast<const float4 *>(p.dout + qrow0 + static_cast<size_t>(h) * D + 4 * f);
+        } else {
+          qo[h] = go[h] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+      }
+      for (int j = warp * orows_w + ogrp; j < nkeys; j += kWarps * orows_w) {
+        float4 ak = make_float4(0.f, 0.f, 0.f, 0.f), av = ak;
+#pragma unroll
+        for (int h = 0; h < GMAX; ++h) {
+          if (h < G) {
+            const float P = sbuf[h * p.chunk + j], dS = pbuf[h * p.chunk + j];
+            ak.x = fmaf(dS, qo[h].x, ak.x); ak.y = fmaf(dS, qo[h].y, ak.y);
+            ak.z = fmaf(dS, qo[h].z, ak.z); ak.w = fmaf(dS, qo[h].w, ak.w);
+            av.x = fmaf(P, go[h].x, av.x);  av.y = fmaf(P, go[h].y, av.y);
+            av.z = fmaf(P, go[h].z, av.z);  av.w = fmaf(P, go[h].w, av.w);
+          }
+        }
+        ak.x *= p.scale; ak.y *= p.scale; ak.z *= p.scale; ak.w *= p.scale;
+        if (on) {
+          const size_t o = ((static_cast<size_t>(b) * p.S + key0 + j) * p.Hkv + kvh) * D + 4 * f;
+          st_cs_f4(p.dk + o, ak);
+          st_cs_f4(p.dv + o, av);
+        }
+      }
+    }
+  }
+
+  // ======================= dq on rank 0 ====================================
+  if (rank == 0) {
+    for (int idx = tid; idx < G * D; idx += kThreads) {
+      const int h = idx / D;
+      float sa = 0.f, sb = 0.f;
+      for (int r = 0; r < p.ncl; ++r) {
+        const float w = rsc[r * kMaxG + h];
+        sa = fmaf(w, cluster.map_shared_rank(xa, r)[idx], sa);
+        sb = fmaf(w, cluster.map_shared_rank(xb, r)[idx], sb);
+      }
+      const float4 g = glob[h];
+      dqs[idx] = p.scale * (sa - g.z * sb) * g.y;
+    }
+    __syncthreads();
+    const int half = D >> 1;
+    for (int i = tid; i < G * half; i += kThreads) {
+      const int h = i / half, pi = i - h * half;
+      const float y0 = dqs[h * D + 2 * pi], y1 = dqs[h * D + 2 * pi + 1];
+      float z0 = y0, z1 = y1;
+      if (p.rope) {
+        const float c = p.rcos[pi], s = p.rsin[pi];
+        z0 = y0 * c + y1 * s;
+        z1 = -y0 * s + y1 * c;
+      }
+      float *out = p.dq + qrow0 + static_cast<size_t>(h) * D + 2 * pi;
+      out[0] = z0;
+      out[1] = z1;
+    }
+  }
+  cluster.sync();   // peers' shared memory stays alive until rank 0 has read it
+}
+
+template <typename KV, int GMAX>
+cudaError_t launch_typed(const CUtensorMap &tk, const CUtensorMap &tv, const DecodeParams &p, int smem,
+                         cudaStream_t st) {
+  auto kern = decode_bwd_kernel<KV, GMAX>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.ncl, p.Hkv, p.B);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = p.ncl;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, tk, tv, p);
+}
+
+template <typename KV>
+cudaError_t launch_g(int gmax, const CUtensorMap &tk, const CUtensorMap &tv, const DecodeParams &p, int smem,
+                     cudaStream_t st) {
+  switch (gmax) {
+    case 1: return launch_typed<KV, 1>(tk, tv, p, smem, st);
+    case 2: return launch_typed<KV, 2>(tk, tv, p, smem, st);
+    case 4: return launch_typed<KV, 4>(tk, tv, p, smem, st);
+    default: return launch_typed<KV, 8>(tk, tv, p, smem, st);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_attn_bwd_decode(const float *q, const void *k, const void *v, const float *dout, float *dq,
+                                   float *dk, float *dv, int B, int Hq, int Hkv, int S, int D, int kv_bf16,
+                                   float scale, double rope_base, int q_pos, const WaitCtl &w, cudaStream_t st,
+                                   const char **why) {
+  const int es = kv_bf16 ? 2 : 4;
+  const int rowbytes = D * es;
+  int lpr_log2 = 0;
+  while ((16 << lpr_log2) < rowbytes) ++lpr_log2;   // lanes per row = ceil to a power of two
+  if (lpr_log2 > 5) {
+    *why = "row too wide";
+    return cudaErrorNotSupported;
+  }
+  if (Hkv > 65535 || B > 65535) {
+    *why = "B or Hkv > 65535";
+    return cudaErrorNotSupported;
+  }
+  const int G = Hq / Hkv;
+  const int gmax = G <= 1 ? 1 : G <= 2 ? 2 : G <= 4 ? 4 : 8;
+  const int tiles = (S + kTile - 1) / kTile;
+  int ncl = tiles < kMaxCluster ? tiles : kMaxCluster;
+  const int chunk = ((tiles + ncl - 1) / ncl) * kTile;
+  ncl = (S + chunk - 1) / chunk;                 // every CTA owns at least one key
+  const Layout L(G, D, chunk, rowbytes);
+  const int smem = L.total + 1024;               // + alignment slack
+  if (smem > 227 * 1024) {
+    *why = "KV length too long for the per-CTA score buffers";
+    return cudaErrorNotSupported;
+  }
+
+  DecodeParams p;
+  p.q = q; p.dout = dout; p.dq = dq; p.dk = dk; p.dv = dv;
+  p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.S = S; p.D = D; p.G = G;
+  p.chunk = chunk; p.ncl = ncl; p.lpr_log2 = lpr_log2; p.rowbytes = rowbytes;
+  p.scale = scale;
+  p.rope = rope_base > 0.0 && q_pos >= 0;
+  for (int i = 0; i < 128; ++i) {
+    if (p.rope && i < D / 2) {
+      const double th = static_cast<double>(q_pos) * pow(rope_base, -2.0 * i / D);
+      p.rcos[i] = static_cast<float>(cos(th));
+      p.rsin[i] = static_cast<float>(sin(th));
+    } else {
+      p.rcos[i] = 1.f;
+      p.rsin[i] = 0.f;
+    }
+  }
+  p.wait = w;
+
+  CUtensorMap tk, tv;
+  const uint64_t dims[4] = {static_cast<uint64_t>(D), static_cast<uint64_t>(Hkv), static_cast<uint64_t>(S),
+                            static_cast<uint64_t>(B)};
+  const uint64_t strides[3] = {static_cast<uint64_t>(rowbytes), static_cast<uint64_t>(Hkv) * rowbytes,
+                               static_cast<uint64_t>(S) * Hkv * rowbytes};
+  const uint32_t box[4] = {static_cast<uint32_t>(D), 1, kTile, 1};
+  const CUtensorMapDataType dt = kv_bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+  if (!encode_tiled(&tk, dt, 4, k, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE, why) ||
+      !encode_tiled(&tv, dt, 4, v, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE, why))
+    return cudaErrorInvalidValue;
+
+  return kv_bf16 ? launch_g<__nv_bfloat16>(gmax, tk, tv, p, smem, st)
+                 : launch_g<float>(gmax, tk, tv, p, smem, st);
+}
+
+}  // namespace abw
