@@ -81,7 +81,10 @@ def test_decode_shapes(abw, shape):
 def test_decode_one_key_closed_form(abw):
     shape = W.DecodeShape(B=2, Hq=4, Hkv=2, S=1, D=64, kv_dtype=torch.float32)
     dq, dk, dv, inp = run_and_compare(abw, shape, seed=3)
-    assert float(dq.abs().max()) == 0.0 and float(dk.abs().max()) == 0.0
+    # dS = P (dP - delta) is exactly 0; dq = scale (A - delta B) / L cancels to
+    # fp32 rounding of one product (|dP K| ~ 10)
+    assert float(dk.abs().max()) == 0.0
+    assert float(dq.abs().max()) < 1e-5
     dsum = inp["dout"].reshape(2, 2, 2, 64).sum(2)   # sum over the group's heads
     assert torch.allclose(dv.cpu()[:, 0], dsum, atol=1e-6)
 

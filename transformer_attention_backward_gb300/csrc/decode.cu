@@ -47,7 +47,8 @@ struct DecodeParams {
   int B, Hq, Hkv, S, D, G;
   int chunk;      // keys per CTA (multiple of kTile)
   int ncl;        // CTAs per (b, kv head) == cluster size
-  int lpr_log2;   // log2(lanes per K/V row), 16 bytes per lane
+  int lpr_log2;   // log2(lanes per K/V row) in the dot phase
+  int rs_log2;    // log2(row splits) of the dq partial sums
   int rowbytes;   // D * sizeof(kv)
   float scale;
   int rope;
@@ -58,11 +59,13 @@ struct DecodeParams {
 
 // Byte offsets of the dynamic shared-memory regions (same in every CTA).
 struct Layout {
-  int kv, sbuf, pbuf, etile, edp, xm, xl, xc, xa, xb, glob, alpha, runm, runl, runc, rsc, dqs, bars, total;
+  int kv, sbuf, pbuf, etile, edp, xm, xl, xc, xa, xb, glob, alpha, runm, runl, runc, rstat, rsc, bars, total;
   __host__ __device__ static int up(int x, int a) { return (x + a - 1) / a * a; }
-  __host__ __device__ Layout(int G, int D, int chunk, int rowbytes) {
+  __host__ __device__ Layout(int G, int D, int chunk, int rowbytes, int rs) {
     int o = 0;
-    kv = o;    o += kStages * 2 * kTile * rowbytes;   o = up(o, 16);
+    const int tiles = kStages * 2 * kTile * rowbytes;
+    const int scratch = 2 * rs * G * D * 4;   // row-split dq partials, after the tile loop
+    kv = o;    o += tiles > scratch ? tiles : scratch;   o = up(o, 16);
     sbuf = o;  o += G * chunk * 4;
     pbuf = o;  o += G * chunk * 4;
     etile = o; o += G * kTile * 4;
@@ -73,58 +76,108 @@ struct Layout {
     xa = o;    o += G * D * 4;
     xb = o;    o += G * D * 4;    o = up(o, 16);
     glob = o;  o += kMaxG * 16;
+    rstat = o; o += kMaxCluster * kMaxG * 16;
     alpha = o; o += kMaxG * 4;
     runm = o;  o += kMaxG * 4;
     runl = o;  o += kMaxG * 4;
     runc = o;  o += kMaxG * 4;
-    rsc = o;   o += kMaxCluster * kMaxG * 4;
-    dqs = o;   o += G * D * 4;    o = up(o, 16);
+    rsc = o;   o += kMaxCluster * kMaxG * 4;  o = up(o, 16);
     bars = o;  o += kStages * 8;
     total = up(o, 16);
   }
 };
 
-template <typename KV>
-__device__ __forceinline__ void load_row16(const unsigned char *p, float (&f)[16 / sizeof(KV)]);
-
+// Loads EPL consecutive elements (8 or 16 bytes) of a K/V row as floats.
+template <typename KV, int GB>
+struct Gran;
 template <>
-__device__ __forceinline__ void load_row16<__nv_bfloat16>(const unsigned char *p, float (&f)[8]) {
-  const uint4 u = *reinterpret_cast<const uint4 *>(p);
-  f[0] = bf16_lo(u.x); f[1] = bf16_hi(u.x);
-  f[2] = bf16_lo(u.y); f[3] = bf16_hi(u.y);
-  f[4] = bf16_lo(u.z); f[5] = bf16_hi(u.z);
-  f[6] = bf16_lo(u.w); f[7] = bf16_hi(u.w);
+struct Gran<__nv_bfloat16, 8> {
+  static constexpr int EPL = 4;
+  __device__ static void load(const unsigned char *p, float (&f)[4]) {
+    const uint2 u = *reinterpret_cast<const uint2 *>(p);
+    f[0] = bf16_lo(u.x); f[1] = bf16_hi(u.x); f[2] = bf16_lo(u.y); f[3] = bf16_hi(u.y);
+  }
+};
+template <>
+struct Gran<__nv_bfloat16, 16> {
+  static constexpr int EPL = 8;
+  __device__ static void load(const unsigned char *p, float (&f)[8]) {
+    const uint4 u = *reinterpret_cast<const uint4 *>(p);
+    f[0] = bf16_lo(u.x); f[1] = bf16_hi(u.x); f[2] = bf16_lo(u.y); f[3] = bf16_hi(u.y);
+    f[4] = bf16_lo(u.z); f[5] = bf16_hi(u.z); f[6] = bf16_lo(u.w); f[7] = bf16_hi(u.w);
+  }
+};
+template <>
+struct Gran<float, 8> {
+  static constexpr int EPL = 2;
+  __device__ static void load(const unsigned char *p, float (&f)[2]) {
+    const float2 u = *reinterpret_cast<const float2 *>(p);
+    f[0] = u.x; f[1] = u.y;
+  }
+};
+template <>
+struct Gran<float, 16> {
+  static constexpr int EPL = 4;
+  __device__ static void load(const unsigned char *p, float (&f)[4]) {
+    const float4 u = *reinterpret_cast<const float4 *>(p);
+    f[0] = u.x; f[1] = u.y; f[2] = u.z; f[3] = u.w;
+  }
+};
+
+// Four consecutive row elements starting at element d (d % 4 == 0).
+__device__ __forceinline__ float4 load4(const unsigned char *row, int d, __nv_bfloat16 *) {
+  const uint2 u = *reinterpret_cast<const uint2 *>(row + 2 * d);
+  return make_float4(bf16_lo(u.x), bf16_hi(u.x), bf16_lo(u.y), bf16_hi(u.y));
+}
+__device__ __forceinline__ float4 load4(const unsigned char *row, int d, float *) {
+  return *reinterpret_cast<const float4 *>(row + 4 * d);
 }
 
-template <>
-__device__ __forceinline__ void load_row16<float>(const unsigned char *p, float (&f)[4]) {
-  const float4 u = *reinterpret_cast<const float4 *>(p);
-  f[0] = u.x; f[1] = u.y; f[2] = u.z; f[3] = u.w;
+// Sums NV values over an aligned group of `lpr` lanes (a power of two) while
+// spreading them out: each exchange step halves the values a lane keeps, so
+// the group needs log2(NV) + log2(lpr / NV) shuffles per value set instead of
+// NV * log2(lpr).  On return lane l holds the group sums of values
+// idx0 .. idx0 + nf - 1 in v[0 .. nf).
+template <int NV>
+__device__ __forceinline__ void reduce_scatter(float (&v)[NV], int lpr, int lane, int &idx0, int &nf) {
+  int o = lpr >> 1;
+  idx0 = 0;
+  nf = NV;
+#pragma unroll
+  for (int s = 0; (NV >> s) > 1; ++s) {
+    if (o == 0) break;
+    constexpr int dummy = 0;
+    (void)dummy;
+    const int h = NV >> (s + 1);
+    const bool up = (lane & o) != 0;
+#pragma unroll
+    for (int i = 0; i < (NV >> (s + 1)); ++i) {
+      const float send = up ? v[i] : v[i + h];
+      const float keep = up ? v[i + h] : v[i];
+      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+    }
+    if (up) idx0 += h;
+    nf = h;
+    o >>= 1;
+  }
+  for (; o > 0; o >>= 1) v[0] += __shfl_xor_sync(0xffffffffu, v[0], o);
 }
 
-template <typename KV>
-__device__ __forceinline__ float load_elem(const unsigned char *row, int d);
-template <>
-__device__ __forceinline__ float load_elem<__nv_bfloat16>(const unsigned char *row, int d) {
-  return __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(row)[d]);
-}
-template <>
-__device__ __forceinline__ float load_elem<float>(const unsigned char *row, int d) {
-  return reinterpret_cast<const float *>(row)[d];
-}
-
-template <typename KV, int GMAX>
-__global__ void __launch_bounds__(kThreads, 1)
+template <typename KV, int GMAX, int GB>
+__global__ void __launch_bounds__(kThreads, 2)
     decode_bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                       const __grid_constant__ DecodeParams p) {
-  constexpr int EPL = 16 / sizeof(KV);                           // elements per lane in the dot phase
-  constexpr int NACC = (GMAX * (512 / static_cast<int>(sizeof(KV))) + kThreads - 1) / kThreads;  // (h, d) pairs per thread
+  using GR = Gran<KV, GB>;
+  constexpr int EPL = GR::EPL;                 // elements per lane in the dot phase
+  constexpr int NV = 2 * GMAX;                 // per-row values: s_h and dP_h
+  constexpr int NIT = (GMAX * (512 / static_cast<int>(sizeof(KV))) / 4 + kThreads - 1) / kThreads;
   cg::cluster_group cluster = cg::this_cluster();
   extern __shared__ unsigned char smem_raw[];
   unsigned char *smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
 
   const int G = p.G, D = p.D;
-  const Layout L(G, D, p.chunk, p.rowbytes);
+  const int RS = 1 << p.rs_log2;
+  const Layout L(G, D, p.chunk, p.rowbytes, RS);
   const int rank = static_cast<int>(cluster.block_rank());
   const int kvh = blockIdx.y, b = blockIdx.z;
   const int key0 = rank * p.chunk;
@@ -142,18 +195,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   float *xa = reinterpret_cast<float *>(smem + L.xa);
   float *xb = reinterpret_cast<float *>(smem + L.xb);
   float4 *glob = reinterpret_cast<float4 *>(smem + L.glob);
+  float4 *rstat = reinterpret_cast<float4 *>(smem + L.rstat);
   float *alph = reinterpret_cast<float *>(smem + L.alpha);
   float *runm = reinterpret_cast<float *>(smem + L.runm);
   float *runl = reinterpret_cast<float *>(smem + L.runl);
   float *runc = reinterpret_cast<float *>(smem + L.runc);
   float *rsc = reinterpret_cast<float *>(smem + L.rsc);
-  float *dqs = reinterpret_cast<float *>(smem + L.dqs);
   const uint32_t bar0 = smem_u32(smem + L.bars);
   const uint32_t kv0 = smem_u32(smem + L.kv);
 
-  auto kv_smem = [&](int stage, int which) -> unsigned char * {
-    return smem + L.kv + (stage * 2 + which) * kTile * p.rowbytes;
-  };
   auto issue = [&](int t) {
     const int st = t % kStages;
     const uint32_t bar = bar0 + st * 8;
@@ -184,7 +234,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int rgrp = lane >> p.lpr_log2;
   const int rows_per_warp = 32 >> p.lpr_log2;
   const int rows_per_step = kWarps * rows_per_warp;
-  const bool lane_on = sub * 16 < p.rowbytes;
+  const bool lane_on = sub * GB < p.rowbytes;
   const size_t qrow0 = (static_cast<size_t>(b) * p.Hq + static_cast<size_t>(kvh) * G) * D;
   float qr[GMAX][EPL], dr[GMAX][EPL];
 #pragma unroll
@@ -196,17 +246,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       qr[h][e] = on ? p.q[qrow0 + static_cast<size_t>(h) * D + d] * p.scale : 0.f;
       dr[h][e] = on ? p.dout[qrow0 + static_cast<size_t>(h) * D + d] : 0.f;
     }
+  const int wmask = (lpr > NV ? lpr / NV : 1) - 1;   // lanes of a group holding identical sums
 
-  float accA[NACC], accB[NACC];
+  // ---- dq partial sums: item = (row split, head, 4-dim chunk)
+  const int D4 = D >> 2;
+  const int nitems = RS * G * D4;
+  float accA[NIT][4], accB[NIT][4];
 #pragma unroll
-  for (int k = 0; k < NACC; ++k) accA[k] = accB[k] = 0.f;
+  for (int k = 0; k < NIT; ++k)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) accA[k][i] = accB[k][i] = 0.f;
 
   // ======================= phase 1: stream the chunk =======================
   for (int t = 0; t < ntiles; ++t) {
     const int st = t % kStages;
     mbar_wait_or_flag(bar0 + st * 8, (t / kStages) & 1, p.wait);
-    const unsigned char *Kt = kv_smem(st, 0);
-    const unsigned char *Vt = kv_smem(st, 1);
+    const unsigned char *Kt = smem + L.kv + (st * 2 + 0) * tile_bytes;
+    const unsigned char *Vt = smem + L.kv + (st * 2 + 1) * tile_bytes;
     const int rows_valid = min(kTile, nkeys - t * kTile);
     const int jt = t * kTile;
 
@@ -214,13 +270,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int r = warp * rows_per_warp + rgrp; r < kTile; r += rows_per_step) {
       float kf[EPL], vf[EPL];
       if (lane_on) {
-        load_row16<KV>(Kt + r * p.rowbytes + sub * 16, kf);
-        load_row16<KV>(Vt + r * p.rowbytes + sub * 16, vf);
+        GR::load(Kt + r * p.rowbytes + sub * GB, kf);
+        GR::load(Vt + r * p.rowbytes + sub * GB, vf);
       } else {
 #pragma unroll
         for (int e = 0; e < EPL; ++e) kf[e] = vf[e] = 0.f;
       }
-      float sp[GMAX], pp[GMAX];
+      float val[NV];
 #pragma unroll
       for (int h = 0; h < GMAX; ++h) {
         float a = 0.f, c = 0.f;
@@ -229,23 +285,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           a = fmaf(qr[h][e], kf[e], a);
           c = fmaf(dr[h][e], vf[e], c);
         }
-        sp[h] = a;
-        pp[h] = c;
+        val[h] = a;
+        val[GMAX + h] = c;
       }
-      for (int off = lpr >> 1; off > 0; off >>= 1) {
+      int idx0, nf;
+      reduce_scatter<NV>(val, lpr, sub, idx0, nf);
+      if ((sub & wmask) == 0 && r < rows_valid) {
 #pragma unroll
-        for (int h = 0; h < GMAX; ++h) {
-          sp[h] += __shfl_xor_sync(0xffffffffu, sp[h], off);
-          pp[h] += __shfl_xor_sync(0xffffffffu, pp[h], off);
-        }
-      }
-      if (sub == 0 && r < rows_valid) {
-#pragma unroll
-        for (int h = 0; h < GMAX; ++h)
-          if (h < G) {
-            sbuf[h * p.chunk + jt + r] = sp[h];
-            pbuf[h * p.chunk + jt + r] = pp[h];
+        for (int i = 0; i < NV; ++i) {
+          if (i < nf) {
+            const int idx = idx0 + i;
+            const int h = idx < GMAX ? idx : idx - GMAX;
+            if (h < G) (idx < GMAX ? sbuf : pbuf)[h * p.chunk + jt + r] = val[i];
           }
+        }
       }
     }
     __syncthreads();
@@ -280,20 +333,28 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // (c) dq partials: A_h[d] = sum_j e_hj dP_hj K_jd, B_h[d] = sum_j e_hj K_jd
 #pragma unroll
-    for (int k = 0; k < NACC; ++k) {
-      const int idx = tid + kThreads * k;
-      if (idx < G * D) {
-        const int h = idx / D, d = idx - h * D;
-        float a = accA[k] * alph[h], c = accB[k] * alph[h];
+    for (int k = 0; k < NIT; ++k) {
+      const int it = tid + kThreads * k;
+      if (it < nitems) {
+        const int rs = it & (RS - 1);
+        const int hd = it >> p.rs_log2;
+        const int h = hd / D4, dc = hd - h * D4;
+        const float a = alph[h];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          accA[k][i] *= a;
+          accB[k][i] *= a;
+        }
         const float *et = etile + h * kTile;
         const float *ed = edp + h * kTile;
-        for (int r = 0; r < rows_valid; ++r) {
-          const float kv = load_elem<KV>(Kt + r * p.rowbytes, d);
-          a = fmaf(ed[r], kv, a);
-          c = fmaf(et[r], kv, c);
+        for (int r = rs; r < rows_valid; r += RS) {
+          const float4 kv = load4(Kt + r * p.rowbytes, 4 * dc, static_cast<KV *>(nullptr));
+          const float e = et[r], w = ed[r];
+          accA[k][0] = fmaf(w, kv.x, accA[k][0]); accA[k][1] = fmaf(w, kv.y, accA[k][1]);
+          accA[k][2] = fmaf(w, kv.z, accA[k][2]); accA[k][3] = fmaf(w, kv.w, accA[k][3]);
+          accB[k][0] = fmaf(e, kv.x, accB[k][0]); accB[k][1] = fmaf(e, kv.y, accB[k][1]);
+          accB[k][2] = fmaf(e, kv.z, accB[k][2]); accB[k][3] = fmaf(e, kv.w, accB[k][3]);
         }
-        accA[k] = a;
-        accB[k] = c;
       }
     }
     __syncthreads();
@@ -303,31 +364,63 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
 
-  // ======================= publish partials, merge across the cluster ======
-  if (tid < G) {
-    xm[tid] = runm[tid];
-    xl[tid] = runl[tid];
-    xc[tid] = runc[tid];
-  }
+  // ======================= publish partials ================================
+  // row-split partials -> scratch (the K/V tiles are consumed), summed in a
+  // fixed order so results do not depend on scheduling
+  {
+    float *sa = reinterpret_cast<float *>(smem + L.kv);
+    float *sb = sa + RS * G * D;
 #pragma unroll
-  for (int k = 0; k < NACC; ++k) {
-    const int idx = tid + kThreads * k;
-    if (idx < G * D) {
-      xa[idx] = accA[k];
-      xb[idx] = accB[k];
+    for (int k = 0; k < NIT; ++k) {
+      const int it = tid + kThreads * k;
+      if (it < nitems) {
+        const int rs = it & (RS - 1);
+        const int hd = it >> p.rs_log2;
+        const int h = hd / D4, dc = hd - h * D4;
+        float *pa = sa + rs * G * D + h * D + 4 * dc;
+        float *pb = sb + rs * G * D + h * D + 4 * dc;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          pa[i] = accA[k][i];
+          pb[i] = accB[k][i];
+        }
+      }
+    }
+    if (tid < G) {
+      xm[tid] = runm[tid];
+      xl[tid] = runl[tid];
+      xc[tid] = runc[tid];
+    }
+    __syncthreads();
+    for (int idx = tid; idx < G * D; idx += kThreads) {
+      float a = 0.f, c = 0.f;
+      for (int rs = 0; rs < RS; ++rs) {
+        a += sa[rs * G * D + idx];
+        c += sb[rs * G * D + idx];
+      }
+      xa[idx] = a;
+      xb[idx] = c;
     }
   }
   cluster.sync();
 
+  // ======================= merge the softmax statistics ====================
+  if (tid < p.ncl * G) {
+    const int r = tid / G, h = tid - r * G;
+    rstat[r * kMaxG + h] = make_float4(cluster.map_shared_rank(xm, r)[h], cluster.map_shared_rank(xl, r)[h],
+                                       cluster.map_shared_rank(xc, r)[h], 0.f);
+  }
+  __syncthreads();
   if (tid < G) {
     const int h = tid;
     float M = -INFINITY;
-    for (int r = 0; r < p.ncl; ++r) M = fmaxf(M, cluster.map_shared_rank(xm, r)[h]);
+    for (int r = 0; r < p.ncl; ++r) M = fmaxf(M, rstat[r * kMaxG + h].x);
     float Ls = 0.f, Cs = 0.f;
     for (int r = 0; r < p.ncl; ++r) {
-      const float w = expf(cluster.map_shared_rank(xm, r)[h] - M);
-      Ls += cluster.map_shared_rank(xl, r)[h] * w;
-      Cs += cluster.map_shared_rank(xc, r)[h] * w;
+      const float4 st = rstat[r * kMaxG + h];
+      const float w = expf(st.x - M);
+      Ls = fmaf(st.y, w, Ls);
+      Cs = fmaf(st.z, w, Cs);
       rsc[r * kMaxG + h] = w;
     }
     glob[h] = make_float4(M, 1.f / Ls, Cs / Ls, 0.f);
@@ -388,42 +481,43 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
 
-  // ======================= dq on rank 0 ====================================
-  if (rank == 0) {
-    for (int idx = tid; idx < G * D; idx += kThreads) {
-      const int h = idx / D;
-      float sa = 0.f, sb = 0.f;
-      for (int r = 0; r < p.ncl; ++r) {
-        const float w = rsc[r * kMaxG + h];
-        sa = fmaf(w, cluster.map_shared_rank(xa, r)[idx], sa);
-        sb = fmaf(w, cluster.map_shared_rank(xb, r)[idx], sb);
+  // ======================= dq: rotary pairs spread over the cluster ========
+  {
+    const int half = D >> 1;
+    const int np = G * half;
+    for (int pr = tid * p.ncl + rank; pr < np; pr += kThreads * p.ncl) {
+      const int h = pr / half, pi = pr - h * half;
+      const int idx = h * D + 2 * pi;
+      float a0 = 0.f, a1 = 0.f, b0 = 0.f, b1 = 0.f;
+#pragma unroll
+      for (int r = 0; r < kMaxCluster; ++r) {
+        if (r < p.ncl) {
+          const float w = rsc[r * kMaxG + h];
+          const float2 ra = *reinterpret_cast<const float2 *>(cluster.map_shared_rank(xa, r) + idx);
+          const float2 rb = *reinterpret_cast<const float2 *>(cluster.map_shared_rank(xb, r) + idx);
+          a0 = fmaf(w, ra.x, a0); a1 = fmaf(w, ra.y, a1);
+          b0 = fmaf(w, rb.x, b0); b1 = fmaf(w, rb.y, b1);
+        }
       }
       const float4 g = glob[h];
-      dqs[idx] = p.scale * (sa - g.z * sb) * g.y;
-    }
-    __syncthreads();
-    const int half = D >> 1;
-    for (int i = tid; i < G * half; i += kThreads) {
-      const int h = i / half, pi = i - h * half;
-      const float y0 = dqs[h * D + 2 * pi], y1 = dqs[h * D + 2 * pi + 1];
+      const float y0 = p.scale * (a0 - g.z * b0) * g.y;
+      const float y1 = p.scale * (a1 - g.z * b1) * g.y;
       float z0 = y0, z1 = y1;
       if (p.rope) {
         const float c = p.rcos[pi], s = p.rsin[pi];
         z0 = y0 * c + y1 * s;
         z1 = -y0 * s + y1 * c;
       }
-      float *out = p.dq + qrow0 + static_cast<size_t>(h) * D + 2 * pi;
-      out[0] = z0;
-      out[1] = z1;
+      *reinterpret_cast<float2 *>(p.dq + qrow0 + idx) = make_float2(z0, z1);
     }
   }
-  cluster.sync();   // peers' shared memory stays alive until rank 0 has read it
+  cluster.sync();   // peers' shared memory stays alive until every CTA has read it
 }
 
-template <typename KV, int GMAX>
+template <typename KV, int GMAX, int GB>
 cudaError_t launch_typed(const CUtensorMap &tk, const CUtensorMap &tv, const DecodeParams &p, int smem,
                          cudaStream_t st) {
-  auto kern = decode_bwd_kernel<KV, GMAX>;
+  auto kern = decode_bwd_kernel<KV, GMAX, GB>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -441,14 +535,14 @@ cudaError_t launch_typed(const CUtensorMap &tk, const CUtensorMap &tv, const Dec
   return cudaLaunchKernelEx(&cfg, kern, tk, tv, p);
 }
 
-template <typename KV>
+template <typename KV, int GB>
 cudaError_t launch_g(int gmax, const CUtensorMap &tk, const CUtensorMap &tv, const DecodeParams &p, int smem,
                      cudaStream_t st) {
   switch (gmax) {
-    case 1: return launch_typed<KV, 1>(tk, tv, p, smem, st);
-    case 2: return launch_typed<KV, 2>(tk, tv, p, smem, st);
-    case 4: return launch_typed<KV, 4>(tk, tv, p, smem, st);
-    default: return launch_typed<KV, 8>(tk, tv, p, smem, st);
+    case 1: return launch_typed<KV, 1, GB>(tk, tv, p, smem, st);
+    case 2: return launch_typed<KV, 2, GB>(tk, tv, p, smem, st);
+    case 4: return launch_typed<KV, 4, GB>(tk, tv, p, smem, st);
+    default: return launch_typed<KV, 8, GB>(tk, tv, p, smem, st);
   }
 }
 
@@ -460,24 +554,27 @@ cudaError_t launch_attn_bwd_decode(const float *q, const void *k, const void *v,
                                    const char **why) {
   const int es = kv_bf16 ? 2 : 4;
   const int rowbytes = D * es;
-  int lpr_log2 = 0;
-  while ((16 << lpr_log2) < rowbytes) ++lpr_log2;   // lanes per row = ceil to a power of two
-  if (lpr_log2 > 5) {
-    *why = "row too wide";
+  if (rowbytes > 512 || rowbytes % 16 != 0) {
+    *why = "row width";
     return cudaErrorNotSupported;
   }
+  const int gb = rowbytes <= 256 ? 8 : 16;        // bytes per lane in the dot phase
+  int lpr_log2 = 0;
+  while ((gb << lpr_log2) < rowbytes) ++lpr_log2;  // lanes per row, rounded up to a power of two
   if (Hkv > 65535 || B > 65535) {
     *why = "B or Hkv > 65535";
     return cudaErrorNotSupported;
   }
   const int G = Hq / Hkv;
   const int gmax = G <= 1 ? 1 : G <= 2 ? 2 : G <= 4 ? 4 : 8;
+  int rs_log2 = 0;                                 // row splits of the dq partial sums
+  while (rs_log2 < 4 && (G * (D / 4)) << (rs_log2 + 1) <= kThreads) ++rs_log2;
   const int tiles = (S + kTile - 1) / kTile;
   int ncl = tiles < kMaxCluster ? tiles : kMaxCluster;
   const int chunk = ((tiles + ncl - 1) / ncl) * kTile;
-  ncl = (S + chunk - 1) / chunk;                 // every CTA owns at least one key
-  const Layout L(G, D, chunk, rowbytes);
-  const int smem = L.total + 1024;               // + alignment slack
+  ncl = (S + chunk - 1) / chunk;                   // every CTA owns at least one key
+  const Layout L(G, D, chunk, rowbytes, 1 << rs_log2);
+  const int smem = L.total + 1024;                 // + alignment slack
   if (smem > 227 * 1024) {
     *why = "KV length too long for the per-CTA score buffers";
     return cudaErrorNotSupported;
@@ -486,7 +583,7 @@ cudaError_t launch_attn_bwd_decode(const float *q, const void *k, const void *v,
   DecodeParams p;
   p.q = q; p.dout = dout; p.dq = dq; p.dk = dk; p.dv = dv;
   p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.S = S; p.D = D; p.G = G;
-  p.chunk = chunk; p.ncl = ncl; p.lpr_log2 = lpr_log2; p.rowbytes = rowbytes;
+  p.chunk = chunk; p.ncl = ncl; p.lpr_log2 = lpr_log2; p.rs_log2 = rs_log2; p.rowbytes = rowbytes;
   p.scale = scale;
   p.rope = rope_base > 0.0 && q_pos >= 0;
   for (int i = 0; i < 128; ++i) {
@@ -512,8 +609,10 @@ cudaError_t launch_attn_bwd_decode(const float *q, const void *k, const void *v,
       !encode_tiled(&tv, dt, 4, v, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE, why))
     return cudaErrorInvalidValue;
 
-  return kv_bf16 ? launch_g<__nv_bfloat16>(gmax, tk, tv, p, smem, st)
-                 : launch_g<float>(gmax, tk, tv, p, smem, st);
+  if (kv_bf16)
+    return gb == 8 ? launch_g<__nv_bfloat16, 8>(gmax, tk, tv, p, smem, st)
+                   : launch_g<__nv_bfloat16, 16>(gmax, tk, tv, p, smem, st);
+  return gb == 8 ? launch_g<float, 8>(gmax, tk, tv, p, smem, st) : launch_g<float, 16>(gmax, tk, tv, p, smem, st);
 }
 
 }  // namespace abw
