@@ -82,7 +82,16 @@ class ClockSampler:
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.monotonic(), line.strip()))
+
+    def wait_first(self, timeout=5.0):
+        """Blocks until nvidia-smi has produced a sample (it takes a moment to start)."""
+        t0 = time.monotonic()
+        while self.proc is not None and not self.lines and time.monotonic() - t0 < timeout:
+            time.sleep(0.02)
+
+    def mark(self):
+        return time.monotonic()
 
     def __exit__(self, *exc):
         if self.proc is not None:
@@ -93,10 +102,20 @@ class ClockSampler:
                 self.proc.kill()
             self.thread.join(timeout=2)
 
-    def summary(self):
+    def summary(self, t0=None, t1=None):
+        """Median SM clock and active throttle reasons of the samples taken in
+        [t0, t1] (the timed region, widened by one sampling period); if the
+        region was shorter than the sampling period, the samples of the whole
+        sampled window (steady warm-up load + timed region) are used."""
         sm, mx, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        window = "timed"
+        lines = [ln for (ts, ln) in self.lines
+                 if t0 is None or (t0 - 0.12 <= ts <= t1 + 0.12)]
+        if not lines:
+            lines = [ln for (_, ln) in self.lines]
+            window = "warmup+timed"
+        for ln in lines:
             parts = [p.strip() for p in ln.split(",")]
             if len(parts) < 8:
                 continue
@@ -111,7 +130,7 @@ class ClockSampler:
         if not sm:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
-                "samples": len(sm)}
+                "samples": len(sm), "window": window}
 
 
 # ----------------------------------------------------------------------------
@@ -243,6 +262,19 @@ def recorded_traffic(kernel_key, src_files):
     return e.get("dram_bytes_per_launch")
 
 
+def keep_busy(fn, stream, seconds):
+    """Runs `fn` back to back for about `seconds` (untimed warm-up load)."""
+    import torch
+    t0 = time.monotonic()
+    n = 0
+    while time.monotonic() - t0 < seconds:
+        for _ in range(8):
+            fn()
+        n += 8
+        stream.synchronize()
+    return n
+
+
 def run_native(args):
     import torch
     import torch.distributed as dist
@@ -304,6 +336,10 @@ def run_native(args):
     kern_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(local) as clocks:
+        clocks.wait_first()
+        keep_busy(step, stream, 0.4)          # steady load while the sampler runs (untimed)
+        barrier()
+        h0 = clocks.mark()
         t_start.record(stream)
         for i in range(args.steps):
             step_ev[i][0].record(stream)
@@ -311,6 +347,7 @@ def run_native(args):
             step_ev[i][1].record(stream)
         t_end.record(stream)
         torch.cuda.synchronize()
+        h1 = clocks.mark()
     barrier()
     abw.device_check(stream)
     total_ms = max_over_ranks(t_start.elapsed_time(t_end))
@@ -373,11 +410,16 @@ def run_native(args):
         c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         csteps = max(1, args.steps)
         with ClockSampler(local) as cclocks:
+            cclocks.wait_first()
+            keep_busy(cstep, stream, 0.3)
+            barrier()
+            ch0 = cclocks.mark()
             c0.record(stream)
             for _ in range(csteps):
                 cstep()
             c1.record(stream)
             torch.cuda.synchronize()
+            ch1 = cclocks.mark()
         barrier()
         abw.device_check(stream)
         cms = max_over_ranks(c0.elapsed_time(c1)) / csteps
@@ -390,7 +432,7 @@ def run_native(args):
                                "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                                "frac": round(ctf / world / peaks["bf16_tflops"], 4), "traffic": None,
                                "peak_kind": kind + " (burst)", "scope": "whole call"},
-                  "clocks": cclocks.summary()}
+                  "clocks": cclocks.summary(ch0, ch1)}
         del cin, o, lse, cq, ck, cv, ws
         torch.cuda.empty_cache()
 
@@ -425,7 +467,7 @@ def run_native(args):
             "e2e": {"value": round(e2e_value, 3), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)},
             "gpu_launches": launches,
-            "clocks": clocks.summary(),
+            "clocks": clocks.summary(h0, h1),
             "causal_t2048": causal,
         }
         print(json.dumps(line), flush=True)
