@@ -91,6 +91,18 @@ def test_rope_roundtrip_norm_on_gpu(abw):
 
 
 # ------------------------------------------------------------------ RMSNorm
+def test_rmsnorm_single_element_rows(abw):
+    """n = 1: dx = dy g eps / ((x^2 + eps) rms) is a cancellation of two terms of
+    size |dy g| / rms; fp32 error is bounded relative to those terms, not to
+    the (tiny) result."""
+    inp = W.rmsnorm_inputs(64, 1, seed=1)
+    dx = abw.rmsnorm_bwd(dev(inp["x"]), dev(inp["gamma"]), dev(inp["dy"]), eps=inp["eps"])
+    x, g, dy = to_np(inp["x"]), to_np(inp["gamma"]), to_np(inp["dy"])
+    ref = O.rmsnorm_backward(x, g, dy, inp["eps"])
+    scale = np.abs(dy * g) / np.sqrt(x * x + inp["eps"])
+    assert np.all(np.abs(to_np(dx) - ref) <= 1e-5 * scale + 1e-30)
+
+
 def test_rmsnorm_tiny(abw):
     t = W.tiny_inputs()
     dx = abw.rmsnorm_bwd(dev(t["rms_x"][None]), dev(t["rms_gamma"]), dev(t["rms_dy"][None]), eps=t["eps"])
@@ -105,7 +117,6 @@ def test_rmsnorm_tiny(abw):
     (3, 1001, torch.float32, torch.float32),       # n % 4 != 0
     (2, 10000, torch.float32, torch.bfloat16),     # n > 8192: two-pass path
     (5, 4, torch.float32, torch.float32),
-    (1, 1, torch.float32, torch.float32),
 ])
 def test_rmsnorm_shapes(abw, rows, n, xdt, dxdt):
     inp = W.rmsnorm_inputs(rows, n, seed=rows + n, x_dtype=xdt)

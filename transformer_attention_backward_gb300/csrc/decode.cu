@@ -61,15 +61,18 @@ struct DecodeParams {
 struct Layout {
   int kv, sbuf, pbuf, etile, edp, xm, xl, xc, xa, xb, glob, alpha, runm, runl, runc, rstat, rsc, bars, total;
   __host__ __device__ static int up(int x, int a) { return (x + a - 1) / a * a; }
-  __host__ __device__ Layout(int G, int D, int chunk, int rowbytes, int rs) {
+  // Per-key scalars are stored key-major with a stride of gs >= G floats
+  // (gs = the kernel's power-of-two head capacity), so one vector load
+  // fetches every head's value for a key.
+  __host__ __device__ Layout(int G, int gs, int D, int chunk, int rowbytes, int rs) {
     int o = 0;
     const int tiles = kStages * 2 * kTile * rowbytes;
     const int scratch = 2 * rs * G * D * 4;   // row-split dq partials, after the tile loop
     kv = o;    o += tiles > scratch ? tiles : scratch;   o = up(o, 16);
-    sbuf = o;  o += G * chunk * 4;
-    pbuf = o;  o += G * chunk * 4;
-    etile = o; o += G * kTile * 4;
-    edp = o;   o += G * kTile * 4;
+    sbuf = o;  o += gs * chunk * 4;
+    pbuf = o;  o += gs * chunk * 4;
+    etile = o; o += gs * kTile * 4;
+    edp = o;   o += gs * kTile * 4;
     xm = o;    o += kMaxG * 4;
     xl = o;    o += kMaxG * 4;
     xc = o;    o += kMaxG * 4;
@@ -133,6 +136,23 @@ __device__ __forceinline__ float4 load4(const unsigned char *row, int d, float *
   return *reinterpret_cast<const float4 *>(row + 4 * d);
 }
 
+// Loads the N consecutive floats at p (16-byte aligned when N >= 4).
+template <int N>
+__device__ __forceinline__ void ld_heads(const float *p, float (&x)[N]) {
+  if constexpr (N >= 4) {
+#pragma unroll
+    for (int i = 0; i < N; i += 4) {
+      const float4 v = *reinterpret_cast<const float4 *>(p + i);
+      x[i] = v.x; x[i + 1] = v.y; x[i + 2] = v.z; x[i + 3] = v.w;
+    }
+  } else if constexpr (N == 2) {
+    const float2 v = *reinterpret_cast<const float2 *>(p);
+    x[0] = v.x; x[1] = v.y;
+  } else {
+    x[0] = p[0];
+  }
+}
+
 // Sums NV values over an aligned group of `lpr` lanes (a power of two) while
 // spreading them out: each exchange step halves the values a lane keeps, so
 // the group needs log2(NV) + log2(lpr / NV) shuffles per value set instead of
@@ -164,20 +184,19 @@ __device__ __forceinline__ void reduce_scatter(float (&v)[NV], int lpr, int lane
 }
 
 template <typename KV, int GMAX, int GB>
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(kThreads, GMAX >= 8 ? 1 : 2)
     decode_bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                       const __grid_constant__ DecodeParams p) {
   using GR = Gran<KV, GB>;
   constexpr int EPL = GR::EPL;                 // elements per lane in the dot phase
   constexpr int NV = 2 * GMAX;                 // per-row values: s_h and dP_h
-  constexpr int NIT = (GMAX * (512 / static_cast<int>(sizeof(KV))) / 4 + kThreads - 1) / kThreads;
   cg::cluster_group cluster = cg::this_cluster();
   extern __shared__ unsigned char smem_raw[];
   unsigned char *smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
 
   const int G = p.G, D = p.D;
   const int RS = 1 << p.rs_log2;
-  const Layout L(G, D, p.chunk, p.rowbytes, RS);
+  const Layout L(G, GMAX, D, p.chunk, p.rowbytes, RS);
   const int rank = static_cast<int>(cluster.block_rank());
   const int kvh = blockIdx.y, b = blockIdx.z;
   const int key0 = rank * p.chunk;
@@ -248,14 +267,15 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
   const int wmask = (lpr > NV ? lpr / NV : 1) - 1;   // lanes of a group holding identical sums
 
-  // ---- dq partial sums: item = (row split, head, 4-dim chunk)
+  // ---- dq partial sums: thread = (row split, 4-dim chunk), every head
   const int D4 = D >> 2;
-  const int nitems = RS * G * D4;
-  float accA[NIT][4], accB[NIT][4];
+  const int dc = tid % D4, rsp = tid / D4;          // rsp < RS for active threads
+  const bool c_on = rsp < RS;
+  float accA[GMAX][4], accB[GMAX][4];
 #pragma unroll
-  for (int k = 0; k < NIT; ++k)
+  for (int h = 0; h < GMAX; ++h)
 #pragma unroll
-    for (int i = 0; i < 4; ++i) accA[k][i] = accB[k][i] = 0.f;
+    for (int i = 0; i < 4; ++i) accA[h][i] = accB[h][i] = 0.f;
 
   // ======================= phase 1: stream the chunk =======================
   for (int t = 0; t < ntiles; ++t) {
@@ -296,7 +316,7 @@ __global__ void __launch_bounds__(kThreads, 2)
           if (i < nf) {
             const int idx = idx0 + i;
             const int h = idx < GMAX ? idx : idx - GMAX;
-            if (h < G) (idx < GMAX ? sbuf : pbuf)[h * p.chunk + jt + r] = val[i];
+            if (h < G) (idx < GMAX ? sbuf : pbuf)[(jt + r) * GMAX + h] = val[i];
           }
         }
       }
@@ -306,20 +326,20 @@ __global__ void __launch_bounds__(kThreads, 2)
     // (b) running max / normaliser / sum e dP per head (warp h)
     if (warp < G) {
       const int h = warp;
-      const float s0 = lane < rows_valid ? sbuf[h * p.chunk + jt + lane] : -INFINITY;
-      const float s1 = lane + 32 < rows_valid ? sbuf[h * p.chunk + jt + lane + 32] : -INFINITY;
-      const float d0 = lane < rows_valid ? pbuf[h * p.chunk + jt + lane] : 0.f;
-      const float d1 = lane + 32 < rows_valid ? pbuf[h * p.chunk + jt + lane + 32] : 0.f;
+      const float s0 = lane < rows_valid ? sbuf[(jt + lane) * GMAX + h] : -INFINITY;
+      const float s1 = lane + 32 < rows_valid ? sbuf[(jt + lane + 32) * GMAX + h] : -INFINITY;
+      const float d0 = lane < rows_valid ? pbuf[(jt + lane) * GMAX + h] : 0.f;
+      const float d1 = lane + 32 < rows_valid ? pbuf[(jt + lane + 32) * GMAX + h] : 0.f;
       const float mt = warp_max(fmaxf(s0, s1));
       const float m_old = runm[h];
       const float m_new = fmaxf(m_old, mt);
       const float a = expf(m_old - m_new);   // 0 on the first tile
       const float e0 = lane < rows_valid ? expf(s0 - m_new) : 0.f;
       const float e1 = lane + 32 < rows_valid ? expf(s1 - m_new) : 0.f;
-      etile[h * kTile + lane] = e0;
-      etile[h * kTile + lane + 32] = e1;
-      edp[h * kTile + lane] = e0 * d0;
-      edp[h * kTile + lane + 32] = e1 * d1;
+      etile[lane * GMAX + h] = e0;
+      etile[(lane + 32) * GMAX + h] = e1;
+      edp[lane * GMAX + h] = e0 * d0;
+      edp[(lane + 32) * GMAX + h] = e1 * d1;
       const float ls = warp_sum(e0 + e1);
       const float csum = warp_sum(e0 * d0 + e1 * d1);
       if (lane == 0) {
@@ -332,28 +352,27 @@ __global__ void __launch_bounds__(kThreads, 2)
     __syncthreads();
 
     // (c) dq partials: A_h[d] = sum_j e_hj dP_hj K_jd, B_h[d] = sum_j e_hj K_jd
+    if (c_on) {
+      float al[GMAX];
+      ld_heads<GMAX>(alph, al);
 #pragma unroll
-    for (int k = 0; k < NIT; ++k) {
-      const int it = tid + kThreads * k;
-      if (it < nitems) {
-        const int rs = it & (RS - 1);
-        const int hd = it >> p.rs_log2;
-        const int h = hd / D4, dc = hd - h * D4;
-        const float a = alph[h];
+      for (int h = 0; h < GMAX; ++h)
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-          accA[k][i] *= a;
-          accB[k][i] *= a;
+          accA[h][i] *= al[h];
+          accB[h][i] *= al[h];
         }
-        const float *et = etile + h * kTile;
-        const float *ed = edp + h * kTile;
-        for (int r = rs; r < rows_valid; r += RS) {
-          const float4 kv = load4(Kt + r * p.rowbytes, 4 * dc, static_cast<KV *>(nullptr));
-          const float e = et[r], w = ed[r];
-          accA[k][0] = fmaf(w, kv.x, accA[k][0]); accA[k][1] = fmaf(w, kv.y, accA[k][1]);
-          accA[k][2] = fmaf(w, kv.z, accA[k][2]); accA[k][3] = fmaf(w, kv.w, accA[k][3]);
-          accB[k][0] = fmaf(e, kv.x, accB[k][0]); accB[k][1] = fmaf(e, kv.y, accB[k][1]);
-          accB[k][2] = fmaf(e, kv.z, accB[k][2]); accB[k][3] = fmaf(e, kv.w, accB[k][3]);
+      for (int r = rsp; r < rows_valid; r += RS) {
+        const float4 kv = load4(Kt + r * p.rowbytes, 4 * dc, static_cast<KV *>(nullptr));
+        float e[GMAX], w[GMAX];
+        ld_heads<GMAX>(etile + r * GMAX, e);
+        ld_heads<GMAX>(edp + r * GMAX, w);
+#pragma unroll
+        for (int h = 0; h < GMAX; ++h) {
+          accA[h][0] = fmaf(w[h], kv.x, accA[h][0]); accA[h][1] = fmaf(w[h], kv.y, accA[h][1]);
+          accA[h][2] = fmaf(w[h], kv.z, accA[h][2]); accA[h][3] = fmaf(w[h], kv.w, accA[h][3]);
+          accB[h][0] = fmaf(e[h], kv.x, accB[h][0]); accB[h][1] = fmaf(e[h], kv.y, accB[h][1]);
+          accB[h][2] = fmaf(e[h], kv.z, accB[h][2]); accB[h][3] = fmaf(e[h], kv.w, accB[h][3]);
         }
       }
     }
@@ -370,19 +389,17 @@ __global__ void __launch_bounds__(kThreads, 2)
   {
     float *sa = reinterpret_cast<float *>(smem + L.kv);
     float *sb = sa + RS * G * D;
+    if (c_on) {
 #pragma unroll
-    for (int k = 0; k < NIT; ++k) {
-      const int it = tid + kThreads * k;
-      if (it < nitems) {
-        const int rs = it & (RS - 1);
-        const int hd = it >> p.rs_log2;
-        const int h = hd / D4, dc = hd - h * D4;
-        float *pa = sa + rs * G * D + h * D + 4 * dc;
-        float *pb = sb + rs * G * D + h * D + 4 * dc;
+      for (int h = 0; h < GMAX; ++h) {
+        if (h < G) {
+          float *pa = sa + rsp * G * D + h * D + 4 * dc;
+          float *pb = sb + rsp * G * D + h * D + 4 * dc;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          pa[i] = accA[k][i];
-          pb[i] = accB[k][i];
+          for (int i = 0; i < 4; ++i) {
+            pa[i] = accA[h][i];
+            pb[i] = accB[h][i];
+          }
         }
       }
     }
@@ -428,12 +445,14 @@ __global__ void __launch_bounds__(kThreads, 2)
   __syncthreads();
 
   // P and dS of this CTA's keys, in place of the score and dP
-  for (int i = tid; i < G * nkeys; i += kThreads) {
-    const int h = i / nkeys, j = i - h * nkeys;
-    const float4 g = glob[h];
-    const float P = expf(sbuf[h * p.chunk + j] - g.x) * g.y;
-    sbuf[h * p.chunk + j] = P;
-    pbuf[h * p.chunk + j] = P * (pbuf[h * p.chunk + j] - g.z);
+  for (int i = tid; i < GMAX * nkeys; i += kThreads) {
+    const int h = i & (GMAX - 1);
+    if (h < G) {
+      const float4 g = glob[h];
+      const float P = expf(sbuf[i] - g.x) * g.y;
+      sbuf[i] = P;
+      pbuf[i] = P * (pbuf[i] - g.z);
+    }
   }
   __syncthreads();
 
@@ -461,10 +480,13 @@ __global__ void __launch_bounds__(kThreads, 2)
       }
       for (int j = warp * orows_w + ogrp; j < nkeys; j += kWarps * orows_w) {
         float4 ak = make_float4(0.f, 0.f, 0.f, 0.f), av = ak;
+        float Ph[GMAX], dSh[GMAX];
+        ld_heads<GMAX>(sbuf + j * GMAX, Ph);
+        ld_heads<GMAX>(pbuf + j * GMAX, dSh);
 #pragma unroll
         for (int h = 0; h < GMAX; ++h) {
           if (h < G) {
-            const float P = sbuf[h * p.chunk + j], dS = pbuf[h * p.chunk + j];
+            const float P = Ph[h], dS = dSh[h];
             ak.x = fmaf(dS, qo[h].x, ak.x); ak.y = fmaf(dS, qo[h].y, ak.y);
             ak.z = fmaf(dS, qo[h].z, ak.z); ak.w = fmaf(dS, qo[h].w, ak.w);
             av.x = fmaf(P, go[h].x, av.x);  av.y = fmaf(P, go[h].y, av.y);
@@ -568,12 +590,12 @@ cudaError_t launch_attn_bwd_decode(const float *q, const void *k, const void *v,
   const int G = Hq / Hkv;
   const int gmax = G <= 1 ? 1 : G <= 2 ? 2 : G <= 4 ? 4 : 8;
   int rs_log2 = 0;                                 // row splits of the dq partial sums
-  while (rs_log2 < 4 && (G * (D / 4)) << (rs_log2 + 1) <= kThreads) ++rs_log2;
+  while ((1 << (rs_log2 + 1)) <= kTile && (D / 4) << (rs_log2 + 1) <= kThreads) ++rs_log2;
   const int tiles = (S + kTile - 1) / kTile;
   int ncl = tiles < kMaxCluster ? tiles : kMaxCluster;
   const int chunk = ((tiles + ncl - 1) / ncl) * kTile;
   ncl = (S + chunk - 1) / chunk;                   // every CTA owns at least one key
-  const Layout L(G, D, chunk, rowbytes, 1 << rs_log2);
+  const Layout L(G, gmax, D, chunk, rowbytes, 1 << rs_log2);
   const int smem = L.total + 1024;                 // + alignment slack
   if (smem > 227 * 1024) {
     *why = "KV length too long for the per-CTA score buffers";
