@@ -47,7 +47,7 @@ struct DecodeParams {
   int B, Hq, Hkv, S, D, G;
   int chunk;      // keys per CTA (multiple of kTile)
   int ncl;        // CTAs per (b, kv head) == cluster size
-  int lpr_log2;   // log2(lanes per K/V row) in the dot phase
+  int lpr_log2;   // log2(lanes per K/V row) in the fallback dot phase
   int rs_log2;    // log2(row splits) of the dq partial sums
   int rowbytes;   // D * sizeof(kv)
   float scale;
@@ -59,7 +59,7 @@ struct DecodeParams {
 
 // Byte offsets of the dynamic shared-memory regions (same in every CTA).
 struct Layout {
-  int kv, sbuf, pbuf, etile, edp, xm, xl, xc, xa, xb, glob, alpha, runm, runl, runc, rstat, rsc, bars, total;
+  int kv, qs, sbuf, pbuf, etile, edp, xm, xl, xc, xa, xb, glob, alpha, runm, runl, runc, rstat, rsc, bars, total;
   __host__ __device__ static int up(int x, int a) { return (x + a - 1) / a * a; }
   // Per-key scalars are stored key-major with a stride of gs >= G floats
   // (gs = the kernel's power-of-two head capacity), so one vector load
@@ -69,6 +69,7 @@ struct Layout {
     const int tiles = kStages * 2 * kTile * rowbytes;
     const int scratch = 2 * rs * G * D * 4;   // row-split dq partials, after the tile loop
     kv = o;    o += tiles > scratch ? tiles : scratch;   o = up(o, 16);
+    qs = o;    o += 2 * gs * 4 * (D / 4 + 4) * 4;
     sbuf = o;  o += gs * chunk * 4;
     pbuf = o;  o += gs * chunk * 4;
     etile = o; o += gs * kTile * 4;
@@ -183,12 +184,19 @@ __device__ __forceinline__ void reduce_scatter(float (&v)[NV], int lpr, int lane
   for (; o > 0; o >>= 1) v[0] += __shfl_xor_sync(0xffffffffu, v[0], o);
 }
 
-template <typename KV, int GMAX, int GB>
+// SWZ: K/V tiles arrive 128B-swizzled (row widths that are a multiple of 128
+// bytes); the dot phase then gives each key row to 4 lanes, each owning a
+// quarter of the head dim, with scale*q and dout broadcast from shared memory.
+// Otherwise (narrow or odd rows) lanes split a row in 16-byte granules with
+// q and dout held in registers.
+template <typename KV, int GMAX, bool SWZ>
 __global__ void __launch_bounds__(kThreads, GMAX >= 8 ? 1 : 2)
     decode_bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                       const __grid_constant__ DecodeParams p) {
+  constexpr int GB = 16;
   using GR = Gran<KV, GB>;
-  constexpr int EPL = GR::EPL;                 // elements per lane in the dot phase
+  constexpr int EPL = GR::EPL;                 // elements per 16-byte granule
+  constexpr int ES = static_cast<int>(sizeof(KV));
   constexpr int NV = 2 * GMAX;                 // per-row values: s_h and dP_h
   cg::cluster_group cluster = cg::this_cluster();
   extern __shared__ unsigned char smem_raw[];
@@ -220,6 +228,8 @@ __global__ void __launch_bounds__(kThreads, GMAX >= 8 ? 1 : 2)
   float *runl = reinterpret_cast<float *>(smem + L.runl);
   float *runc = reinterpret_cast<float *>(smem + L.runc);
   float *rsc = reinterpret_cast<float *>(smem + L.rsc);
+  float *qsm = reinterpret_cast<float *>(smem + L.qs);    // [GMAX][4 parts][DPL + 4]: scale*q
+  float *dsm = qsm + GMAX * 4 * (D / 4 + 4);              // same for dout
   const uint32_t bar0 = smem_u32(smem + L.bars);
   const uint32_t kv0 = smem_u32(smem + L.kv);
 
@@ -227,8 +237,18 @@ __global__ void __launch_bounds__(kThreads, GMAX >= 8 ? 1 : 2)
     const int st = t % kStages;
     const uint32_t bar = bar0 + st * 8;
     mbar_arrive_expect_tx(bar, 2 * tile_bytes);
-    tma_load_4d(kv0 + (st * 2 + 0) * tile_bytes, &tmK, 0, kvh, key0 + t * kTile, b, bar);
-    tma_load_4d(kv0 + (st * 2 + 1) * tile_bytes, &tmV, 0, kvh, key0 + t * kTile, b, bar);
+    if constexpr (SWZ) {
+      // one 128-byte-wide box per 128 bytes of row; box bx lands at bx * 8 KiB
+      const int nbox = p.rowbytes >> 7;
+      for (int bx = 0; bx < nbox; ++bx) {
+        const uint32_t o = bx * (kTile * 128);
+        tma_load_4d(kv0 + (st * 2 + 0) * tile_bytes + o, &tmK, bx * (128 / ES), kvh, key0 + t * kTile, b, bar);
+        tma_load_4d(kv0 + (st * 2 + 1) * tile_bytes + o, &tmV, bx * (128 / ES), kvh, key0 + t * kTile, b, bar);
+      }
+    } else {
+      tma_load_4d(kv0 + (st * 2 + 0) * tile_bytes, &tmK, 0, kvh, key0 + t * kTile, b, bar);
+      tma_load_4d(kv0 + (st * 2 + 1) * tile_bytes, &tmV, 0, kvh, key0 + t * kTile, b, bar);
+    }
   };
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -247,24 +267,37 @@ __global__ void __launch_bounds__(kThreads, GMAX >= 8 ? 1 : 2)
   if (tid == 0)
     for (int t = 0; t < min(kStages, ntiles); ++t) issue(t);
 
-  // ---- per-lane slices of scale*q and dout for the dot products
-  const int lpr = 1 << p.lpr_log2;
+  // ---- scale*q and dout for the dot products
+  const size_t qrow0 = (static_cast<size_t>(b) * p.Hq + static_cast<size_t>(kvh) * G) * D;
+  const int DPL = D >> 2;                               // dims per lane-part (SWZ)
+  const int lpr = 1 << p.lpr_log2;                      // lanes per row (fallback)
   const int sub = lane & (lpr - 1);
   const int rgrp = lane >> p.lpr_log2;
   const int rows_per_warp = 32 >> p.lpr_log2;
   const int rows_per_step = kWarps * rows_per_warp;
   const bool lane_on = sub * GB < p.rowbytes;
-  const size_t qrow0 = (static_cast<size_t>(b) * p.Hq + static_cast<size_t>(kvh) * G) * D;
-  float qr[GMAX][EPL], dr[GMAX][EPL];
-#pragma unroll
-  for (int h = 0; h < GMAX; ++h)
-#pragma unroll
-    for (int e = 0; e < EPL; ++e) {
-      const int d = sub * EPL + e;
-      const bool on = h < G && lane_on;
-      qr[h][e] = on ? p.q[qrow0 + static_cast<size_t>(h) * D + d] * p.scale : 0.f;
-      dr[h][e] = on ? p.dout[qrow0 + static_cast<size_t>(h) * D + d] : 0.f;
+  constexpr int QR = SWZ ? 1 : GMAX;                    // register copies (fallback only)
+  float qr[QR][EPL], dr[QR][EPL];
+  if constexpr (SWZ) {
+    for (int idx = tid; idx < GMAX * D; idx += kThreads) {
+      const int h = idx / D, d = idx - h * D;
+      const int o = (h * 4 + d / DPL) * (DPL + 4) + d % DPL;
+      const bool on = h < G;
+      qsm[o] = on ? p.q[qrow0 + idx] * p.scale : 0.f;
+      dsm[o] = on ? p.dout[qrow0 + idx] : 0.f;
     }
+    __syncthreads();
+  } else {
+#pragma unroll
+    for (int h = 0; h < QR; ++h)
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) {
+        const int d = sub * EPL + e;
+        const bool on = h < G && lane_on;
+        qr[h][e] = on ? p.q[qrow0 + static_cast<size_t>(h) * D + d] * p.scale : 0.f;
+        dr[h][e] = on ? p.dout[qrow0 + static_cast<size_t>(h) * D + d] : 0.f;
+      }
+  }
   const int wmask = (lpr > NV ? lpr / NV : 1) - 1;   // lanes of a group holding identical sums
 
   // ---- dq partial sums: thread = (row split, 4-dim chunk), every head
@@ -287,36 +320,84 @@ __global__ void __launch_bounds__(kThreads, GMAX >= 8 ? 1 : 2)
     const int jt = t * kTile;
 
     // (a) s_hj = (scale q_h) . K_j and dP_hj = dout_h . V_j
-    for (int r = warp * rows_per_warp + rgrp; r < kTile; r += rows_per_step) {
-      float kf[EPL], vf[EPL];
-      if (lane_on) {
-        GR::load(Kt + r * p.rowbytes + sub * GB, kf);
-        GR::load(Vt + r * p.rowbytes + sub * GB, vf);
-      } else {
-#pragma unroll
-        for (int e = 0; e < EPL; ++e) kf[e] = vf[e] = 0.f;
-      }
+    if constexpr (SWZ) {
+      const int r = tid >> 2, pp = tid & 3;             // 64 rows x 4 quarter-rows
       float val[NV];
 #pragma unroll
-      for (int h = 0; h < GMAX; ++h) {
-        float a = 0.f, c = 0.f;
+      for (int i = 0; i < NV; ++i) val[i] = 0.f;
+      const int nch = (DPL * ES) >> 4;
+      const float *qp = qsm + pp * (DPL + 4);
+      const float *dp_ = dsm + pp * (DPL + 4);
+      for (int c = 0; c < nch; ++c) {
+        const int off = pp * DPL * ES + (c << 4);       // byte offset in the row
+        const int so = (off >> 7) * (kTile * 128) + r * 128 + ((((off & 127) >> 4) ^ (r & 7)) << 4);
+        float kf[EPL], vf[EPL];
+        GR::load(Kt + so, kf);
+        GR::load(Vt + so, vf);
 #pragma unroll
-        for (int e = 0; e < EPL; ++e) {
-          a = fmaf(qr[h][e], kf[e], a);
-          c = fmaf(dr[h][e], vf[e], c);
+        for (int h = 0; h < GMAX; ++h) {
+#pragma unroll
+          for (int e = 0; e < EPL; e += 4) {
+            const float4 q4 = *reinterpret_cast<const float4 *>(qp + h * 4 * (DPL + 4) + c * EPL + e);
+            const float4 d4 = *reinterpret_cast<const float4 *>(dp_ + h * 4 * (DPL + 4) + c * EPL + e);
+            val[h] = fmaf(q4.x, kf[e], val[h]);
+            val[h] = fmaf(q4.y, kf[e + 1], val[h]);
+            val[h] = fmaf(q4.z, kf[e + 2], val[h]);
+            val[h] = fmaf(q4.w, kf[e + 3], val[h]);
+            val[GMAX + h] = fmaf(d4.x, vf[e], val[GMAX + h]);
+            val[GMAX + h] = fmaf(d4.y, vf[e + 1], val[GMAX + h]);
+            val[GMAX + h] = fmaf(d4.z, vf[e + 2], val[GMAX + h]);
+            val[GMAX + h] = fmaf(d4.w, vf[e + 3], val[GMAX + h]);
+          }
         }
-        val[h] = a;
-        val[GMAX + h] = c;
       }
       int idx0, nf;
-      reduce_scatter<NV>(val, lpr, sub, idx0, nf);
-      if ((sub & wmask) == 0 && r < rows_valid) {
+      reduce_scatter<NV>(val, 4, pp, idx0, nf);
+      // nf = NV / 4 values (NV >= 4) or 1, all scores or all dP, heads
+      // idx0 % GMAX onward; a group of 4 lanes covers every value
+      constexpr int NF = NV >= 4 ? NV / 4 : 1;
+      if (r < rows_valid && (NV >= 4 || (pp & 1) == 0)) {
+        float *dst = (idx0 < GMAX ? sbuf : pbuf) + (jt + r) * GMAX + (idx0 & (GMAX - 1));
+        if constexpr (NF == 4) {
+          *reinterpret_cast<float4 *>(dst) = make_float4(val[0], val[1], val[2], val[3]);
+        } else if constexpr (NF == 2) {
+          *reinterpret_cast<float2 *>(dst) = make_float2(val[0], val[1]);
+        } else {
+          dst[0] = val[0];
+        }
+      }
+    } else {
+      for (int r = warp * rows_per_warp + rgrp; r < kTile; r += rows_per_step) {
+        float kf[EPL], vf[EPL];
+        if (lane_on) {
+          GR::load(Kt + r * p.rowbytes + sub * GB, kf);
+          GR::load(Vt + r * p.rowbytes + sub * GB, vf);
+        } else {
 #pragma unroll
-        for (int i = 0; i < NV; ++i) {
-          if (i < nf) {
-            const int idx = idx0 + i;
-            const int h = idx < GMAX ? idx : idx - GMAX;
-            if (h < G) (idx < GMAX ? sbuf : pbuf)[(jt + r) * GMAX + h] = val[i];
+          for (int e = 0; e < EPL; ++e) kf[e] = vf[e] = 0.f;
+        }
+        float val[NV];
+#pragma unroll
+        for (int h = 0; h < GMAX; ++h) {
+          float a = 0.f, c = 0.f;
+#pragma unroll
+          for (int e = 0; e < EPL; ++e) {
+            a = fmaf(qr[h][e], kf[e], a);
+            c = fmaf(dr[h][e], vf[e], c);
+          }
+          val[h] = a;
+          val[GMAX + h] = c;
+        }
+        int idx0, nf;
+        reduce_scatter<NV>(val, lpr, sub, idx0, nf);
+        if ((sub & wmask) == 0 && r < rows_valid) {
+#pragma unroll
+          for (int i = 0; i < NV; ++i) {
+            if (i < nf) {
+              const int idx = idx0 + i;
+              const int h = idx < GMAX ? idx : idx - GMAX;
+              if (h < G) (idx < GMAX ? sbuf : pbuf)[(jt + r) * GMAX + h] = val[i];
+            }
           }
         }
       }
@@ -363,7 +444,15 @@ __global__ void __launch_bounds__(kThreads, GMAX >= 8 ? 1 : 2)
           accB[h][i] *= al[h];
         }
       for (int r = rsp; r < rows_valid; r += RS) {
-        const float4 kv = load4(Kt + r * p.rowbytes, 4 * dc, static_cast<KV *>(nullptr));
+        float4 kv;
+        if constexpr (SWZ) {
+          const int off = dc * 4 * ES;                  // byte offset of the 4 elements in the row
+          const unsigned char *kp = Kt + (off >> 7) * (kTile * 128) + r * 128 +
+                                    ((((off & 127) >> 4) ^ (r & 7)) << 4) + (off & 15);
+          kv = load4(kp, 0, static_cast<KV *>(nullptr));
+        } else {
+          kv = load4(Kt + r * p.rowbytes, 4 * dc, static_cast<KV *>(nullptr));
+        }
         float e[GMAX], w[GMAX];
         ld_heads<GMAX>(etile + r * GMAX, e);
         ld_heads<GMAX>(edp + r * GMAX, w);
@@ -536,10 +625,10 @@ __global__ void __launch_bounds__(kThreads, GMAX >= 8 ? 1 : 2)
   cluster.sync();   // peers' shared memory stays alive until every CTA has read it
 }
 
-template <typename KV, int GMAX, int GB>
+template <typename KV, int GMAX, bool SWZ>
 cudaError_t launch_typed(const CUtensorMap &tk, const CUtensorMap &tv, const DecodeParams &p, int smem,
                          cudaStream_t st) {
-  auto kern = decode_bwd_kernel<KV, GMAX, GB>;
+  auto kern = decode_bwd_kernel<KV, GMAX, SWZ>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -557,14 +646,14 @@ cudaError_t launch_typed(const CUtensorMap &tk, const CUtensorMap &tv, const Dec
   return cudaLaunchKernelEx(&cfg, kern, tk, tv, p);
 }
 
-template <typename KV, int GB>
+template <typename KV, bool SWZ>
 cudaError_t launch_g(int gmax, const CUtensorMap &tk, const CUtensorMap &tv, const DecodeParams &p, int smem,
                      cudaStream_t st) {
   switch (gmax) {
-    case 1: return launch_typed<KV, 1, GB>(tk, tv, p, smem, st);
-    case 2: return launch_typed<KV, 2, GB>(tk, tv, p, smem, st);
-    case 4: return launch_typed<KV, 4, GB>(tk, tv, p, smem, st);
-    default: return launch_typed<KV, 8, GB>(tk, tv, p, smem, st);
+    case 1: return launch_typed<KV, 1, SWZ>(tk, tv, p, smem, st);
+    case 2: return launch_typed<KV, 2, SWZ>(tk, tv, p, smem, st);
+    case 4: return launch_typed<KV, 4, SWZ>(tk, tv, p, smem, st);
+    default: return launch_typed<KV, 8, SWZ>(tk, tv, p, smem, st);
   }
 }
 
@@ -580,9 +669,9 @@ cudaError_t launch_attn_bwd_decode(const float *q, const void *k, const void *v,
     *why = "row width";
     return cudaErrorNotSupported;
   }
-  const int gb = rowbytes <= 256 ? 8 : 16;        // bytes per lane in the dot phase
+  const bool swz = rowbytes % 128 == 0;            // 128B-swizzled tiles, quarter-row lanes
   int lpr_log2 = 0;
-  while ((gb << lpr_log2) < rowbytes) ++lpr_log2;  // lanes per row, rounded up to a power of two
+  while ((16 << lpr_log2) < rowbytes) ++lpr_log2;  // fallback: lanes per row (16 B each), power of two
   if (Hkv > 65535 || B > 65535) {
     *why = "B or Hkv > 65535";
     return cudaErrorNotSupported;
@@ -625,16 +714,17 @@ cudaError_t launch_attn_bwd_decode(const float *q, const void *k, const void *v,
                             static_cast<uint64_t>(B)};
   const uint64_t strides[3] = {static_cast<uint64_t>(rowbytes), static_cast<uint64_t>(Hkv) * rowbytes,
                                static_cast<uint64_t>(S) * Hkv * rowbytes};
-  const uint32_t box[4] = {static_cast<uint32_t>(D), 1, kTile, 1};
+  const uint32_t box[4] = {static_cast<uint32_t>(swz ? 128 / es : D), 1, kTile, 1};
   const CUtensorMapDataType dt = kv_bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
-  if (!encode_tiled(&tk, dt, 4, k, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE, why) ||
-      !encode_tiled(&tv, dt, 4, v, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE, why))
+  const CUtensorMapSwizzle sw = swz ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE;
+  if (!encode_tiled(&tk, dt, 4, k, dims, strides, box, sw, why) ||
+      !encode_tiled(&tv, dt, 4, v, dims, strides, box, sw, why))
     return cudaErrorInvalidValue;
 
   if (kv_bf16)
-    return gb == 8 ? launch_g<__nv_bfloat16, 8>(gmax, tk, tv, p, smem, st)
-                   : launch_g<__nv_bfloat16, 16>(gmax, tk, tv, p, smem, st);
-  return gb == 8 ? launch_g<float, 8>(gmax, tk, tv, p, smem, st) : launch_g<float, 16>(gmax, tk, tv, p, smem, st);
+    return swz ? launch_g<__nv_bfloat16, true>(gmax, tk, tv, p, smem, st)
+               : launch_g<__nv_bfloat16, false>(gmax, tk, tv, p, smem, st);
+  return swz ? launch_g<float, true>(gmax, tk, tv, p, smem, st) : launch_g<float, false>(gmax, tk, tv, p, smem, st);
 }
 
 }  // namespace abw
