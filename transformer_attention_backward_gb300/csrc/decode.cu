@@ -10,17 +10,27 @@
 // Design (GB300): the work is bound by HBM -- K and V are read once (bf16) and
 // dK, dV are written once (fp32).  One (batch, KV head) unit is split over a
 // thread-block cluster of up to 8 CTAs, each owning a contiguous chunk of
-// keys.  K/V tiles of 64 rows arrive by TMA into a two-stage shared-memory
-// ring.  Per key the CTA keeps only two scalars per query head (the score and
-// dP) in shared memory; the softmax normaliser, delta = sum P dP and the dq
-// partial sums sum_j e_j dP_j K_j and sum_j e_j K_j are carried as running
-// (max-rescaled) partials, the same online-softmax merge Hesper's split-KV
-// flash attention uses for its tile partials (pull request #1, "Phase 2:
-// Merge partial results").  The cluster merges the per-CTA partials through
-// distributed shared memory; every CTA then writes its dK/dV rows straight
-// from the two scalars per head with streaming 16-byte stores, and rank 0
-// finishes dq (with the inverse rotation) -- so no byte of K/V is read twice
-// and nothing goes through a global scratch buffer.
+// keys; K/V tiles of 64 rows arrive by TMA.  Per key the CTA keeps two
+// scalars per query head (score, dP) in shared memory.  The cluster merges the
+// per-CTA softmax statistics (max, normaliser, sum e dP) through distributed
+// shared memory -- the online-softmax merge Hesper's split-KV flash attention
+// applies to its tile partials (pull request #1, "Phase 2: Merge partial
+// results") -- and every CTA then writes its dK/dV rows straight from the
+// two scalars per head with streaming 16-byte stores.
+//
+// Two shapes of the same kernel:
+//  * resident (a CTA's chunk fits its two TMA stages -- e.g. 1024 keys over 8
+//    CTAs): the K tiles stay in shared memory, so the CTA's share of dq is
+//    accumulated with the final dS in the same pass that writes dK/dV.  With
+//    a bf16 head dim of 64, 128 or 256 the tiles arrive 128B-swizzled and
+//    each key row is split over 4 lanes, every lane owning a quarter of the
+//    head dim, with scale*q and dout broadcast from shared memory
+//    (conflict-free on both operands).
+//  * streaming (longer chunks): tiles cycle through the two stages and the
+//    dq partials sum_j e_j dP_j K_j and sum_j e_j K_j are carried as running
+//    max-rescaled sums, merged across the cluster with the statistics.
+// Either way no byte of K/V is read twice and nothing goes through a global
+// scratch buffer.
 #include <cooperative_groups.h>
 #include <math.h>
 
@@ -34,7 +44,7 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kTile = 64;       // K/V rows per TMA tile
-constexpr int kStages = 2;      // TMA ring depth
+constexpr int kStages = 2;      // TMA stages
 constexpr int kMaxCluster = 8;  // portable cluster size
 constexpr int kMaxG = 8;
 
@@ -47,8 +57,9 @@ struct DecodeParams {
   int B, Hq, Hkv, S, D, G;
   int chunk;      // keys per CTA (multiple of kTile)
   int ncl;        // CTAs per (b, kv head) == cluster size
-  int lpr_log2;   // log2(lanes per K/V row) in the fallback dot phase
-  int rs_log2;    // log2(row splits) of the dq partial sums
+  int resident;   // chunk <= kStages * kTile: K stays in shared memory
+  int lpr_log2;   // generic dot phase: log2(lanes per K/V row), 16 bytes per lane
+  int rs_log2;    // streaming: log2(row splits) of the dq partial sums
   int rowbytes;   // D * sizeof(kv)
   float scale;
   int rope;
@@ -58,16 +69,15 @@ struct DecodeParams {
 };
 
 // Byte offsets of the dynamic shared-memory regions (same in every CTA).
+// Per-key scalars are key-major with a stride of gs (the kernel's
+// power-of-two head capacity), so one vector load fetches all heads of a key.
 struct Layout {
-  int kv, qs, sbuf, pbuf, etile, edp, xm, xl, xc, xa, xb, glob, alpha, runm, runl, runc, rstat, rsc, bars, total;
+  int kv, qs, sbuf, pbuf, etile, edp, xm, xl, xc, xa, xb, glob, rstat, alpha, runm, runl, runc, rsc, bars, total;
   __host__ __device__ static int up(int x, int a) { return (x + a - 1) / a * a; }
-  // Per-key scalars are stored key-major with a stride of gs >= G floats
-  // (gs = the kernel's power-of-two head capacity), so one vector load
-  // fetches every head's value for a key.
   __host__ __device__ Layout(int G, int gs, int D, int chunk, int rowbytes, int rs) {
     int o = 0;
-    const int tiles = kStages * 2 * kTile * rowbytes;
-    const int scratch = 2 * rs * G * D * 4;   // row-split dq partials, after the tile loop
+    const int tiles = 2 * kStages * kTile * rowbytes;        // [K st0][K st1][V st0][V st1]
+    const int scratch = 2 * rs * G * D * 4;                   // streaming: row-split dq partials
     kv = o;    o += tiles > scratch ? tiles : scratch;   o = up(o, 16);
     qs = o;    o += 2 * gs * 4 * (D / 4 + 4) * 4;
     sbuf = o;  o += gs * chunk * 4;
@@ -91,50 +101,24 @@ struct Layout {
   }
 };
 
-// Loads EPL consecutive elements (8 or 16 bytes) of a K/V row as floats.
-template <typename KV, int GB>
-struct Gran;
-template <>
-struct Gran<__nv_bfloat16, 8> {
-  static constexpr int EPL = 4;
-  __device__ static void load(const unsigned char *p, float (&f)[4]) {
-    const uint2 u = *reinterpret_cast<const uint2 *>(p);
-    f[0] = bf16_lo(u.x); f[1] = bf16_hi(u.x); f[2] = bf16_lo(u.y); f[3] = bf16_hi(u.y);
-  }
-};
-template <>
-struct Gran<__nv_bfloat16, 16> {
-  static constexpr int EPL = 8;
-  __device__ static void load(const unsigned char *p, float (&f)[8]) {
-    const uint4 u = *reinterpret_cast<const uint4 *>(p);
-    f[0] = bf16_lo(u.x); f[1] = bf16_hi(u.x); f[2] = bf16_lo(u.y); f[3] = bf16_hi(u.y);
-    f[4] = bf16_lo(u.z); f[5] = bf16_hi(u.z); f[6] = bf16_lo(u.w); f[7] = bf16_hi(u.w);
-  }
-};
-template <>
-struct Gran<float, 8> {
-  static constexpr int EPL = 2;
-  __device__ static void load(const unsigned char *p, float (&f)[2]) {
-    const float2 u = *reinterpret_cast<const float2 *>(p);
-    f[0] = u.x; f[1] = u.y;
-  }
-};
-template <>
-struct Gran<float, 16> {
-  static constexpr int EPL = 4;
-  __device__ static void load(const unsigned char *p, float (&f)[4]) {
-    const float4 u = *reinterpret_cast<const float4 *>(p);
-    f[0] = u.x; f[1] = u.y; f[2] = u.z; f[3] = u.w;
-  }
-};
+// 16 bytes of a K/V row as floats.
+__device__ __forceinline__ void load16(const unsigned char *p, float (&f)[8]) {
+  const uint4 u = *reinterpret_cast<const uint4 *>(p);
+  f[0] = bf16_lo(u.x); f[1] = bf16_hi(u.x); f[2] = bf16_lo(u.y); f[3] = bf16_hi(u.y);
+  f[4] = bf16_lo(u.z); f[5] = bf16_hi(u.z); f[6] = bf16_lo(u.w); f[7] = bf16_hi(u.w);
+}
+__device__ __forceinline__ void load16(const unsigned char *p, float (&f)[4]) {
+  const float4 u = *reinterpret_cast<const float4 *>(p);
+  f[0] = u.x; f[1] = u.y; f[2] = u.z; f[3] = u.w;
+}
 
-// Four consecutive row elements starting at element d (d % 4 == 0).
-__device__ __forceinline__ float4 load4(const unsigned char *row, int d, __nv_bfloat16 *) {
-  const uint2 u = *reinterpret_cast<const uint2 *>(row + 2 * d);
+// Four consecutive row elements at p.
+__device__ __forceinline__ float4 load4(const unsigned char *p, __nv_bfloat16 *) {
+  const uint2 u = *reinterpret_cast<const uint2 *>(p);
   return make_float4(bf16_lo(u.x), bf16_hi(u.x), bf16_lo(u.y), bf16_hi(u.y));
 }
-__device__ __forceinline__ float4 load4(const unsigned char *row, int d, float *) {
-  return *reinterpret_cast<const float4 *>(row + 4 * d);
+__device__ __forceinline__ float4 load4(const unsigned char *p, float *) {
+  return *reinterpret_cast<const float4 *>(p);
 }
 
 // Loads the N consecutive floats at p (16-byte aligned when N >= 4).
@@ -167,8 +151,6 @@ __device__ __forceinline__ void reduce_scatter(float (&v)[NV], int lpr, int lane
 #pragma unroll
   for (int s = 0; (NV >> s) > 1; ++s) {
     if (o == 0) break;
-    constexpr int dummy = 0;
-    (void)dummy;
     const int h = NV >> (s + 1);
     const bool up = (lane & o) != 0;
 #pragma unroll
@@ -184,33 +166,32 @@ __device__ __forceinline__ void reduce_scatter(float (&v)[NV], int lpr, int lane
   for (; o > 0; o >>= 1) v[0] += __shfl_xor_sync(0xffffffffu, v[0], o);
 }
 
-// SWZ: K/V tiles arrive 128B-swizzled (row widths that are a multiple of 128
-// bytes); the dot phase then gives each key row to 4 lanes, each owning a
-// quarter of the head dim, with scale*q and dout broadcast from shared memory.
-// Otherwise (narrow or odd rows) lanes split a row in 16-byte granules with
-// q and dout held in registers.
-template <typename KV, int GMAX, bool SWZ>
+// DT > 0: resident chunk, 128B-swizzled bf16 tiles, head dim DT, quarter-row
+// lanes.  DT == 0: any supported head dim, resident or streaming, unswizzled.
+template <typename KV, int GMAX, int DT>
 __global__ void __launch_bounds__(kThreads, GMAX >= 8 ? 1 : 2)
     decode_bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                       const __grid_constant__ DecodeParams p) {
-  constexpr int GB = 16;
-  using GR = Gran<KV, GB>;
-  constexpr int EPL = GR::EPL;                 // elements per 16-byte granule
+  constexpr bool SWZ = DT > 0;
   constexpr int ES = static_cast<int>(sizeof(KV));
+  constexpr int EPL = 16 / ES;                 // elements per 16-byte granule
   constexpr int NV = 2 * GMAX;                 // per-row values: s_h and dP_h
   cg::cluster_group cluster = cg::this_cluster();
   extern __shared__ unsigned char smem_raw[];
   unsigned char *smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
 
-  const int G = p.G, D = p.D;
+  const int G = p.G;
+  const int D = SWZ ? DT : p.D;
+  const int rowbytes = SWZ ? DT * ES : p.rowbytes;
+  const bool resident = SWZ || p.resident;
   const int RS = 1 << p.rs_log2;
-  const Layout L(G, GMAX, D, p.chunk, p.rowbytes, RS);
+  const Layout L(G, GMAX, D, p.chunk, rowbytes, RS);
   const int rank = static_cast<int>(cluster.block_rank());
   const int kvh = blockIdx.y, b = blockIdx.z;
   const int key0 = rank * p.chunk;
   const int nkeys = min(p.chunk, p.S - key0);   // >= 1 by construction of chunk / ncl
   const int ntiles = (nkeys + kTile - 1) / kTile;
-  const uint32_t tile_bytes = static_cast<uint32_t>(kTile * p.rowbytes);
+  const uint32_t tile_bytes = static_cast<uint32_t>(kTile * rowbytes);
 
   float *sbuf = reinterpret_cast<float *>(smem + L.sbuf);
   float *pbuf = reinterpret_cast<float *>(smem + L.pbuf);
@@ -228,26 +209,37 @@ __global__ void __launch_bounds__(kThreads, GMAX >= 8 ? 1 : 2)
   float *runl = reinterpret_cast<float *>(smem + L.runl);
   float *runc = reinterpret_cast<float *>(smem + L.runc);
   float *rsc = reinterpret_cast<float *>(smem + L.rsc);
-  float *qsm = reinterpret_cast<float *>(smem + L.qs);    // [GMAX][4 parts][DPL + 4]: scale*q
+  float *qsm = reinterpret_cast<float *>(smem + L.qs);    // [GMAX][4 parts][D/4 + 4]: scale*q
   float *dsm = qsm + GMAX * 4 * (D / 4 + 4);              // same for dout
   const uint32_t bar0 = smem_u32(smem + L.bars);
   const uint32_t kv0 = smem_u32(smem + L.kv);
+  auto ktile = [&](int st) -> const unsigned char * { return smem + L.kv + st * tile_bytes; };
+  auto vtile = [&](int st) -> const unsigned char * { return smem + L.kv + (kStages + st) * tile_bytes; };
+  // address of element d of row r in a tile
+  auto elem = [&](const unsigned char *tile, int r, int d) -> const unsigned char * {
+    if constexpr (SWZ) {
+      const int off = d * ES;
+      return tile + (off >> 7) * (kTile * 128) + r * 128 + ((((off & 127) >> 4) ^ (r & 7)) << 4) + (off & 15);
+    } else {
+      return tile + r * rowbytes + d * ES;
+    }
+  };
 
   auto issue = [&](int t) {
     const int st = t % kStages;
     const uint32_t bar = bar0 + st * 8;
+    const uint32_t kd = kv0 + st * tile_bytes, vd = kv0 + (kStages + st) * tile_bytes;
     mbar_arrive_expect_tx(bar, 2 * tile_bytes);
     if constexpr (SWZ) {
       // one 128-byte-wide box per 128 bytes of row; box bx lands at bx * 8 KiB
-      const int nbox = p.rowbytes >> 7;
-      for (int bx = 0; bx < nbox; ++bx) {
-        const uint32_t o = bx * (kTile * 128);
-        tma_load_4d(kv0 + (st * 2 + 0) * tile_bytes + o, &tmK, bx * (128 / ES), kvh, key0 + t * kTile, b, bar);
-        tma_load_4d(kv0 + (st * 2 + 1) * tile_bytes + o, &tmV, bx * (128 / ES), kvh, key0 + t * kTile, b, bar);
+#pragma unroll
+      for (int bx = 0; bx < DT * ES / 128; ++bx) {
+        tma_load_4d(kd + bx * (kTile * 128), &tmK, bx * (128 / ES), kvh, key0 + t * kTile, b, bar);
+        tma_load_4d(vd + bx * (kTile * 128), &tmV, bx * (128 / ES), kvh, key0 + t * kTile, b, bar);
       }
     } else {
-      tma_load_4d(kv0 + (st * 2 + 0) * tile_bytes, &tmK, 0, kvh, key0 + t * kTile, b, bar);
-      tma_load_4d(kv0 + (st * 2 + 1) * tile_bytes, &tmV, 0, kvh, key0 + t * kTile, b, bar);
+      tma_load_4d(kd, &tmK, 0, kvh, key0 + t * kTile, b, bar);
+      tma_load_4d(vd, &tmV, 0, kvh, key0 + t * kTile, b, bar);
     }
   };
 
@@ -269,18 +261,18 @@ __global__ void __launch_bounds__(kThreads, GMAX >= 8 ? 1 : 2)
 
   // ---- scale*q and dout for the dot products
   const size_t qrow0 = (static_cast<size_t>(b) * p.Hq + static_cast<size_t>(kvh) * G) * D;
-  const int DPL = D >> 2;                               // dims per lane-part (SWZ)
-  const int lpr = 1 << p.lpr_log2;                      // lanes per row (fallback)
+  const int lpr = 1 << p.lpr_log2;                      // generic: lanes per row
   const int sub = lane & (lpr - 1);
   const int rgrp = lane >> p.lpr_log2;
   const int rows_per_warp = 32 >> p.lpr_log2;
   const int rows_per_step = kWarps * rows_per_warp;
-  const bool lane_on = sub * GB < p.rowbytes;
-  constexpr int QR = SWZ ? 1 : GMAX;                    // register copies (fallback only)
+  const bool lane_on = sub * 16 < rowbytes;
+  constexpr int QR = SWZ ? 1 : GMAX;                    // register copies (generic only)
   float qr[QR][EPL], dr[QR][EPL];
   if constexpr (SWZ) {
-    for (int idx = tid; idx < GMAX * D; idx += kThreads) {
-      const int h = idx / D, d = idx - h * D;
+    constexpr int DPL = DT / 4;
+    for (int idx = tid; idx < GMAX * DT; idx += kThreads) {
+      const int h = idx / DT, d = idx - h * DT;
       const int o = (h * 4 + d / DPL) * (DPL + 4) + d % DPL;
       const bool on = h < G;
       qsm[o] = on ? p.q[qrow0 + idx] * p.scale : 0.f;
@@ -298,42 +290,26 @@ __global__ void __launch_bounds__(kThreads, GMAX >= 8 ? 1 : 2)
         dr[h][e] = on ? p.dout[qrow0 + static_cast<size_t>(h) * D + d] : 0.f;
       }
   }
-  const int wmask = (lpr > NV ? lpr / NV : 1) - 1;   // lanes of a group holding identical sums
+  const int wmask = (lpr > NV ? lpr / NV : 1) - 1;   // generic: lanes of a group holding identical sums
 
-  // ---- dq partial sums: thread = (row split, 4-dim chunk), every head
-  const int D4 = D >> 2;
-  const int dc = tid % D4, rsp = tid / D4;          // rsp < RS for active threads
-  const bool c_on = rsp < RS;
-  float accA[GMAX][4], accB[GMAX][4];
-#pragma unroll
-  for (int h = 0; h < GMAX; ++h)
-#pragma unroll
-    for (int i = 0; i < 4; ++i) accA[h][i] = accB[h][i] = 0.f;
-
-  // ======================= phase 1: stream the chunk =======================
-  for (int t = 0; t < ntiles; ++t) {
-    const int st = t % kStages;
-    mbar_wait_or_flag(bar0 + st * 8, (t / kStages) & 1, p.wait);
-    const unsigned char *Kt = smem + L.kv + (st * 2 + 0) * tile_bytes;
-    const unsigned char *Vt = smem + L.kv + (st * 2 + 1) * tile_bytes;
-    const int rows_valid = min(kTile, nkeys - t * kTile);
-    const int jt = t * kTile;
-
-    // (a) s_hj = (scale q_h) . K_j and dP_hj = dout_h . V_j
+  // (a) s_hj = (scale q_h) . K_j and dP_hj = dout_h . V_j for one tile
+  auto dots = [&](int st, int jt, int rows_valid) {
+    const unsigned char *Kt = ktile(st), *Vt = vtile(st);
     if constexpr (SWZ) {
+      constexpr int DPL = DT / 4;
+      constexpr int NCH = DPL * ES / 16;
       const int r = tid >> 2, pp = tid & 3;             // 64 rows x 4 quarter-rows
       float val[NV];
 #pragma unroll
       for (int i = 0; i < NV; ++i) val[i] = 0.f;
-      const int nch = (DPL * ES) >> 4;
       const float *qp = qsm + pp * (DPL + 4);
       const float *dp_ = dsm + pp * (DPL + 4);
-      for (int c = 0; c < nch; ++c) {
-        const int off = pp * DPL * ES + (c << 4);       // byte offset in the row
-        const int so = (off >> 7) * (kTile * 128) + r * 128 + ((((off & 127) >> 4) ^ (r & 7)) << 4);
+#pragma unroll
+      for (int c = 0; c < NCH; ++c) {
+        const int d0 = pp * DPL + c * EPL;
         float kf[EPL], vf[EPL];
-        GR::load(Kt + so, kf);
-        GR::load(Vt + so, vf);
+        load16(elem(Kt, r, d0), kf);
+        load16(elem(Vt, r, d0), vf);
 #pragma unroll
         for (int h = 0; h < GMAX; ++h) {
 #pragma unroll
@@ -353,8 +329,8 @@ __global__ void __launch_bounds__(kThreads, GMAX >= 8 ? 1 : 2)
       }
       int idx0, nf;
       reduce_scatter<NV>(val, 4, pp, idx0, nf);
-      // nf = NV / 4 values (NV >= 4) or 1, all scores or all dP, heads
-      // idx0 % GMAX onward; a group of 4 lanes covers every value
+      // each of the 4 lanes keeps NV/4 sums (all scores or all dP, heads
+      // idx0 % GMAX onward); with NV = 2, lanes 0 and 2 hold the two sums
       constexpr int NF = NV >= 4 ? NV / 4 : 1;
       if (r < rows_valid && (NV >= 4 || (pp & 1) == 0)) {
         float *dst = (idx0 < GMAX ? sbuf : pbuf) + (jt + r) * GMAX + (idx0 & (GMAX - 1));
@@ -370,8 +346,8 @@ __global__ void __launch_bounds__(kThreads, GMAX >= 8 ? 1 : 2)
       for (int r = warp * rows_per_warp + rgrp; r < kTile; r += rows_per_step) {
         float kf[EPL], vf[EPL];
         if (lane_on) {
-          GR::load(Kt + r * p.rowbytes + sub * GB, kf);
-          GR::load(Vt + r * p.rowbytes + sub * GB, vf);
+          load16(Kt + r * rowbytes + sub * 16, kf);
+          load16(Vt + r * rowbytes + sub * 16, vf);
         } else {
 #pragma unroll
           for (int e = 0; e < EPL; ++e) kf[e] = vf[e] = 0.f;
@@ -402,80 +378,112 @@ __global__ void __launch_bounds__(kThreads, GMAX >= 8 ? 1 : 2)
         }
       }
     }
-    __syncthreads();
+  };
 
-    // (b) running max / normaliser / sum e dP per head (warp h)
+  // ======================= phase 1 =========================================
+  const int D4 = D >> 2;
+  if (resident) {
+    for (int t = 0; t < ntiles; ++t) {
+      mbar_wait_or_flag(bar0 + t * 8, 0, p.wait);
+      dots(t, t * kTile, min(kTile, nkeys - t * kTile));
+    }
+    __syncthreads();
+    // chunk statistics per head (warp h): max, sum e, sum e dP
     if (warp < G) {
       const int h = warp;
-      const float s0 = lane < rows_valid ? sbuf[(jt + lane) * GMAX + h] : -INFINITY;
-      const float s1 = lane + 32 < rows_valid ? sbuf[(jt + lane + 32) * GMAX + h] : -INFINITY;
-      const float d0 = lane < rows_valid ? pbuf[(jt + lane) * GMAX + h] : 0.f;
-      const float d1 = lane + 32 < rows_valid ? pbuf[(jt + lane + 32) * GMAX + h] : 0.f;
-      const float mt = warp_max(fmaxf(s0, s1));
-      const float m_old = runm[h];
-      const float m_new = fmaxf(m_old, mt);
-      const float a = expf(m_old - m_new);   // 0 on the first tile
-      const float e0 = lane < rows_valid ? expf(s0 - m_new) : 0.f;
-      const float e1 = lane + 32 < rows_valid ? expf(s1 - m_new) : 0.f;
-      etile[lane * GMAX + h] = e0;
-      etile[(lane + 32) * GMAX + h] = e1;
-      edp[lane * GMAX + h] = e0 * d0;
-      edp[(lane + 32) * GMAX + h] = e1 * d1;
-      const float ls = warp_sum(e0 + e1);
-      const float csum = warp_sum(e0 * d0 + e1 * d1);
+      float m = -INFINITY;
+      for (int j = lane; j < nkeys; j += 32) m = fmaxf(m, sbuf[j * GMAX + h]);
+      m = warp_max(m);
+      float ls = 0.f, cs = 0.f;
+      for (int j = lane; j < nkeys; j += 32) {
+        const float e = expf(sbuf[j * GMAX + h] - m);
+        ls += e;
+        cs = fmaf(e, pbuf[j * GMAX + h], cs);
+      }
+      ls = warp_sum(ls);
+      cs = warp_sum(cs);
       if (lane == 0) {
-        runl[h] = runl[h] * a + ls;
-        runc[h] = runc[h] * a + csum;
-        runm[h] = m_new;
-        alph[h] = a;
+        xm[h] = m;
+        xl[h] = ls;
+        xc[h] = cs;
       }
     }
-    __syncthreads();
-
-    // (c) dq partials: A_h[d] = sum_j e_hj dP_hj K_jd, B_h[d] = sum_j e_hj K_jd
-    if (c_on) {
-      float al[GMAX];
-      ld_heads<GMAX>(alph, al);
+  } else {
+    // streaming: running statistics and running dq partials
+    const int dc = tid % D4, rsp = tid / D4;
+    const bool c_on = rsp < RS;
+    float accA[GMAX][4], accB[GMAX][4];
 #pragma unroll
-      for (int h = 0; h < GMAX; ++h)
+    for (int h = 0; h < GMAX; ++h)
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          accA[h][i] *= al[h];
-          accB[h][i] *= al[h];
-        }
-      for (int r = rsp; r < rows_valid; r += RS) {
-        float4 kv;
-        if constexpr (SWZ) {
-          const int off = dc * 4 * ES;                  // byte offset of the 4 elements in the row
-          const unsigned char *kp = Kt + (off >> 7) * (kTile * 128) + r * 128 +
-                                    ((((off & 127) >> 4) ^ (r & 7)) << 4) + (off & 15);
-          kv = load4(kp, 0, static_cast<KV *>(nullptr));
-        } else {
-          kv = load4(Kt + r * p.rowbytes, 4 * dc, static_cast<KV *>(nullptr));
-        }
-        float e[GMAX], w[GMAX];
-        ld_heads<GMAX>(etile + r * GMAX, e);
-        ld_heads<GMAX>(edp + r * GMAX, w);
-#pragma unroll
-        for (int h = 0; h < GMAX; ++h) {
-          accA[h][0] = fmaf(w[h], kv.x, accA[h][0]); accA[h][1] = fmaf(w[h], kv.y, accA[h][1]);
-          accA[h][2] = fmaf(w[h], kv.z, accA[h][2]); accA[h][3] = fmaf(w[h], kv.w, accA[h][3]);
-          accB[h][0] = fmaf(e[h], kv.x, accB[h][0]); accB[h][1] = fmaf(e[h], kv.y, accB[h][1]);
-          accB[h][2] = fmaf(e[h], kv.z, accB[h][2]); accB[h][3] = fmaf(e[h], kv.w, accB[h][3]);
+      for (int i = 0; i < 4; ++i) accA[h][i] = accB[h][i] = 0.f;
+    for (int t = 0; t < ntiles; ++t) {
+      const int st = t % kStages;
+      mbar_wait_or_flag(bar0 + st * 8, (t / kStages) & 1, p.wait);
+      const int rows_valid = min(kTile, nkeys - t * kTile);
+      const int jt = t * kTile;
+      dots(st, jt, rows_valid);
+      __syncthreads();
+      if (warp < G) {
+        const int h = warp;
+        const float s0 = lane < rows_valid ? sbuf[(jt + lane) * GMAX + h] : -INFINITY;
+        const float s1 = lane + 32 < rows_valid ? sbuf[(jt + lane + 32) * GMAX + h] : -INFINITY;
+        const float d0 = lane < rows_valid ? pbuf[(jt + lane) * GMAX + h] : 0.f;
+        const float d1 = lane + 32 < rows_valid ? pbuf[(jt + lane + 32) * GMAX + h] : 0.f;
+        const float mt = warp_max(fmaxf(s0, s1));
+        const float m_old = runm[h];
+        const float m_new = fmaxf(m_old, mt);
+        const float a = expf(m_old - m_new);   // 0 on the first tile
+        const float e0 = lane < rows_valid ? expf(s0 - m_new) : 0.f;
+        const float e1 = lane + 32 < rows_valid ? expf(s1 - m_new) : 0.f;
+        etile[lane * GMAX + h] = e0;
+        etile[(lane + 32) * GMAX + h] = e1;
+        edp[lane * GMAX + h] = e0 * d0;
+        edp[(lane + 32) * GMAX + h] = e1 * d1;
+        const float ls = warp_sum(e0 + e1);
+        const float csum = warp_sum(e0 * d0 + e1 * d1);
+        if (lane == 0) {
+          runl[h] = runl[h] * a + ls;
+          runc[h] = runc[h] * a + csum;
+          runm[h] = m_new;
+          alph[h] = a;
         }
       }
+      __syncthreads();
+      // A_h[d] = sum_j e_hj dP_hj K_jd, B_h[d] = sum_j e_hj K_jd (max-rescaled)
+      if (c_on) {
+        const unsigned char *Kt = ktile(st);
+        float al[GMAX];
+        ld_heads<GMAX>(alph, al);
+#pragma unroll
+        for (int h = 0; h < GMAX; ++h)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            accA[h][i] *= al[h];
+            accB[h][i] *= al[h];
+          }
+        for (int r = rsp; r < rows_valid; r += RS) {
+          const float4 kv = load4(elem(Kt, r, 4 * dc), static_cast<KV *>(nullptr));
+          float e[GMAX], w[GMAX];
+          ld_heads<GMAX>(etile + r * GMAX, e);
+          ld_heads<GMAX>(edp + r * GMAX, w);
+#pragma unroll
+          for (int h = 0; h < GMAX; ++h) {
+            accA[h][0] = fmaf(w[h], kv.x, accA[h][0]); accA[h][1] = fmaf(w[h], kv.y, accA[h][1]);
+            accA[h][2] = fmaf(w[h], kv.z, accA[h][2]); accA[h][3] = fmaf(w[h], kv.w, accA[h][3]);
+            accB[h][0] = fmaf(e[h], kv.x, accB[h][0]); accB[h][1] = fmaf(e[h], kv.y, accB[h][1]);
+            accB[h][2] = fmaf(e[h], kv.z, accB[h][2]); accB[h][3] = fmaf(e[h], kv.w, accB[h][3]);
+          }
+        }
+      }
+      __syncthreads();
+      if (tid == 0 && t + kStages < ntiles) {
+        fence_proxy_async_smem();
+        issue(t + kStages);
+      }
     }
-    __syncthreads();
-    if (tid == 0 && t + kStages < ntiles) {
-      fence_proxy_async_smem();
-      issue(t + kStages);
-    }
-  }
-
-  // ======================= publish partials ================================
-  // row-split partials -> scratch (the K/V tiles are consumed), summed in a
-  // fixed order so results do not depend on scheduling
-  {
+    // row-split partials -> scratch (the tiles are consumed), summed in a
+    // fixed order so results do not depend on scheduling
     float *sa = reinterpret_cast<float *>(smem + L.kv);
     float *sb = sa + RS * G * D;
     if (c_on) {
@@ -533,19 +541,19 @@ __global__ void __launch_bounds__(kThreads, GMAX >= 8 ? 1 : 2)
   }
   __syncthreads();
 
-  // P and dS of this CTA's keys, in place of the score and dP
+  // P and scale * dS of this CTA's keys, in place of the score and dP
   for (int i = tid; i < GMAX * nkeys; i += kThreads) {
     const int h = i & (GMAX - 1);
     if (h < G) {
       const float4 g = glob[h];
       const float P = expf(sbuf[i] - g.x) * g.y;
       sbuf[i] = P;
-      pbuf[i] = P * (pbuf[i] - g.z);
+      pbuf[i] = p.scale * P * (pbuf[i] - g.z);
     }
   }
   __syncthreads();
 
-  // ======================= phase 2: dK / dV rows ===========================
+  // ======================= phase 2: dK / dV rows (and dq partials) =========
   {
     const int F4 = D >> 2;                                  // float4 per output row
     int olog = 0;
@@ -554,12 +562,14 @@ __global__ void __launch_bounds__(kThreads, GMAX >= 8 ? 1 : 2)
     const int osub = lane & (olpr - 1), ogrp = lane >> olog;
     const int orows_w = 32 >> olog;
     const int npass = (F4 + 31) / 32;
+    float *red = reinterpret_cast<float *>(smem + L.kv + kStages * tile_bytes);   // V tiles: consumed
     for (int pass = 0; pass < npass; ++pass) {
       const int f = osub + 32 * pass;
       const bool on = f < F4;
-      float4 qo[GMAX], go[GMAX];
+      float4 qo[GMAX], go[GMAX], aq[GMAX];
 #pragma unroll
       for (int h = 0; h < GMAX; ++h) {
+        aq[h] = make_float4(0.f, 0.f, 0.f, 0.f);
         if (on && h < G) {
           qo[h] = *reinterpret_cast<const float4 *>(p.q + qrow0 + static_cast<size_t>(h) * D + 4 * f);
           go[h] = *reinterpret_cast<const float4 *>(p.dout + qrow0 + static_cast<size_t>(h) * D + 4 * f);
@@ -572,6 +582,8 @@ __global__ void __launch_bounds__(kThreads, GMAX >= 8 ? 1 : 2)
         float Ph[GMAX], dSh[GMAX];
         ld_heads<GMAX>(sbuf + j * GMAX, Ph);
         ld_heads<GMAX>(pbuf + j * GMAX, dSh);
+        float4 kv = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (resident && on) kv = load4(elem(ktile(j / kTile), j % kTile, 4 * f), static_cast<KV *>(nullptr));
 #pragma unroll
         for (int h = 0; h < GMAX; ++h) {
           if (h < G) {
@@ -580,17 +592,47 @@ __global__ void __launch_bounds__(kThreads, GMAX >= 8 ? 1 : 2)
             ak.z = fmaf(dS, qo[h].z, ak.z); ak.w = fmaf(dS, qo[h].w, ak.w);
             av.x = fmaf(P, go[h].x, av.x);  av.y = fmaf(P, go[h].y, av.y);
             av.z = fmaf(P, go[h].z, av.z);  av.w = fmaf(P, go[h].w, av.w);
+            if (resident) {
+              aq[h].x = fmaf(dS, kv.x, aq[h].x); aq[h].y = fmaf(dS, kv.y, aq[h].y);
+              aq[h].z = fmaf(dS, kv.z, aq[h].z); aq[h].w = fmaf(dS, kv.w, aq[h].w);
+            }
           }
         }
-        ak.x *= p.scale; ak.y *= p.scale; ak.z *= p.scale; ak.w *= p.scale;
         if (on) {
           const size_t o = ((static_cast<size_t>(b) * p.S + key0 + j) * p.Hkv + kvh) * D + 4 * f;
           st_cs_f4(p.dk + o, ak);
           st_cs_f4(p.dv + o, av);
         }
       }
+      if (resident) {
+        // sum the row groups of the warp, then one partial per warp
+        for (int o = olpr; o < 32; o <<= 1) {
+#pragma unroll
+          for (int h = 0; h < GMAX; ++h) {
+            aq[h].x += __shfl_xor_sync(0xffffffffu, aq[h].x, o);
+            aq[h].y += __shfl_xor_sync(0xffffffffu, aq[h].y, o);
+            aq[h].z += __shfl_xor_sync(0xffffffffu, aq[h].z, o);
+            aq[h].w += __shfl_xor_sync(0xffffffffu, aq[h].w, o);
+          }
+        }
+        if (ogrp == 0 && on) {
+#pragma unroll
+          for (int h = 0; h < GMAX; ++h)
+            if (h < G) *reinterpret_cast<float4 *>(red + (warp * G + h) * D + 4 * f) = aq[h];
+        }
+      }
+    }
+    if (resident) {
+      __syncthreads();
+      for (int idx = tid; idx < G * D; idx += kThreads) {
+        float a = 0.f;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) a += red[w * G * D + idx];
+        xa[idx] = a;
+      }
     }
   }
+  cluster.sync();   // dq partials visible cluster-wide
 
   // ======================= dq: rotary pairs spread over the cluster ========
   {
@@ -599,20 +641,34 @@ __global__ void __launch_bounds__(kThreads, GMAX >= 8 ? 1 : 2)
     for (int pr = tid * p.ncl + rank; pr < np; pr += kThreads * p.ncl) {
       const int h = pr / half, pi = pr - h * half;
       const int idx = h * D + 2 * pi;
-      float a0 = 0.f, a1 = 0.f, b0 = 0.f, b1 = 0.f;
+      float y0, y1;
+      if (resident) {
+        y0 = 0.f;
+        y1 = 0.f;
 #pragma unroll
-      for (int r = 0; r < kMaxCluster; ++r) {
-        if (r < p.ncl) {
-          const float w = rsc[r * kMaxG + h];
-          const float2 ra = *reinterpret_cast<const float2 *>(cluster.map_shared_rank(xa, r) + idx);
-          const float2 rb = *reinterpret_cast<const float2 *>(cluster.map_shared_rank(xb, r) + idx);
-          a0 = fmaf(w, ra.x, a0); a1 = fmaf(w, ra.y, a1);
-          b0 = fmaf(w, rb.x, b0); b1 = fmaf(w, rb.y, b1);
+        for (int r = 0; r < kMaxCluster; ++r) {
+          if (r < p.ncl) {
+            const float2 ra = *reinterpret_cast<const float2 *>(cluster.map_shared_rank(xa, r) + idx);
+            y0 += ra.x;
+            y1 += ra.y;
+          }
         }
+      } else {
+        float a0 = 0.f, a1 = 0.f, b0 = 0.f, b1 = 0.f;
+#pragma unroll
+        for (int r = 0; r < kMaxCluster; ++r) {
+          if (r < p.ncl) {
+            const float w = rsc[r * kMaxG + h];
+            const float2 ra = *reinterpret_cast<const float2 *>(cluster.map_shared_rank(xa, r) + idx);
+            const float2 rb = *reinterpret_cast<const float2 *>(cluster.map_shared_rank(xb, r) + idx);
+            a0 = fmaf(w, ra.x, a0); a1 = fmaf(w, ra.y, a1);
+            b0 = fmaf(w, rb.x, b0); b1 = fmaf(w, rb.y, b1);
+          }
+        }
+        const float4 g = glob[h];
+        y0 = p.scale * (a0 - g.z * b0) * g.y;
+        y1 = p.scale * (a1 - g.z * b1) * g.y;
       }
-      const float4 g = glob[h];
-      const float y0 = p.scale * (a0 - g.z * b0) * g.y;
-      const float y1 = p.scale * (a1 - g.z * b1) * g.y;
       float z0 = y0, z1 = y1;
       if (p.rope) {
         const float c = p.rcos[pi], s = p.rsin[pi];
@@ -625,10 +681,10 @@ __global__ void __launch_bounds__(kThreads, GMAX >= 8 ? 1 : 2)
   cluster.sync();   // peers' shared memory stays alive until every CTA has read it
 }
 
-template <typename KV, int GMAX, bool SWZ>
+template <typename KV, int GMAX, int DT>
 cudaError_t launch_typed(const CUtensorMap &tk, const CUtensorMap &tv, const DecodeParams &p, int smem,
                          cudaStream_t st) {
-  auto kern = decode_bwd_kernel<KV, GMAX, SWZ>;
+  auto kern = decode_bwd_kernel<KV, GMAX, DT>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -646,14 +702,14 @@ cudaError_t launch_typed(const CUtensorMap &tk, const CUtensorMap &tv, const Dec
   return cudaLaunchKernelEx(&cfg, kern, tk, tv, p);
 }
 
-template <typename KV, bool SWZ>
+template <typename KV, int DT>
 cudaError_t launch_g(int gmax, const CUtensorMap &tk, const CUtensorMap &tv, const DecodeParams &p, int smem,
                      cudaStream_t st) {
   switch (gmax) {
-    case 1: return launch_typed<KV, 1, SWZ>(tk, tv, p, smem, st);
-    case 2: return launch_typed<KV, 2, SWZ>(tk, tv, p, smem, st);
-    case 4: return launch_typed<KV, 4, SWZ>(tk, tv, p, smem, st);
-    default: return launch_typed<KV, 8, SWZ>(tk, tv, p, smem, st);
+    case 1: return launch_typed<KV, 1, DT>(tk, tv, p, smem, st);
+    case 2: return launch_typed<KV, 2, DT>(tk, tv, p, smem, st);
+    case 4: return launch_typed<KV, 4, DT>(tk, tv, p, smem, st);
+    default: return launch_typed<KV, 8, DT>(tk, tv, p, smem, st);
   }
 }
 
@@ -669,21 +725,23 @@ cudaError_t launch_attn_bwd_decode(const float *q, const void *k, const void *v,
     *why = "row width";
     return cudaErrorNotSupported;
   }
-  const bool swz = rowbytes % 128 == 0;            // 128B-swizzled tiles, quarter-row lanes
-  int lpr_log2 = 0;
-  while ((16 << lpr_log2) < rowbytes) ++lpr_log2;  // fallback: lanes per row (16 B each), power of two
   if (Hkv > 65535 || B > 65535) {
     *why = "B or Hkv > 65535";
     return cudaErrorNotSupported;
   }
+  int lpr_log2 = 0;
+  while ((16 << lpr_log2) < rowbytes) ++lpr_log2;  // generic: lanes per row (16 B each), power of two
   const int G = Hq / Hkv;
   const int gmax = G <= 1 ? 1 : G <= 2 ? 2 : G <= 4 ? 4 : 8;
-  int rs_log2 = 0;                                 // row splits of the dq partial sums
+  int rs_log2 = 0;                                 // streaming: row splits of the dq partial sums
   while ((1 << (rs_log2 + 1)) <= kTile && (D / 4) << (rs_log2 + 1) <= kThreads) ++rs_log2;
   const int tiles = (S + kTile - 1) / kTile;
   int ncl = tiles < kMaxCluster ? tiles : kMaxCluster;
   const int chunk = ((tiles + ncl - 1) / ncl) * kTile;
   ncl = (S + chunk - 1) / chunk;                   // every CTA owns at least one key
+  const bool resident = chunk <= kStages * kTile;
+  // specialised head dims: bf16 rows of 128 / 256 / 512 bytes with a resident chunk
+  const int dt = (kv_bf16 && resident && (D == 64 || D == 128 || D == 256)) ? D : 0;
   const Layout L(G, gmax, D, chunk, rowbytes, 1 << rs_log2);
   const int smem = L.total + 1024;                 // + alignment slack
   if (smem > 227 * 1024) {
@@ -694,7 +752,8 @@ cudaError_t launch_attn_bwd_decode(const float *q, const void *k, const void *v,
   DecodeParams p;
   p.q = q; p.dout = dout; p.dq = dq; p.dk = dk; p.dv = dv;
   p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.S = S; p.D = D; p.G = G;
-  p.chunk = chunk; p.ncl = ncl; p.lpr_log2 = lpr_log2; p.rs_log2 = rs_log2; p.rowbytes = rowbytes;
+  p.chunk = chunk; p.ncl = ncl; p.resident = resident ? 1 : 0;
+  p.lpr_log2 = lpr_log2; p.rs_log2 = rs_log2; p.rowbytes = rowbytes;
   p.scale = scale;
   p.rope = rope_base > 0.0 && q_pos >= 0;
   for (int i = 0; i < 128; ++i) {
@@ -714,17 +773,21 @@ cudaError_t launch_attn_bwd_decode(const float *q, const void *k, const void *v,
                             static_cast<uint64_t>(B)};
   const uint64_t strides[3] = {static_cast<uint64_t>(rowbytes), static_cast<uint64_t>(Hkv) * rowbytes,
                                static_cast<uint64_t>(S) * Hkv * rowbytes};
-  const uint32_t box[4] = {static_cast<uint32_t>(swz ? 128 / es : D), 1, kTile, 1};
-  const CUtensorMapDataType dt = kv_bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
-  const CUtensorMapSwizzle sw = swz ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE;
-  if (!encode_tiled(&tk, dt, 4, k, dims, strides, box, sw, why) ||
-      !encode_tiled(&tv, dt, 4, v, dims, strides, box, sw, why))
+  const uint32_t box[4] = {static_cast<uint32_t>(dt ? 128 / es : D), 1, kTile, 1};
+  const CUtensorMapDataType dtp = kv_bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+  const CUtensorMapSwizzle sw = dt ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE;
+  if (!encode_tiled(&tk, dtp, 4, k, dims, strides, box, sw, why) ||
+      !encode_tiled(&tv, dtp, 4, v, dims, strides, box, sw, why))
     return cudaErrorInvalidValue;
 
-  if (kv_bf16)
-    return swz ? launch_g<__nv_bfloat16, true>(gmax, tk, tv, p, smem, st)
-               : launch_g<__nv_bfloat16, false>(gmax, tk, tv, p, smem, st);
-  return swz ? launch_g<float, true>(gmax, tk, tv, p, smem, st) : launch_g<float, false>(gmax, tk, tv, p, smem, st);
+  switch (dt) {
+    case 64: return launch_g<__nv_bfloat16, 64>(gmax, tk, tv, p, smem, st);
+    case 128: return launch_g<__nv_bfloat16, 128>(gmax, tk, tv, p, smem, st);
+    case 256: return launch_g<__nv_bfloat16, 256>(gmax, tk, tv, p, smem, st);
+    default:
+      return kv_bf16 ? launch_g<__nv_bfloat16, 0>(gmax, tk, tv, p, smem, st)
+                     : launch_g<float, 0>(gmax, tk, tv, p, smem, st);
+  }
 }
 
 }  // namespace abw
