@@ -21,7 +21,7 @@
 // Two shapes of the same kernel:
 //  * resident (a CTA's chunk fits its two TMA stages -- e.g. 1024 keys over 8
 //    CTAs): the K tiles stay in shared memory, so the CTA's share of dq is
-//    accumulated with the final dS in the same pass that writes dK/dV.  With
+//    summed with the final dS straight from them.  With
 //    a bf16 head dim of 64, 128 or 256 the tiles arrive 128B-swizzled and
 //    each key row is split over 4 lanes, every lane owning a quarter of the
 //    head dim, with scale*q and dout broadcast from shared memory
@@ -553,83 +553,38 @@ __global__ void __launch_bounds__(kThreads, GMAX >= 8 ? 1 : 2)
   }
   __syncthreads();
 
-  // ======================= phase 2: dK / dV rows (and dq partials) =========
-  {
-    const int F4 = D >> 2;                                  // float4 per output row
-    int olog = 0;
-    while ((1 << olog) < F4 && olog < 5) ++olog;
-    const int olpr = 1 << olog;                             // lanes per row (<= 32)
-    const int osub = lane & (olpr - 1), ogrp = lane >> olog;
-    const int orows_w = 32 >> olog;
-    const int npass = (F4 + 31) / 32;
-    float *red = reinterpret_cast<float *>(smem + L.kv + kStages * tile_bytes);   // V tiles: consumed
-    for (int pass = 0; pass < npass; ++pass) {
-      const int f = osub + 32 * pass;
-      const bool on = f < F4;
-      float4 qo[GMAX], go[GMAX], aq[GMAX];
+  // ======================= dq partial of this CTA (resident K) =============
+  // Done before any dK/dV store is issued, so the cluster barrier that
+  // publishes it does not wait for those stores to drain.
+  if (resident) {
+    const int dc = tid % D4, rsp = tid / D4;           // (row split, 4-dim chunk)
+    // row splits: all threads, capped so nrs * G * D floats fit the (consumed)
+    // V tiles, which hold 2 * kTile * D * ES bytes
+    const int nrs = min(kThreads / D4, 32 * ES / GMAX);
+    float *red = reinterpret_cast<float *>(smem + L.kv + kStages * tile_bytes);
+    float4 aq[GMAX];
+#pragma unroll
+    for (int h = 0; h < GMAX; ++h) aq[h] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int j = rsp; j < nkeys && rsp < nrs; j += nrs) {
+      const float4 kv = load4(elem(ktile(j / kTile), j % kTile, 4 * dc), static_cast<KV *>(nullptr));
+      float dSh[GMAX];
+      ld_heads<GMAX>(pbuf + j * GMAX, dSh);
 #pragma unroll
       for (int h = 0; h < GMAX; ++h) {
-        aq[h] = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (on && h < G) {
-          qo[h] = *reinterpret_cast<const float4 *>(p.q + qrow0 + static_cast<size_t>(h) * D + 4 * f);
-          go[h] = *reinterpret_cast<const float4 *>(p.dout + qrow0 + static_cast<size_t>(h) * D + 4 * f);
-        } else {
-          qo[h] = go[h] = make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-      }
-      for (int j = warp * orows_w + ogrp; j < nkeys; j += kWarps * orows_w) {
-        float4 ak = make_float4(0.f, 0.f, 0.f, 0.f), av = ak;
-        float Ph[GMAX], dSh[GMAX];
-        ld_heads<GMAX>(sbuf + j * GMAX, Ph);
-        ld_heads<GMAX>(pbuf + j * GMAX, dSh);
-        float4 kv = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (resident && on) kv = load4(elem(ktile(j / kTile), j % kTile, 4 * f), static_cast<KV *>(nullptr));
-#pragma unroll
-        for (int h = 0; h < GMAX; ++h) {
-          if (h < G) {
-            const float P = Ph[h], dS = dSh[h];
-            ak.x = fmaf(dS, qo[h].x, ak.x); ak.y = fmaf(dS, qo[h].y, ak.y);
-            ak.z = fmaf(dS, qo[h].z, ak.z); ak.w = fmaf(dS, qo[h].w, ak.w);
-            av.x = fmaf(P, go[h].x, av.x);  av.y = fmaf(P, go[h].y, av.y);
-            av.z = fmaf(P, go[h].z, av.z);  av.w = fmaf(P, go[h].w, av.w);
-            if (resident) {
-              aq[h].x = fmaf(dS, kv.x, aq[h].x); aq[h].y = fmaf(dS, kv.y, aq[h].y);
-              aq[h].z = fmaf(dS, kv.z, aq[h].z); aq[h].w = fmaf(dS, kv.w, aq[h].w);
-            }
-          }
-        }
-        if (on) {
-          const size_t o = ((static_cast<size_t>(b) * p.S + key0 + j) * p.Hkv + kvh) * D + 4 * f;
-          st_cs_f4(p.dk + o, ak);
-          st_cs_f4(p.dv + o, av);
-        }
-      }
-      if (resident) {
-        // sum the row groups of the warp, then one partial per warp
-        for (int o = olpr; o < 32; o <<= 1) {
-#pragma unroll
-          for (int h = 0; h < GMAX; ++h) {
-            aq[h].x += __shfl_xor_sync(0xffffffffu, aq[h].x, o);
-            aq[h].y += __shfl_xor_sync(0xffffffffu, aq[h].y, o);
-            aq[h].z += __shfl_xor_sync(0xffffffffu, aq[h].z, o);
-            aq[h].w += __shfl_xor_sync(0xffffffffu, aq[h].w, o);
-          }
-        }
-        if (ogrp == 0 && on) {
-#pragma unroll
-          for (int h = 0; h < GMAX; ++h)
-            if (h < G) *reinterpret_cast<float4 *>(red + (warp * G + h) * D + 4 * f) = aq[h];
-        }
+        aq[h].x = fmaf(dSh[h], kv.x, aq[h].x); aq[h].y = fmaf(dSh[h], kv.y, aq[h].y);
+        aq[h].z = fmaf(dSh[h], kv.z, aq[h].z); aq[h].w = fmaf(dSh[h], kv.w, aq[h].w);
       }
     }
-    if (resident) {
-      __syncthreads();
-      for (int idx = tid; idx < G * D; idx += kThreads) {
-        float a = 0.f;
+    if (rsp < nrs) {
 #pragma unroll
-        for (int w = 0; w < kWarps; ++w) a += red[w * G * D + idx];
-        xa[idx] = a;
-      }
+      for (int h = 0; h < GMAX; ++h)
+        if (h < G) *reinterpret_cast<float4 *>(red + (rsp * G + h) * D + 4 * dc) = aq[h];
+    }
+    __syncthreads();
+    for (int idx = tid; idx < G * D; idx += kThreads) {
+      float a = 0.f;
+      for (int r = 0; r < nrs; ++r) a += red[r * G * D + idx];
+      xa[idx] = a;
     }
   }
   cluster.sync();   // dq partials visible cluster-wide
@@ -678,7 +633,57 @@ __global__ void __launch_bounds__(kThreads, GMAX >= 8 ? 1 : 2)
       *reinterpret_cast<float2 *>(p.dq + qrow0 + idx) = make_float2(z0, z1);
     }
   }
-  cluster.sync();   // peers' shared memory stays alive until every CTA has read it
+
+  // ======================= phase 2: dK / dV rows ===========================
+  {
+    const int F4 = D >> 2;                                  // float4 per output row
+    int olog = 0;
+    while ((1 << olog) < F4 && olog < 5) ++olog;
+    const int olpr = 1 << olog;                             // lanes per row (<= 32)
+    const int osub = lane & (olpr - 1), ogrp = lane >> olog;
+    const int orows_w = 32 >> olog;
+    const int npass = (F4 + 31) / 32;
+    for (int pass = 0; pass < npass; ++pass) {
+      const int f = osub + 32 * pass;
+      const bool on = f < F4;
+      float4 qo[GMAX], go[GMAX];
+#pragma unroll
+      for (int h = 0; h < GMAX; ++h) {
+        if (on && h < G) {
+          qo[h] = *reinterpret_cast<const float4 *>(p.q + qrow0 + static_cast<size_t>(h) * D + 4 * f);
+          go[h] = *reinterpret_cast<const float4 *>(p.dout + qrow0 + static_cast<size_t>(h) * D + 4 * f);
+        } else {
+          qo[h] = go[h] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+      }
+      for (int j = warp * orows_w + ogrp; j < nkeys; j += kWarps * orows_w) {
+        float4 ak = make_float4(0.f, 0.f, 0.f, 0.f), av = ak;
+        float Ph[GMAX], dSh[GMAX];
+        ld_heads<GMAX>(sbuf + j * GMAX, Ph);
+        ld_heads<GMAX>(pbuf + j * GMAX, dSh);
+#pragma unroll
+        for (int h = 0; h < GMAX; ++h) {
+          if (h < G) {
+            const float P = Ph[h], dS = dSh[h];
+            ak.x = fmaf(dS, qo[h].x, ak.x); ak.y = fmaf(dS, qo[h].y, ak.y);
+            ak.z = fmaf(dS, qo[h].z, ak.z); ak.w = fmaf(dS, qo[h].w, ak.w);
+            av.x = fmaf(P, go[h].x, av.x);  av.y = fmaf(P, go[h].y, av.y);
+            av.z = fmaf(P, go[h].z, av.z);  av.w = fmaf(P, go[h].w, av.w);
+          }
+        }
+        if (on) {
+          const size_t o = ((static_cast<size_t>(b) * p.S + key0 + j) * p.Hkv + kvh) * D + 4 * f;
+          st_cs_f4(p.dk + o, ak);
+          st_cs_f4(p.dv + o, av);
+        }
+      }
+    }
+  }
+  // Peers' shared memory must stay alive until every CTA has read it; this
+  // barrier orders no memory (the remote reads completed before the arrive),
+  // so it is relaxed and does not wait for the dK/dV stores to drain.
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+  asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
 }
 
 template <typename KV, int GMAX, int DT>
