@@ -73,6 +73,9 @@ def test_decode_tiny_single_head(abw):
     W.DecodeShape(B=1, Hq=2, Hkv=1, S=1, D=16),                                     # one key
     W.DecodeShape(B=2, Hq=4, Hkv=2, S=77, D=256),                                   # 512-byte rows
     W.DecodeShape(B=1, Hq=2, Hkv=2, S=33, D=8, kv_dtype=torch.float32),             # 32-byte rows
+    W.DecodeShape(B=2, Hq=16, Hkv=2, S=128, D=64, rope_base=10000.0, q_pos=127),    # swizzled D=64, G=8
+    W.DecodeShape(B=1, Hq=2, Hkv=1, S=1024, D=64),                                  # swizzled D=64, G=2
+    W.DecodeShape(B=1, Hq=8, Hkv=8, S=3000, D=64, kv_dtype=torch.float32),          # fp32 streaming, G=1
 ])
 def test_decode_shapes(abw, shape):
     run_and_compare(abw, shape, seed=shape.S + shape.D)
