@@ -34,6 +34,8 @@
 #include <cooperative_groups.h>
 #include <math.h>
 
+#include <type_traits>
+
 #include "abw_host.h"
 
 namespace cg = cooperative_groups;
@@ -292,48 +294,66 @@ __global__ void __launch_bounds__(kThreads, GMAX >= 8 ? 1 : 2)
   }
   const int wmask = (lpr > NV ? lpr / NV : 1) - 1;   // generic: lanes of a group holding identical sums
 
-  // (a) s_hj = (scale q_h) . K_j and dP_hj = dout_h . V_j for one tile
-  auto dots = [&](int st, int jt, int rows_valid) {
-    const unsigned char *Kt = ktile(st), *Vt = vtile(st);
-    if constexpr (SWZ) {
-      constexpr int DPL = DT / 4;
-      constexpr int NCH = DPL * ES / 16;
-      const int r = tid >> 2, pp = tid & 3;             // 64 rows x 4 quarter-rows
-      float val[NV];
+  // (a) s_hj = (scale q_h) . K_j and dP_hj = dout_h . V_j.
+  // Swizzled path: thread (r, pp) owns quarter pp of row r of NR tiles
+  // (st0, st0 + 1, ...), so each broadcast q/dout load feeds NR rows; the dot
+  // products use packed fp32x2 FMAs and a 4-lane reduce-scatter.
+  auto dots_swz = [&](auto nr_tag, int st0, int rows0, int rows1) {
+    constexpr int NR = decltype(nr_tag)::value;
+    constexpr int DPL = (DT > 0 ? DT : 4) / 4;
+    constexpr int NCH = DPL * ES / 16;
+    const int r = tid >> 2, pp = tid & 3;             // 64 rows x 4 quarter-rows
+    float2 acc[NR][NV];
 #pragma unroll
-      for (int i = 0; i < NV; ++i) val[i] = 0.f;
-      const float *qp = qsm + pp * (DPL + 4);
-      const float *dp_ = dsm + pp * (DPL + 4);
+    for (int rr = 0; rr < NR; ++rr)
 #pragma unroll
-      for (int c = 0; c < NCH; ++c) {
-        const int d0 = pp * DPL + c * EPL;
-        float kf[EPL], vf[EPL];
-        load16(elem(Kt, r, d0), kf);
-        load16(elem(Vt, r, d0), vf);
+      for (int i = 0; i < NV; ++i) acc[rr][i] = make_float2(0.f, 0.f);
+    const float *qp = qsm + pp * (DPL + 4);
+    const float *dp_ = dsm + pp * (DPL + 4);
 #pragma unroll
-        for (int h = 0; h < GMAX; ++h) {
+    for (int c = 0; c < NCH; ++c) {
+      const int d0 = pp * DPL + c * 8;
+      float2 kf[NR][4], vf[NR][4];
 #pragma unroll
-          for (int e = 0; e < EPL; e += 4) {
-            const float4 q4 = *reinterpret_cast<const float4 *>(qp + h * 4 * (DPL + 4) + c * EPL + e);
-            const float4 d4 = *reinterpret_cast<const float4 *>(dp_ + h * 4 * (DPL + 4) + c * EPL + e);
-            val[h] = fmaf(q4.x, kf[e], val[h]);
-            val[h] = fmaf(q4.y, kf[e + 1], val[h]);
-            val[h] = fmaf(q4.z, kf[e + 2], val[h]);
-            val[h] = fmaf(q4.w, kf[e + 3], val[h]);
-            val[GMAX + h] = fmaf(d4.x, vf[e], val[GMAX + h]);
-            val[GMAX + h] = fmaf(d4.y, vf[e + 1], val[GMAX + h]);
-            val[GMAX + h] = fmaf(d4.z, vf[e + 2], val[GMAX + h]);
-            val[GMAX + h] = fmaf(d4.w, vf[e + 3], val[GMAX + h]);
-          }
+      for (int rr = 0; rr < NR; ++rr) {
+        const uint4 ku = *reinterpret_cast<const uint4 *>(elem(ktile(st0 + rr), r, d0));
+        const uint4 vu = *reinterpret_cast<const uint4 *>(elem(vtile(st0 + rr), r, d0));
+        kf[rr][0] = make_float2(bf16_lo(ku.x), bf16_hi(ku.x)); kf[rr][1] = make_float2(bf16_lo(ku.y), bf16_hi(ku.y));
+        kf[rr][2] = make_float2(bf16_lo(ku.z), bf16_hi(ku.z)); kf[rr][3] = make_float2(bf16_lo(ku.w), bf16_hi(ku.w));
+        vf[rr][0] = make_float2(bf16_lo(vu.x), bf16_hi(vu.x)); vf[rr][1] = make_float2(bf16_lo(vu.y), bf16_hi(vu.y));
+        vf[rr][2] = make_float2(bf16_lo(vu.z), bf16_hi(vu.z)); vf[rr][3] = make_float2(bf16_lo(vu.w), bf16_hi(vu.w));
+      }
+#pragma unroll
+      for (int h = 0; h < GMAX; ++h) {
+        const float4 qa = *reinterpret_cast<const float4 *>(qp + h * 4 * (DPL + 4) + c * 8);
+        const float4 qb = *reinterpret_cast<const float4 *>(qp + h * 4 * (DPL + 4) + c * 8 + 4);
+        const float4 da = *reinterpret_cast<const float4 *>(dp_ + h * 4 * (DPL + 4) + c * 8);
+        const float4 db = *reinterpret_cast<const float4 *>(dp_ + h * 4 * (DPL + 4) + c * 8 + 4);
+#pragma unroll
+        for (int rr = 0; rr < NR; ++rr) {
+          acc[rr][h] = __ffma2_rn(make_float2(qa.x, qa.y), kf[rr][0], acc[rr][h]);
+          acc[rr][h] = __ffma2_rn(make_float2(qa.z, qa.w), kf[rr][1], acc[rr][h]);
+          acc[rr][h] = __ffma2_rn(make_float2(qb.x, qb.y), kf[rr][2], acc[rr][h]);
+          acc[rr][h] = __ffma2_rn(make_float2(qb.z, qb.w), kf[rr][3], acc[rr][h]);
+          acc[rr][GMAX + h] = __ffma2_rn(make_float2(da.x, da.y), vf[rr][0], acc[rr][GMAX + h]);
+          acc[rr][GMAX + h] = __ffma2_rn(make_float2(da.z, da.w), vf[rr][1], acc[rr][GMAX + h]);
+          acc[rr][GMAX + h] = __ffma2_rn(make_float2(db.x, db.y), vf[rr][2], acc[rr][GMAX + h]);
+          acc[rr][GMAX + h] = __ffma2_rn(make_float2(db.z, db.w), vf[rr][3], acc[rr][GMAX + h]);
         }
       }
+    }
+#pragma unroll
+    for (int rr = 0; rr < NR; ++rr) {
+      float val[NV];
+#pragma unroll
+      for (int i = 0; i < NV; ++i) val[i] = acc[rr][i].x + acc[rr][i].y;
       int idx0, nf;
       reduce_scatter<NV>(val, 4, pp, idx0, nf);
       // each of the 4 lanes keeps NV/4 sums (all scores or all dP, heads
       // idx0 % GMAX onward); with NV = 2, lanes 0 and 2 hold the two sums
       constexpr int NF = NV >= 4 ? NV / 4 : 1;
-      if (r < rows_valid && (NV >= 4 || (pp & 1) == 0)) {
-        float *dst = (idx0 < GMAX ? sbuf : pbuf) + (jt + r) * GMAX + (idx0 & (GMAX - 1));
+      if (r < (rr == 0 ? rows0 : rows1) && (NV >= 4 || (pp & 1) == 0)) {
+        float *dst = (idx0 < GMAX ? sbuf : pbuf) + ((st0 + rr) * kTile + r) * GMAX + (idx0 & (GMAX - 1));
         if constexpr (NF == 4) {
           *reinterpret_cast<float4 *>(dst) = make_float4(val[0], val[1], val[2], val[3]);
         } else if constexpr (NF == 2) {
@@ -342,6 +362,13 @@ __global__ void __launch_bounds__(kThreads, GMAX >= 8 ? 1 : 2)
           dst[0] = val[0];
         }
       }
+    }
+  };
+  // Generic path: a row split over `lpr` lanes of 16 bytes, q/dout in registers.
+  auto dots = [&](int st, int jt, int rows_valid) {
+    const unsigned char *Kt = ktile(st), *Vt = vtile(st);
+    if constexpr (SWZ) {
+      dots_swz(std::integral_constant<int, 1>{}, st, rows_valid, 0);
     } else {
       for (int r = warp * rows_per_warp + rgrp; r < kTile; r += rows_per_step) {
         float kf[EPL], vf[EPL];
@@ -383,9 +410,15 @@ __global__ void __launch_bounds__(kThreads, GMAX >= 8 ? 1 : 2)
   // ======================= phase 1 =========================================
   const int D4 = D >> 2;
   if (resident) {
-    for (int t = 0; t < ntiles; ++t) {
-      mbar_wait_or_flag(bar0 + t * 8, 0, p.wait);
-      dots(t, t * kTile, min(kTile, nkeys - t * kTile));
+    if (SWZ && ntiles == 2) {
+      mbar_wait_or_flag(bar0, 0, p.wait);
+      mbar_wait_or_flag(bar0 + 8, 0, p.wait);
+      dots_swz(std::integral_constant<int, 2>{}, 0, kTile, nkeys - kTile);
+    } else {
+      for (int t = 0; t < ntiles; ++t) {
+        mbar_wait_or_flag(bar0 + t * 8, 0, p.wait);
+        dots(t, t * kTile, min(kTile, nkeys - t * kTile));
+      }
     }
     __syncthreads();
     // chunk statistics per head (warp h): max, sum e, sum e dP
@@ -542,97 +575,95 @@ __global__ void __launch_bounds__(kThreads, GMAX >= 8 ? 1 : 2)
   __syncthreads();
 
   // P and scale * dS of this CTA's keys, in place of the score and dP
+  // (heads G .. GMAX-1 of the padded layout get 0, so later loops need no
+  // head predicate)
   for (int i = tid; i < GMAX * nkeys; i += kThreads) {
     const int h = i & (GMAX - 1);
+    float P = 0.f, dS = 0.f;
     if (h < G) {
       const float4 g = glob[h];
-      const float P = expf(sbuf[i] - g.x) * g.y;
-      sbuf[i] = P;
-      pbuf[i] = p.scale * P * (pbuf[i] - g.z);
+      P = expf(sbuf[i] - g.x) * g.y;
+      dS = p.scale * P * (pbuf[i] - g.z);
     }
+    sbuf[i] = P;
+    pbuf[i] = dS;
   }
   __syncthreads();
 
-  // ======================= dq partial of this CTA (resident K) =============
-  // Done before any dK/dV store is issued, so the cluster barrier that
-  // publishes it does not wait for those stores to drain.
+  // ======================= dq partial of this CTA ==========================
+  // Resident K: sum_j dS'_hj K_j over this CTA's keys, pushed into a slot of
+  // rank 0's (consumed) V tiles.  Streaming: rank 0 merges the running
+  // partials of every CTA now.  Either way this happens before any dK/dV
+  // store is issued, and the cluster barrier that publishes it is split: its
+  // arrive goes out here and its wait comes after the stores, so neither side
+  // stalls on the other.
+  float *slots = reinterpret_cast<float *>(smem + L.kv + kStages * tile_bytes);   // [ncl][G*D] in rank 0
+  const int half = D >> 1;
   if (resident) {
     const int dc = tid % D4, rsp = tid / D4;           // (row split, 4-dim chunk)
-    // row splits: all threads, capped so nrs * G * D floats fit the (consumed)
-    // V tiles, which hold 2 * kTile * D * ES bytes
+    // row splits, capped so nrs * G * D floats fit the K tiles once consumed
     const int nrs = min(kThreads / D4, 32 * ES / GMAX);
-    float *red = reinterpret_cast<float *>(smem + L.kv + kStages * tile_bytes);
-    float4 aq[GMAX];
+    float2 aq[GMAX][2];
 #pragma unroll
-    for (int h = 0; h < GMAX; ++h) aq[h] = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int j = rsp; j < nkeys && rsp < nrs; j += nrs) {
-      const float4 kv = load4(elem(ktile(j / kTile), j % kTile, 4 * dc), static_cast<KV *>(nullptr));
-      float dSh[GMAX];
-      ld_heads<GMAX>(pbuf + j * GMAX, dSh);
+    for (int h = 0; h < GMAX; ++h) aq[h][0] = aq[h][1] = make_float2(0.f, 0.f);
+    if (rsp < nrs) {
+      for (int j = rsp; j < nkeys; j += nrs) {
+        const float4 kv = load4(elem(ktile(j / kTile), j % kTile, 4 * dc), static_cast<KV *>(nullptr));
+        const float2 k01 = make_float2(kv.x, kv.y), k23 = make_float2(kv.z, kv.w);
+        float dSh[GMAX];
+        ld_heads<GMAX>(pbuf + j * GMAX, dSh);
 #pragma unroll
-      for (int h = 0; h < GMAX; ++h) {
-        aq[h].x = fmaf(dSh[h], kv.x, aq[h].x); aq[h].y = fmaf(dSh[h], kv.y, aq[h].y);
-        aq[h].z = fmaf(dSh[h], kv.z, aq[h].z); aq[h].w = fmaf(dSh[h], kv.w, aq[h].w);
+        for (int h = 0; h < GMAX; ++h) {
+          const float2 w = make_float2(dSh[h], dSh[h]);
+          aq[h][0] = __ffma2_rn(w, k01, aq[h][0]);
+          aq[h][1] = __ffma2_rn(w, k23, aq[h][1]);
+        }
       }
     }
+    __syncthreads();                                   // K tiles consumed
+    float *red = reinterpret_cast<float *>(smem + L.kv);
     if (rsp < nrs) {
 #pragma unroll
       for (int h = 0; h < GMAX; ++h)
-        if (h < G) *reinterpret_cast<float4 *>(red + (rsp * G + h) * D + 4 * dc) = aq[h];
+        if (h < G)
+          *reinterpret_cast<float4 *>(red + (rsp * G + h) * D + 4 * dc) =
+              make_float4(aq[h][0].x, aq[h][0].y, aq[h][1].x, aq[h][1].y);
     }
     __syncthreads();
+    float *dst0 = cluster.map_shared_rank(slots, 0) + rank * G * D;
     for (int idx = tid; idx < G * D; idx += kThreads) {
       float a = 0.f;
       for (int r = 0; r < nrs; ++r) a += red[r * G * D + idx];
-      xa[idx] = a;
+      dst0[idx] = a;
     }
-  }
-  cluster.sync();   // dq partials visible cluster-wide
-
-  // ======================= dq: rotary pairs spread over the cluster ========
-  {
-    const int half = D >> 1;
-    const int np = G * half;
-    for (int pr = tid * p.ncl + rank; pr < np; pr += kThreads * p.ncl) {
+  } else if (rank == 0) {
+    for (int pr = tid; pr < G * half; pr += kThreads) {
       const int h = pr / half, pi = pr - h * half;
       const int idx = h * D + 2 * pi;
-      float y0, y1;
-      if (resident) {
-        y0 = 0.f;
-        y1 = 0.f;
+      float a0 = 0.f, a1 = 0.f, b0 = 0.f, b1 = 0.f;
 #pragma unroll
-        for (int r = 0; r < kMaxCluster; ++r) {
-          if (r < p.ncl) {
-            const float2 ra = *reinterpret_cast<const float2 *>(cluster.map_shared_rank(xa, r) + idx);
-            y0 += ra.x;
-            y1 += ra.y;
-          }
+      for (int r = 0; r < kMaxCluster; ++r) {
+        if (r < p.ncl) {
+          const float w = rsc[r * kMaxG + h];
+          const float2 ra = *reinterpret_cast<const float2 *>(cluster.map_shared_rank(xa, r) + idx);
+          const float2 rb = *reinterpret_cast<const float2 *>(cluster.map_shared_rank(xb, r) + idx);
+          a0 = fmaf(w, ra.x, a0); a1 = fmaf(w, ra.y, a1);
+          b0 = fmaf(w, rb.x, b0); b1 = fmaf(w, rb.y, b1);
         }
-      } else {
-        float a0 = 0.f, a1 = 0.f, b0 = 0.f, b1 = 0.f;
-#pragma unroll
-        for (int r = 0; r < kMaxCluster; ++r) {
-          if (r < p.ncl) {
-            const float w = rsc[r * kMaxG + h];
-            const float2 ra = *reinterpret_cast<const float2 *>(cluster.map_shared_rank(xa, r) + idx);
-            const float2 rb = *reinterpret_cast<const float2 *>(cluster.map_shared_rank(xb, r) + idx);
-            a0 = fmaf(w, ra.x, a0); a1 = fmaf(w, ra.y, a1);
-            b0 = fmaf(w, rb.x, b0); b1 = fmaf(w, rb.y, b1);
-          }
-        }
-        const float4 g = glob[h];
-        y0 = p.scale * (a0 - g.z * b0) * g.y;
-        y1 = p.scale * (a1 - g.z * b1) * g.y;
       }
+      const float4 g = glob[h];
+      const float y0 = p.scale * (a0 - g.z * b0) * g.y;
+      const float y1 = p.scale * (a1 - g.z * b1) * g.y;
       float z0 = y0, z1 = y1;
       if (p.rope) {
-        const float c = p.rcos[pi], s = p.rsin[pi];
-        z0 = y0 * c + y1 * s;
-        z1 = -y0 * s + y1 * c;
+        const float c = p.rcos[pi], sn = p.rsin[pi];
+        z0 = y0 * c + y1 * sn;
+        z1 = -y0 * sn + y1 * c;
       }
       *reinterpret_cast<float2 *>(p.dq + qrow0 + idx) = make_float2(z0, z1);
     }
   }
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
 
   // ======================= phase 2: dK / dV rows ===========================
   {
@@ -646,44 +677,62 @@ __global__ void __launch_bounds__(kThreads, GMAX >= 8 ? 1 : 2)
     for (int pass = 0; pass < npass; ++pass) {
       const int f = osub + 32 * pass;
       const bool on = f < F4;
-      float4 qo[GMAX], go[GMAX];
+      float2 qo[GMAX][2], go[GMAX][2];
 #pragma unroll
       for (int h = 0; h < GMAX; ++h) {
+        float4 a = make_float4(0.f, 0.f, 0.f, 0.f), c = a;
         if (on && h < G) {
-          qo[h] = *reinterpret_cast<const float4 *>(p.q + qrow0 + static_cast<size_t>(h) * D + 4 * f);
-          go[h] = *reinterpret_cast<const float4 *>(p.dout + qrow0 + static_cast<size_t>(h) * D + 4 * f);
-        } else {
-          qo[h] = go[h] = make_float4(0.f, 0.f, 0.f, 0.f);
+          a = *reinterpret_cast<const float4 *>(p.q + qrow0 + static_cast<size_t>(h) * D + 4 * f);
+          c = *reinterpret_cast<const float4 *>(p.dout + qrow0 + static_cast<size_t>(h) * D + 4 * f);
         }
+        qo[h][0] = make_float2(a.x, a.y); qo[h][1] = make_float2(a.z, a.w);
+        go[h][0] = make_float2(c.x, c.y); go[h][1] = make_float2(c.z, c.w);
       }
+      float *dkp = p.dk + ((static_cast<size_t>(b) * p.S + key0) * p.Hkv + kvh) * D + 4 * f;
+      float *dvp = p.dv + ((static_cast<size_t>(b) * p.S + key0) * p.Hkv + kvh) * D + 4 * f;
+      const size_t rstride = static_cast<size_t>(p.Hkv) * D;
       for (int j = warp * orows_w + ogrp; j < nkeys; j += kWarps * orows_w) {
-        float4 ak = make_float4(0.f, 0.f, 0.f, 0.f), av = ak;
+        float2 k0 = make_float2(0.f, 0.f), k1 = k0, v0 = k0, v1 = k0;
         float Ph[GMAX], dSh[GMAX];
         ld_heads<GMAX>(sbuf + j * GMAX, Ph);
         ld_heads<GMAX>(pbuf + j * GMAX, dSh);
 #pragma unroll
         for (int h = 0; h < GMAX; ++h) {
-          if (h < G) {
-            const float P = Ph[h], dS = dSh[h];
-            ak.x = fmaf(dS, qo[h].x, ak.x); ak.y = fmaf(dS, qo[h].y, ak.y);
-            ak.z = fmaf(dS, qo[h].z, ak.z); ak.w = fmaf(dS, qo[h].w, ak.w);
-            av.x = fmaf(P, go[h].x, av.x);  av.y = fmaf(P, go[h].y, av.y);
-            av.z = fmaf(P, go[h].z, av.z);  av.w = fmaf(P, go[h].w, av.w);
-          }
+          const float2 ds = make_float2(dSh[h], dSh[h]), pw = make_float2(Ph[h], Ph[h]);
+          k0 = __ffma2_rn(ds, qo[h][0], k0);
+          k1 = __ffma2_rn(ds, qo[h][1], k1);
+          v0 = __ffma2_rn(pw, go[h][0], v0);
+          v1 = __ffma2_rn(pw, go[h][1], v1);
         }
         if (on) {
-          const size_t o = ((static_cast<size_t>(b) * p.S + key0 + j) * p.Hkv + kvh) * D + 4 * f;
-          st_cs_f4(p.dk + o, ak);
-          st_cs_f4(p.dv + o, av);
+          st_cs_f4(dkp + j * rstride, make_float4(k0.x, k0.y, k1.x, k1.y));
+          st_cs_f4(dvp + j * rstride, make_float4(v0.x, v0.y, v1.x, v1.y));
         }
       }
     }
   }
-  // Peers' shared memory must stay alive until every CTA has read it; this
-  // barrier orders no memory (the remote reads completed before the arrive),
-  // so it is relaxed and does not wait for the dK/dV stores to drain.
-  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
-  asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+
+  // ======================= dq (resident): rank 0 sums the slots ============
+  if (resident && rank == 0) {
+    for (int pr = tid; pr < G * half; pr += kThreads) {
+      const int h = pr / half, pi = pr - h * half;
+      const int idx = h * D + 2 * pi;
+      float y0 = 0.f, y1 = 0.f;
+      for (int r = 0; r < p.ncl; ++r) {
+        const float2 v = *reinterpret_cast<const float2 *>(slots + r * G * D + idx);
+        y0 += v.x;
+        y1 += v.y;
+      }
+      float z0 = y0, z1 = y1;
+      if (p.rope) {
+        const float c = p.rcos[pi], sn = p.rsin[pi];
+        z0 = y0 * c + y1 * sn;
+        z1 = -y0 * sn + y1 * c;
+      }
+      *reinterpret_cast<float2 *>(p.dq + qrow0 + idx) = make_float2(z0, z1);
+    }
+  }
 }
 
 template <typename KV, int GMAX, int DT>
