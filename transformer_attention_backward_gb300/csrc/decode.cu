@@ -76,23 +76,27 @@ struct DecodeParams {
 struct Layout {
   int kv, qs, sbuf, pbuf, etile, edp, xm, xl, xc, xa, xb, glob, rstat, alpha, runm, runl, runc, rsc, bars, total;
   __host__ __device__ static int up(int x, int a) { return (x + a - 1) / a * a; }
-  __host__ __device__ Layout(int G, int gs, int D, int chunk, int rowbytes, int rs) {
+  // swz: the quarter-row layout of scale*q / dout is used; resident: the
+  // streaming-only regions (running statistics, tile exponentials, dq
+  // partial exchange) are left out -- every region a path uses is present.
+  __host__ __device__ Layout(int G, int gs, int D, int chunk, int rowbytes, int rs, bool swz, bool resident) {
     int o = 0;
     const int tiles = 2 * kStages * kTile * rowbytes;        // [K st0][K st1][V st0][V st1]
-    const int scratch = 2 * rs * G * D * 4;                   // streaming: row-split dq partials
+    const int scratch = resident ? 0 : 2 * rs * G * D * 4;    // streaming: row-split dq partials
+    const int ns = resident ? 0 : 1;
     kv = o;    o += tiles > scratch ? tiles : scratch;   o = up(o, 16);
-    qs = o;    o += 2 * gs * 4 * (D / 4 + 4) * 4;
+    qs = o;    o += swz ? 2 * gs * 4 * (D / 4 + 4) * 4 : 0;
     sbuf = o;  o += gs * chunk * 4;
     pbuf = o;  o += gs * chunk * 4;
-    etile = o; o += gs * kTile * 4;
-    edp = o;   o += gs * kTile * 4;
+    etile = o; o += ns * gs * kTile * 4;
+    edp = o;   o += ns * gs * kTile * 4;
     xm = o;    o += kMaxG * 4;
     xl = o;    o += kMaxG * 4;
     xc = o;    o += kMaxG * 4;
-    xa = o;    o += G * D * 4;
-    xb = o;    o += G * D * 4;    o = up(o, 16);
+    xa = o;    o += ns * G * D * 4;
+    xb = o;    o += ns * G * D * 4;    o = up(o, 16);
     glob = o;  o += kMaxG * 16;
-    rstat = o; o += kMaxCluster * kMaxG * 16;
+    rstat = o; o += kMaxCluster * gs * 16;
     alpha = o; o += kMaxG * 4;
     runm = o;  o += kMaxG * 4;
     runl = o;  o += kMaxG * 4;
@@ -171,7 +175,7 @@ __device__ __forceinline__ void reduce_scatter(float (&v)[NV], int lpr, int lane
 // DT > 0: resident chunk, 128B-swizzled bf16 tiles, head dim DT, quarter-row
 // lanes.  DT == 0: any supported head dim, resident or streaming, unswizzled.
 template <typename KV, int GMAX, int DT>
-__global__ void __launch_bounds__(kThreads, GMAX >= 8 ? 1 : 2)
+__global__ void __launch_bounds__(kThreads, GMAX >= 8 ? 1 : (DT > 0 ? 3 : 2))
     decode_bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                       const __grid_constant__ DecodeParams p) {
   constexpr bool SWZ = DT > 0;
@@ -187,7 +191,7 @@ __global__ void __launch_bounds__(kThreads, GMAX >= 8 ? 1 : 2)
   const int rowbytes = SWZ ? DT * ES : p.rowbytes;
   const bool resident = SWZ || p.resident;
   const int RS = 1 << p.rs_log2;
-  const Layout L(G, GMAX, D, p.chunk, rowbytes, RS);
+  const Layout L(G, GMAX, D, p.chunk, rowbytes, RS, SWZ, resident);
   const int rank = static_cast<int>(cluster.block_rank());
   const int kvh = blockIdx.y, b = blockIdx.z;
   const int key0 = rank * p.chunk;
@@ -554,17 +558,17 @@ __global__ void __launch_bounds__(kThreads, GMAX >= 8 ? 1 : 2)
   // ======================= merge the softmax statistics ====================
   if (tid < p.ncl * G) {
     const int r = tid / G, h = tid - r * G;
-    rstat[r * kMaxG + h] = make_float4(cluster.map_shared_rank(xm, r)[h], cluster.map_shared_rank(xl, r)[h],
+    rstat[r * GMAX + h] = make_float4(cluster.map_shared_rank(xm, r)[h], cluster.map_shared_rank(xl, r)[h],
                                        cluster.map_shared_rank(xc, r)[h], 0.f);
   }
   __syncthreads();
   if (tid < G) {
     const int h = tid;
     float M = -INFINITY;
-    for (int r = 0; r < p.ncl; ++r) M = fmaxf(M, rstat[r * kMaxG + h].x);
+    for (int r = 0; r < p.ncl; ++r) M = fmaxf(M, rstat[r * GMAX + h].x);
     float Ls = 0.f, Cs = 0.f;
     for (int r = 0; r < p.ncl; ++r) {
-      const float4 st = rstat[r * kMaxG + h];
+      const float4 st = rstat[r * GMAX + h];
       const float w = expf(st.x - M);
       Ls = fmaf(st.y, w, Ls);
       Cs = fmaf(st.z, w, Cs);
@@ -796,7 +800,7 @@ cudaError_t launch_attn_bwd_decode(const float *q, const void *k, const void *v,
   const bool resident = chunk <= kStages * kTile;
   // specialised head dims: bf16 rows of 128 / 256 / 512 bytes with a resident chunk
   const int dt = (kv_bf16 && resident && (D == 64 || D == 128 || D == 256)) ? D : 0;
-  const Layout L(G, gmax, D, chunk, rowbytes, 1 << rs_log2);
+  const Layout L(G, gmax, D, chunk, rowbytes, 1 << rs_log2, dt > 0, resident);
   const int smem = L.total + 1024;                 // + alignment slack
   if (smem > 227 * 1024) {
     *why = "KV length too long for the per-CTA score buffers";
