@@ -6,64 +6,123 @@
 // over the causal softmax of forward(); "Hesper.Training.VerifiedBackward"
 // sections Softmax / Scaled Dot-Product / RoPE for the per-element steps.
 //
-// Three launches per call:
-//   1. prep     : delta_i = dout_i . o_i (the identity sum_j P_ij dP_ij =
-//                 dout_i . o_i), the RoPE cos/sin table, zeroed dq accumulator
-//   2. main     : one CTA per (64-key block, KV head, batch); loops over the
-//                 query heads of the group and the query blocks at or after
-//                 the key block; dK/dV accumulate in registers, dq through
-//                 fp32 atomics into the workspace
-//   3. finalize : dq = R(-theta) (scale * accumulator)
+// Launches per call:
+//   1. memset   : fp32 dq accumulator
+//   2. prep     : delta_i = dout_i . o_i (the identity sum_j P_ij dP_ij =
+//                 dout_i . o_i) and lse_i * log2(e), both padded to a multiple
+//                 of 64 queries (padding: delta 0, lse +inf so P = 0 there)
+//   3. rope     : cos/sin table of theta(t, i) (only with RoPE)
+//   4. main     : tcgen05 kernel, one CTA per (128-key block, KV head, batch)
+//   5. finalize : dq = R(-theta) (scale * accumulator)
+//
+// Main kernel (sm_103a, 12 warps, one CTA per SM).  Per CTA the K and V
+// block stays in shared memory; the CTA loops over the query heads of its KV
+// group and the 64-query blocks at or after its key block:
+//   MMA1  S^T  = K Q^T          M=128 keys, N=64 queries, K=128 (TMEM)
+//   MMA2  dP^T = V dO^T         same shape
+//   softmax warps: P = exp2(S scale log2e - lse log2e) (causal mask),
+//          dS = P (dP - delta), both rounded to bf16 into swizzled smem
+//   MMA3  dV  += P^T dO          M=128 keys, N=128, K=64 queries
+//   MMA4  dK  += dS^T Q          same shape
+//   MMA5  dQ^T = K^T dS^T        M=128 (head dim), N=64 queries, K=128 keys,
+//          written over the S columns the softmax warps have finished with;
+//          dq warps reduce it into the fp32 accumulator in global memory.
+// Warp roles: 0 TMA producer, 1 MMA issuer, 2 TMEM owner, 4-7 softmax
+// (and the dK epilogue: scale + RoPE), 8-11 dq reduction (and the dV
+// epilogue).  S/dP are double-buffered in TMEM so the tensor core computes
+// block n+1 while the softmax warps work on block n.  TMEM (512 columns):
+//   [0,64) S0 / dQ^T0   [64,128) dP0   [128,192) S1 / dQ^T1   [192,256) dP1
+//   [256,384) dV        [384,512) dK
 #include <math.h>
 
 #include "abw_host.h"
+#include "tcgen05.cuh"
 
 namespace abw {
 namespace {
 
 constexpr int kD = 128;
-constexpr int kBK = 64;   // keys per CTA
-constexpr int kBQ = 64;   // queries per inner block
-constexpr int kThr = 256;
+constexpr int kBK = 128;   // keys per CTA
+constexpr int kBQ = 64;    // queries per block
+constexpr int kThr = 384;  // 12 warps
+
+// Shared memory (offsets from a 1024-byte aligned base).
+constexpr int kOffK = 0;                 // [2 D-halves][128 keys][128 B], 128B-swizzled
+constexpr int kOffV = 32768;
+constexpr int kOffStage = 65536;         // 2 stages
+constexpr int kStageBytes = 33792;       // Q 16 KB, dO 16 KB, lse2 256 B, delta 256 B (1 KB aligned)
+constexpr int kStQ = 0, kStDO = 16384, kStLse = 32768, kStDelta = 33024;
+constexpr int kOffP = kOffStage + 2 * kStageBytes;   // P^T  [128 keys][64 queries] bf16, swizzled
+constexpr int kOffDS = kOffP + 16384;                 // dS^T [128 keys][64 queries] bf16, swizzled
+constexpr int kOffBar = kOffDS + 16384;
+constexpr int kSmem = kOffBar + 256 + 1024;           // + alignment slack
+
+// Barrier slots (8 bytes each) after kOffBar.
+enum {
+  kBarKV = 0, kBarQFull = 1, kBarQEmpty = 3, kBarSFull = 5, kBarPFull = 7, kBarPEmpty = 8,
+  kBarDQFull = 9, kBarTEmpty = 11, kBarDKV = 13, kBarFinal = 14, kNumBars = 15
+};
+constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
+constexpr int kOffAbort = kOffTmemSlot + 4;
+
+constexpr uint32_t kColS0 = 0, kColDP0 = 64, kColS1 = 128, kColDP1 = 192, kColDV = 256, kColDK = 384;
 
 struct CausalWs {
   float *dq_acc;     // [B][T][Hq][D]
-  float *delta;      // [B][Hq][T]
+  float *delta;      // [B][Hq][Tp]
+  float *lse2;       // [B][Hq][Tp]  lse * log2(e), +inf past T
   float2 *rope;      // [T][D/2] (cos, sin)
 };
 
 size_t up256(size_t x) { return (x + 255) / 256 * 256; }
 
+int padded_T(int T) { return (T + kBQ - 1) / kBQ * kBQ; }
+
 CausalWs carve(void *ws, int B, int T, int Hq, int D) {
+  const size_t Tp = static_cast<size_t>(padded_T(T));
   CausalWs w;
   char *p = static_cast<char *>(ws);
   p += (256 - (reinterpret_cast<uintptr_t>(p) & 255)) & 255;
   w.dq_acc = reinterpret_cast<float *>(p);
   p += up256(static_cast<size_t>(B) * T * Hq * D * 4);
   w.delta = reinterpret_cast<float *>(p);
-  p += up256(static_cast<size_t>(B) * Hq * T * 4);
+  p += up256(static_cast<size_t>(B) * Hq * Tp * 4);
+  w.lse2 = reinterpret_cast<float *>(p);
+  p += up256(static_cast<size_t>(B) * Hq * Tp * 4);
   w.rope = reinterpret_cast<float2 *>(p);
   return w;
 }
 
-// delta_i = dout_i . o_i, one warp per (b, t, h) row of D = 128 bf16.
-__global__ void __launch_bounds__(256) causal_delta_kernel(const __nv_bfloat16 *__restrict__ o,
-                                                           const __nv_bfloat16 *__restrict__ dout,
-                                                           float *__restrict__ delta, int B, int T, int Hq) {
+// delta and lse*log2(e) for every (b, h, t < Tp): one warp per (b, t, h) row
+// of D = 128 bf16 for t < T; padding rows get delta 0 and lse +inf.
+__global__ void __launch_bounds__(256) causal_prep_kernel(const __nv_bfloat16 *__restrict__ o,
+                                                          const __nv_bfloat16 *__restrict__ dout,
+                                                          const float *__restrict__ lse, float *__restrict__ delta,
+                                                          float *__restrict__ lse2, int B, int T, int Tp, int Hq) {
   const long long row = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
-  if (row >= static_cast<long long>(B) * T * Hq) return;
-  const uint2 a = reinterpret_cast<const uint2 *>(o + row * kD)[lane];
-  const uint2 g = reinterpret_cast<const uint2 *>(dout + row * kD)[lane];
+  if (row >= static_cast<long long>(B) * Tp * Hq) return;
+  const int h = static_cast<int>(row % Hq);
+  const long long bt = row / Hq;
+  const int t = static_cast<int>(bt % Tp);
+  const int b = static_cast<int>(bt / Tp);
+  const size_t out = (static_cast<size_t>(b) * Hq + h) * Tp + t;
+  if (t >= T) {
+    if (lane == 0) {
+      delta[out] = 0.f;
+      lse2[out] = INFINITY;
+    }
+    return;
+  }
+  const size_t src = ((static_cast<size_t>(b) * T + t) * Hq + h) * kD;
+  const uint2 a = reinterpret_cast<const uint2 *>(o + src)[lane];
+  const uint2 g = reinterpret_cast<const uint2 *>(dout + src)[lane];
   float s = bf16_lo(a.x) * bf16_lo(g.x) + bf16_hi(a.x) * bf16_hi(g.x) + bf16_lo(a.y) * bf16_lo(g.y) +
             bf16_hi(a.y) * bf16_hi(g.y);
   s = warp_sum(s);
   if (lane == 0) {
-    const int h = static_cast<int>(row % Hq);
-    const long long bt = row / Hq;
-    const int t = static_cast<int>(bt % T);
-    const int b = static_cast<int>(bt / T);
-    delta[(static_cast<size_t>(b) * Hq + h) * T + t] = s;
+    delta[out] = s;
+    lse2[out] = lse[(static_cast<size_t>(b) * Hq + h) * T + t] * 1.4426950408889634f;
   }
 }
 
@@ -82,174 +141,287 @@ __global__ void causal_rope_table_kernel(float2 *__restrict__ tab, int T, int po
   tab[idx] = make_float2(c, s);
 }
 
-struct MainParams {
-  const __nv_bfloat16 *q, *k, *v, *dout;
-  const float *lse;
-  float *dk, *dv;
+struct TcParams {
   CausalWs ws;
-  int B, T, Hq, Hkv, G;
+  float *dk, *dv;
+  int B, T, Tp, Hq, Hkv, G, nkb, nqb;
   float scale;
   int rope;
+  WaitCtl wait;
 };
 
-// SIMT reference kernel: correct for any T, D = 128.
-__global__ void __launch_bounds__(kThr, 1) causal_bwd_simt(const __grid_constant__ MainParams p) {
-  extern __shared__ float sm[];
-  float *Ks = sm;                          // [64][128]
-  float *Vs = Ks + kBK * kD;               // [64][128]
-  float *Qs = Vs + kBK * kD;               // [64][128]
-  float *Os = Qs + kBQ * kD;               // dout [64][128]
-  float *Ps = Os + kBQ * kD;               // [64][65]
-  float *Ds = Ps + kBQ * 65;               // [64][65]
-  float *ls = Ds + kBQ * 65;               // lse [64]
-  float *dl = ls + kBQ;                    // delta [64]
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t *>(&v);
+}
 
-  const int nkb = (p.T + kBK - 1) / kBK;
-  const int kb = nkb - 1 - blockIdx.x;     // heavy (early) key blocks first
-  const int kvh = blockIdx.y, b = blockIdx.z;
+__global__ void __launch_bounds__(kThr, 1)
+    causal_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmDO,
+                         const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                         const __grid_constant__ TcParams p) {
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char *smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+  const uint32_t sb = smem_u32(smem);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  // work item: heavy (early) key blocks first across the whole grid
+  const int per_kb = p.Hkv * p.B;
+  const int kb = blockIdx.x / per_kb;
+  const int rem = blockIdx.x - kb * per_kb;
+  const int kvh = rem % p.Hkv, b = rem / p.Hkv;
   const int k0 = kb * kBK;
-  const int tid = threadIdx.x;
+  const int qb0 = k0 / kBQ;
+  const int nq = p.nqb - qb0;            // query blocks per head
+  const int N = p.G * nq;                // iterations of this CTA
 
-  // load K, V block (rows beyond T are zero)
-  for (int i = tid; i < kBK * kD; i += kThr) {
-    const int r = i / kD, d = i % kD;
-    const int j = k0 + r;
-    float kv = 0.f, vv = 0.f;
-    if (j < p.T) {
-      const size_t off = ((static_cast<size_t>(b) * p.T + j) * p.Hkv + kvh) * kD + d;
-      kv = __bfloat162float(p.k[off]);
-      vv = __bfloat162float(p.v[off]);
+  auto bar = [&](int i) -> uint32_t { return sb + kOffBar + i * 8; };
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + kOffAbort);
+  auto wt = [&](uint32_t br, uint32_t parity) -> bool {
+    if (*abort_flag) return false;
+    if (mbar_wait_bounded(br, parity, p.wait.limit_ns)) return true;
+    *abort_flag = 1;
+    atomicOr(p.wait.err, kErrWaitTimeout);
+    return false;
+  };
+
+  if (tid == 0) {
+    mbar_init(bar(kBarKV), 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar(kBarQFull + s), 1);
+      mbar_init(bar(kBarQEmpty + s), 1);
+      mbar_init(bar(kBarSFull + s), 1);
+      mbar_init(bar(kBarDQFull + s), 1);
+      mbar_init(bar(kBarTEmpty + s), 128);
     }
-    Ks[i] = kv;
-    Vs[i] = vv;
+    mbar_init(bar(kBarPFull), 128);
+    mbar_init(bar(kBarPEmpty), 1);
+    mbar_init(bar(kBarDKV), 1);
+    mbar_init(bar(kBarFinal), 1);
+    *abort_flag = 0;
+    fence_barrier_init();
   }
+  if (warp == 2) tc::tmem_alloc(sb + kOffTmemSlot, 512);
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + kOffTmemSlot);
 
-  // dK, dV accumulators: thread owns key row jr, dims c + 4m (m < 32)
-  const int jr = tid >> 2, c4 = tid & 3;
-  float aK[32], aV[32];
-#pragma unroll
-  for (int m = 0; m < 32; ++m) aK[m] = aV[m] = 0.f;
-
-  const float l2e = 1.4426950408889634f;
-  for (int hh = 0; hh < p.G; ++hh) {
-    const int h = kvh * p.G + hh;
-    for (int q0 = (k0 / kBQ) * kBQ; q0 < p.T; q0 += kBQ) {
-      __syncthreads();
-      for (int i = tid; i < kBQ * kD; i += kThr) {
-        const int r = i / kD, d = i % kD;
-        const int t = q0 + r;
-        float qv = 0.f, ov = 0.f;
-        if (t < p.T) {
-          const size_t off = ((static_cast<size_t>(b) * p.T + t) * p.Hq + h) * kD + d;
-          qv = __bfloat162float(p.q[off]);
-          ov = __bfloat162float(p.dout[off]);
+  if (warp == 0) {
+    // ============================ TMA producer ============================
+    if (lane == 0) {
+      prefetch_tensormap(&tmQ);
+      prefetch_tensormap(&tmDO);
+      prefetch_tensormap(&tmK);
+      prefetch_tensormap(&tmV);
+      mbar_arrive_expect_tx(bar(kBarKV), 4 * 16384);
+      for (int hx = 0; hx < 2; ++hx) {
+        tma_load_4d(sb + kOffK + hx * 16384, &tmK, hx * 64, kvh, k0, b, bar(kBarKV));
+        tma_load_4d(sb + kOffV + hx * 16384, &tmV, hx * 64, kvh, k0, b, bar(kBarKV));
+      }
+      int issued = 0;
+      for (int n = 0; n < N; ++n) {
+        const int s = n & 1, cyc = n >> 1;
+        if (!wt(bar(kBarQEmpty + s), (cyc & 1) ^ 1)) break;
+        const int h = kvh * p.G + n / nq;
+        const int q0 = (qb0 + n % nq) * kBQ;
+        const uint32_t st = sb + kOffStage + s * kStageBytes;
+        const uint32_t fb = bar(kBarQFull + s);
+        mbar_arrive_expect_tx(fb, 2 * 16384 + 2 * 256);
+        for (int hx = 0; hx < 2; ++hx) {
+          tma_load_4d(st + kStQ + hx * 8192, &tmQ, hx * 64, h, q0, b, fb);
+          tma_load_4d(st + kStDO + hx * 8192, &tmDO, hx * 64, h, q0, b, fb);
         }
-        Qs[i] = qv;
-        Os[i] = ov;
+        const size_t ro = (static_cast<size_t>(b) * p.Hq + h) * p.Tp + q0;
+        bulk_load(st + kStLse, p.ws.lse2 + ro, 256, fb);
+        bulk_load(st + kStDelta, p.ws.delta + ro, 256, fb);
+        issued = n + 1;
       }
-      if (tid < kBQ) {
-        const int t = q0 + tid;
-        const size_t lo = (static_cast<size_t>(b) * p.Hq + h) * p.T + t;
-        ls[tid] = t < p.T ? p.lse[lo] : 0.f;
-        dl[tid] = t < p.T ? p.ws.delta[lo] : 0.f;
+      if (*abort_flag) {
+        // let copies already in flight land before the CTA can exit
+        for (int n = (issued > 2 ? issued - 2 : 0); n < issued; ++n)
+          mbar_wait_bounded(bar(kBarQFull + (n & 1)), (n >> 1) & 1, 2000000000ull);
+        mbar_wait_bounded(bar(kBarKV), 0, 2000000000ull);
       }
-      __syncthreads();
-      // S, dP: thread computes rows 4*ti..4*ti+3, cols tj + 16*m
-      {
-        const int ti = tid >> 4, tj = tid & 15;
-        float s[4][4], dp[4][4];
+    }
+  } else if (warp == 1) {
+    // ============================ MMA issuer ==============================
+    if (lane == 0) {
+      constexpr uint32_t id_sdp = tc::idesc_bf16_f32(128, 64, 0, 0);    // S^T, dP^T
+      constexpr uint32_t id_kv = tc::idesc_bf16_f32(128, 128, 0, 1);    // dV, dK
+      constexpr uint32_t id_dq = tc::idesc_bf16_f32(128, 64, 1, 1);     // dQ^T
+      bool ok = wt(bar(kBarKV), 0);
+      tc::fence_after_sync();
+      auto issue_sdp = [&](int n) -> bool {
+        const int s = n & 1, cyc = n >> 1;
+        if (!wt(bar(kBarQFull + s), cyc & 1)) return false;
+        if (!wt(bar(kBarTEmpty + s), (cyc & 1) ^ 1)) return false;
+        tc::fence_after_sync();
+        const uint32_t st = sb + kOffStage + s * kStageBytes;
+        const uint32_t dS = tmem + (s ? kColS1 : kColS0), dP = tmem + (s ? kColDP1 : kColDP0);
 #pragma unroll
-        for (int a = 0; a < 4; ++a)
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t ko = (kk >> 2) * 16384 + (kk & 3) * 32, qo = (kk >> 2) * 8192 + (kk & 3) * 32;
+          tc::mma_bf16(dS, tc::sdesc_sw128(sb + kOffK + ko, 16, 1024), tc::sdesc_sw128(st + kStQ + qo, 16, 1024),
+                       id_sdp, kk > 0);
+        }
 #pragma unroll
-          for (int c = 0; c < 4; ++c) s[a][c] = dp[a][c] = 0.f;
-        for (int d = 0; d < kD; ++d) {
-          float qa[4], oa[4], kc[4], vc[4];
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t ko = (kk >> 2) * 16384 + (kk & 3) * 32, qo = (kk >> 2) * 8192 + (kk & 3) * 32;
+          tc::mma_bf16(dP, tc::sdesc_sw128(sb + kOffV + ko, 16, 1024), tc::sdesc_sw128(st + kStDO + qo, 16, 1024),
+                       id_sdp, kk > 0);
+        }
+        tc::commit(bar(kBarSFull + s));
+        return true;
+      };
+      if (ok) ok = issue_sdp(0);
+      for (int n = 0; ok && n < N; ++n) {
+        const int s = n & 1;
+        if (n + 1 < N && !issue_sdp(n + 1)) break;
+        if (!wt(bar(kBarPFull), n & 1)) break;
+        tc::fence_after_sync();
+        const uint32_t st = sb + kOffStage + s * kStageBytes;
 #pragma unroll
-          for (int a = 0; a < 4; ++a) {
-            qa[a] = Qs[(4 * ti + a) * kD + d];
-            oa[a] = Os[(4 * ti + a) * kD + d];
-          }
+        for (int kk = 0; kk < 4; ++kk)   // dV += P^T dO
+          tc::mma_bf16(tmem + kColDV, tc::sdesc_sw128(sb + kOffP + kk * 32, 16, 1024),
+                       tc::sdesc_sw128(st + kStDO + kk * 2048, 8192, 1024), id_kv, (n > 0 || kk > 0));
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            kc[c] = Ks[(tj + 16 * c) * kD + d];
-            vc[c] = Vs[(tj + 16 * c) * kD + d];
-          }
+        for (int kk = 0; kk < 4; ++kk)   // dK += dS^T Q
+          tc::mma_bf16(tmem + kColDK, tc::sdesc_sw128(sb + kOffDS + kk * 32, 16, 1024),
+                       tc::sdesc_sw128(st + kStQ + kk * 2048, 8192, 1024), id_kv, (n > 0 || kk > 0));
 #pragma unroll
-          for (int a = 0; a < 4; ++a)
+        for (int kk = 0; kk < 8; ++kk)   // dQ^T = K^T dS^T
+          tc::mma_bf16(tmem + (s ? kColS1 : kColS0), tc::sdesc_sw128(sb + kOffK + kk * 2048, 16384, 1024),
+                       tc::sdesc_sw128(sb + kOffDS + kk * 2048, 8192, 1024), id_dq, kk > 0);
+        tc::commit(bar(kBarQEmpty + s));
+        tc::commit(bar(kBarPEmpty));
+        tc::commit(bar(kBarDQFull + s));
+      }
+      tc::commit(bar(kBarDKV));
+      tc::commit(bar(kBarFinal));
+      mbar_wait_bounded(bar(kBarFinal), 0, 2000000000ull);   // every MMA has completed
+    }
+  } else if (warp >= 4 && warp < 8) {
+    // ============================ softmax warps ===========================
+    const int qd = warp & 3;
+    const int j = 32 * qd + lane;                       // key row in the block
+    const int key = k0 + j;
+    const uint32_t lanebase = static_cast<uint32_t>(32 * qd) << 16;
+    const float sl2 = p.scale * 1.4426950408889634f;
+    for (int n = 0; n < N; ++n) {
+      const int s = n & 1, cyc = n >> 1;
+      const int q0 = (qb0 + n % nq) * kBQ;
+      if (!wt(bar(kBarSFull + s), cyc & 1)) break;
+      tc::fence_after_sync();
+      const float *lse2 = reinterpret_cast<const float *>(smem + kOffStage + s * kStageBytes + kStLse);
+      const float *dl = reinterpret_cast<const float *>(smem + kOffStage + s * kStageBytes + kStDelta);
+      uint32_t pk[32], dk[32];
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-              s[a][c] = fmaf(qa[a], kc[c], s[a][c]);
-              dp[a][c] = fmaf(oa[a], vc[c], dp[a][c]);
+      for (int hf = 0; hf < 2; ++hf) {
+        float sv[32], pv[32];
+        tc::ld32x2_wait(tmem + lanebase + (s ? kColS1 : kColS0) + 32 * hf,
+                        tmem + lanebase + (s ? kColDP1 : kColDP0) + 32 * hf, sv, pv);
+#pragma unroll
+        for (int c = 0; c < 32; c += 4) {
+          const float4 l4 = *reinterpret_cast<const float4 *>(lse2 + 32 * hf + c);
+          const float4 d4 = *reinterpret_cast<const float4 *>(dl + 32 * hf + c);
+          const int q = q0 + 32 * hf + c;
+          float P0 = exp2f(fmaf(sv[c], sl2, -l4.x));
+          float P1 = exp2f(fmaf(sv[c + 1], sl2, -l4.y));
+          float P2 = exp2f(fmaf(sv[c + 2], sl2, -l4.z));
+          float P3 = exp2f(fmaf(sv[c + 3], sl2, -l4.w));
+          P0 = key <= q ? P0 : 0.f;
+          P1 = key <= q + 1 ? P1 : 0.f;
+          P2 = key <= q + 2 ? P2 : 0.f;
+          P3 = key <= q + 3 ? P3 : 0.f;
+          const float dS0 = P0 * (pv[c] - d4.x), dS1 = P1 * (pv[c + 1] - d4.y);
+          const float dS2 = P2 * (pv[c + 2] - d4.z), dS3 = P3 * (pv[c + 3] - d4.w);
+          pk[16 * hf + c / 2] = pack_bf16x2(P0, P1);
+          pk[16 * hf + c / 2 + 1] = pack_bf16x2(P2, P3);
+          dk[16 * hf + c / 2] = pack_bf16x2(dS0, dS1);
+          dk[16 * hf + c / 2 + 1] = pack_bf16x2(dS2, dS3);
+        }
+      }
+      if (!wt(bar(kBarPEmpty), (n & 1) ^ 1)) break;
+      unsigned char *prow = smem + kOffP + j * 128;
+      unsigned char *drow = smem + kOffDS + j * 128;
+#pragma unroll
+      for (int c8 = 0; c8 < 8; ++c8) {
+        const int o = (c8 ^ (j & 7)) << 4;
+        *reinterpret_cast<uint4 *>(prow + o) = make_uint4(pk[4 * c8], pk[4 * c8 + 1], pk[4 * c8 + 2], pk[4 * c8 + 3]);
+        *reinterpret_cast<uint4 *>(drow + o) = make_uint4(dk[4 * c8], dk[4 * c8 + 1], dk[4 * c8 + 2], dk[4 * c8 + 3]);
+      }
+      fence_proxy_async_smem();
+      tc::fence_before_sync();
+      mbar_arrive(bar(kBarPFull));
+    }
+    // ---- dK epilogue: scale, RoPE backward, store
+    if (wt(bar(kBarDKV), 0)) {
+      tc::fence_after_sync();
+      for (int c = 0; c < 4; ++c) {
+        float v[32];
+        tc::ld32_wait(tmem + lanebase + kColDK + 32 * c, v);
+        if (key < p.T) {
+          float *dst = p.dk + ((static_cast<size_t>(b) * p.T + key) * p.Hkv + kvh) * kD + 32 * c;
+#pragma unroll
+          for (int i = 0; i < 32; i += 4) {
+            float y0 = v[i] * p.scale, y1 = v[i + 1] * p.scale, y2 = v[i + 2] * p.scale, y3 = v[i + 3] * p.scale;
+            if (p.rope) {
+              const float4 cs = *reinterpret_cast<const float4 *>(p.ws.rope + key * (kD / 2) + 16 * c + i / 2);
+              const float z0 = y0 * cs.x + y1 * cs.y, z1 = -y0 * cs.y + y1 * cs.x;
+              const float z2 = y2 * cs.z + y3 * cs.w, z3 = -y2 * cs.w + y3 * cs.z;
+              y0 = z0; y1 = z1; y2 = z2; y3 = z3;
             }
-        }
-#pragma unroll
-        for (int a = 0; a < 4; ++a) {
-          const int i = 4 * ti + a, t = q0 + i;
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            const int jj = tj + 16 * c, j = k0 + jj;
-            float P = 0.f;
-            if (t < p.T && j <= t) P = exp2f((s[a][c] * p.scale - ls[i]) * l2e);
-            Ps[i * 65 + jj] = P;
-            Ds[i * 65 + jj] = P * (dp[a][c] - dl[i]);
+            *reinterpret_cast<float4 *>(dst + i) = make_float4(y0, y1, y2, y3);
           }
         }
       }
-      __syncthreads();
-      // dV[jr] += sum_i P[i][jr] dO[i];  dK[jr] += sum_i dS[i][jr] Q[i]
-      for (int i = 0; i < kBQ; ++i) {
-        const float P = Ps[i * 65 + jr], dS = Ds[i * 65 + jr];
+    }
+  } else if (warp >= 8) {
+    // ============================ dq reduction warps ======================
+    const int qd = warp & 3;
+    const int d = 32 * qd + lane;                       // head-dim row of dQ^T
+    const uint32_t lanebase = static_cast<uint32_t>(32 * qd) << 16;
+    for (int n = 0; n < N; ++n) {
+      const int s = n & 1, cyc = n >> 1;
+      if (!wt(bar(kBarDQFull + s), cyc & 1)) break;
+      tc::fence_after_sync();
+      float v0[32], v1[32];
+      tc::ld32x2_wait(tmem + lanebase + (s ? kColS1 : kColS0), tmem + lanebase + (s ? kColS1 : kColS0) + 32, v0, v1);
+      tc::fence_before_sync();
+      mbar_arrive(bar(kBarTEmpty + s));
+      const int h = kvh * p.G + n / nq;
+      const int q0 = (qb0 + n % nq) * kBQ;
+      const size_t rs = static_cast<size_t>(p.Hq) * kD;
+      float *base = p.ws.dq_acc + ((static_cast<size_t>(b) * p.T + q0) * p.Hq + h) * kD + d;
+      const int nv = min(kBQ, p.T - q0);
 #pragma unroll
-        for (int m = 0; m < 32; ++m) {
-          aV[m] = fmaf(P, Os[i * kD + c4 + 4 * m], aV[m]);
-          aK[m] = fmaf(dS, Qs[i * kD + c4 + 4 * m], aK[m]);
-        }
-      }
-      // dQ[i] += sum_j dS[i][j] K[j]  (thread: row i = jr, dims c4 + 4m)
-      {
-        float aq[32];
+      for (int c = 0; c < 32; ++c)
+        if (c < nv) atomicAdd(base + c * rs, v0[c]);
 #pragma unroll
-        for (int m = 0; m < 32; ++m) aq[m] = 0.f;
-        for (int jj = 0; jj < kBK; ++jj) {
-          const float dS = Ds[jr * 65 + jj];
+      for (int c = 0; c < 32; ++c)
+        if (32 + c < nv) atomicAdd(base + (32 + c) * rs, v1[c]);
+    }
+    // ---- dV epilogue
+    const int key = k0 + d;   // TMEM lane == key row for dV
+    if (wt(bar(kBarDKV), 0)) {
+      tc::fence_after_sync();
+      for (int c = 0; c < 4; ++c) {
+        float v[32];
+        tc::ld32_wait(tmem + lanebase + kColDV + 32 * c, v);
+        if (key < p.T) {
+          float *dst = p.dv + ((static_cast<size_t>(b) * p.T + key) * p.Hkv + kvh) * kD + 32 * c;
 #pragma unroll
-          for (int m = 0; m < 32; ++m) aq[m] = fmaf(dS, Ks[jj * kD + c4 + 4 * m], aq[m]);
-        }
-        const int t = q0 + jr;
-        if (t < p.T) {
-          float *dst = p.ws.dq_acc + ((static_cast<size_t>(b) * p.T + t) * p.Hq + h) * kD;
-#pragma unroll
-          for (int m = 0; m < 32; ++m) atomicAdd(dst + c4 + 4 * m, aq[m]);
+          for (int i = 0; i < 32; i += 4)
+            *reinterpret_cast<float4 *>(dst + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
         }
       }
     }
   }
+  tc::fence_before_sync();
   __syncthreads();
-  // epilogue: dK (scaled, rotated) and dV
-  float *Kout = Qs;   // reuse: [64][128]
-#pragma unroll
-  for (int m = 0; m < 32; ++m) Kout[jr * kD + c4 + 4 * m] = aK[m] * p.scale;
-  __syncthreads();
-  for (int i = tid; i < kBK * (kD / 2); i += kThr) {
-    const int r = i / (kD / 2), pi = i % (kD / 2);
-    const int j = k0 + r;
-    if (j >= p.T) continue;
-    float y0 = Kout[r * kD + 2 * pi], y1 = Kout[r * kD + 2 * pi + 1];
-    if (p.rope) {
-      const float2 cs = p.ws.rope[j * (kD / 2) + pi];
-      const float z0 = y0 * cs.x + y1 * cs.y, z1 = -y0 * cs.y + y1 * cs.x;
-      y0 = z0;
-      y1 = z1;
-    }
-    float *dst = p.dk + ((static_cast<size_t>(b) * p.T + j) * p.Hkv + kvh) * kD + 2 * pi;
-    dst[0] = y0;
-    dst[1] = y1;
-  }
-  const int j = k0 + jr;
-  if (j < p.T) {
-    float *dst = p.dv + ((static_cast<size_t>(b) * p.T + j) * p.Hkv + kvh) * kD;
-#pragma unroll
-    for (int m = 0; m < 32; ++m) dst[c4 + 4 * m] = aV[m];
+  if (warp == 2) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tmem, 512);
   }
 }
 
@@ -273,10 +445,19 @@ __global__ void __launch_bounds__(256) causal_dq_finalize(const float *__restric
   reinterpret_cast<float2 *>(dq)[i] = make_float2(z0, z1);
 }
 
+bool make_map(CUtensorMap *m, const void *base, int H, int T, int B, uint32_t rows, const char **why) {
+  const uint64_t dims[4] = {kD, static_cast<uint64_t>(H), static_cast<uint64_t>(T), static_cast<uint64_t>(B)};
+  const uint64_t strides[3] = {kD * 2, static_cast<uint64_t>(H) * kD * 2, static_cast<uint64_t>(T) * H * kD * 2};
+  const uint32_t box[4] = {64, 1, rows, 1};
+  return encode_tiled(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, base, dims, strides, box,
+                      CU_TENSOR_MAP_SWIZZLE_128B, why);
+}
+
 }  // namespace
 
 size_t causal_workspace_bytes(int B, int T, int Hq, int D) {
-  return 256 + up256(static_cast<size_t>(B) * T * Hq * D * 4) + up256(static_cast<size_t>(B) * Hq * T * 4) +
+  const size_t Tp = static_cast<size_t>(padded_T(T));
+  return 256 + up256(static_cast<size_t>(B) * T * Hq * D * 4) + 2 * up256(static_cast<size_t>(B) * Hq * Tp * 4) +
          up256(static_cast<size_t>(T) * (D / 2) * 8);
 }
 
@@ -285,14 +466,15 @@ cudaError_t launch_attn_bwd_causal(const void *q, const void *k, const void *v, 
                                    int D, float scale, double rope_base, int pos0, void *ws, size_t ws_bytes,
                                    const WaitCtl &w, cudaStream_t st, const char **why) {
   (void)ws_bytes;
-  (void)w;
   if (D != kD) {
     *why = "D != 128";
     return cudaErrorNotSupported;
   }
   const int nkb = (T + kBK - 1) / kBK;
-  if (Hkv > 65535 || B > 65535) {
-    *why = "B or Hkv > 65535";
+  const int Tp = padded_T(T);
+  const long long ctas = static_cast<long long>(nkb) * Hkv * B;
+  if (ctas > 0x7fffffffLL) {
+    *why = "grid too large";
     return cudaErrorNotSupported;
   }
   CausalWs cw = carve(ws, B, T, Hq, D);
@@ -300,32 +482,34 @@ cudaError_t launch_attn_bwd_causal(const void *q, const void *k, const void *v, 
   cudaError_t e = cudaMemsetAsync(cw.dq_acc, 0, qn * 4, st);
   if (e != cudaSuccess) return e;
   {
-    const long long rows = static_cast<long long>(B) * T * Hq;
+    const long long rows = static_cast<long long>(B) * Tp * Hq;
     const long long blocks = (rows * 32 + 255) / 256;
-    causal_delta_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(
-        static_cast<const __nv_bfloat16 *>(o), static_cast<const __nv_bfloat16 *>(dout), cw.delta, B, T, Hq);
+    causal_prep_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(
+        static_cast<const __nv_bfloat16 *>(o), static_cast<const __nv_bfloat16 *>(dout), lse, cw.delta, cw.lse2, B,
+        T, Tp, Hq);
   }
   const int rope = rope_base > 0.0;
   if (rope) {
     const int n = T * (kD / 2);
     causal_rope_table_kernel<<<(n + 255) / 256, 256, 0, st>>>(cw.rope, T, pos0, log2(rope_base));
   }
-  MainParams p;
-  p.q = static_cast<const __nv_bfloat16 *>(q);
-  p.k = static_cast<const __nv_bfloat16 *>(k);
-  p.v = static_cast<const __nv_bfloat16 *>(v);
-  p.dout = static_cast<const __nv_bfloat16 *>(dout);
-  p.lse = lse;
+  CUtensorMap tq, tdo, tk, tv;
+  if (!make_map(&tq, q, Hq, T, B, kBQ, why) || !make_map(&tdo, dout, Hq, T, B, kBQ, why) ||
+      !make_map(&tk, k, Hkv, T, B, kBK, why) || !make_map(&tv, v, Hkv, T, B, kBK, why))
+    return cudaErrorInvalidValue;
+  TcParams p;
+  p.ws = cw;
   p.dk = dk;
   p.dv = dv;
-  p.ws = cw;
-  p.B = B; p.T = T; p.Hq = Hq; p.Hkv = Hkv; p.G = Hq / Hkv;
+  p.B = B; p.T = T; p.Tp = Tp; p.Hq = Hq; p.Hkv = Hkv; p.G = Hq / Hkv;
+  p.nkb = nkb;
+  p.nqb = Tp / kBQ;
   p.scale = scale;
   p.rope = rope;
-  const int smem = (4 * 64 * kD + 2 * 64 * 65 + 2 * 64) * 4;
-  e = cudaFuncSetAttribute(causal_bwd_simt, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  p.wait = w;
+  e = cudaFuncSetAttribute(causal_bwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
   if (e != cudaSuccess) return e;
-  causal_bwd_simt<<<dim3(nkb, Hkv, B), kThr, smem, st>>>(p);
+  causal_bwd_tc_kernel<<<static_cast<unsigned>(ctas), kThr, kSmem, st>>>(tq, tdo, tk, tv, p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const long long npairs = static_cast<long long>(qn / 2);
