@@ -26,7 +26,8 @@
 //   MMA4  dK  += dS^T Q          same shape
 //   MMA5  dQ^T = K^T dS^T        M=128 (head dim), N=64 queries, K=128 keys,
 //          written over the S columns the softmax warps have finished with;
-//          dq warps reduce it into the fp32 accumulator in global memory.
+//          dq warps stage it in shared memory (32 queries at a time) and a
+//          TMA tensor reduce-add folds it into the fp32 dq accumulator.
 // Warp roles: 0 TMA producer, 1 MMA issuer, 2 TMEM owner, 4-7 softmax
 // (and the dK epilogue: scale + RoPE), 8-11 dq reduction (and the dV
 // epilogue).  S/dP are double-buffered in TMEM so the tensor core computes
@@ -57,7 +58,8 @@ constexpr int kStageBytes = 33792;       // Q 16 KB, dO 16 KB, lse2 256 B, delta
 constexpr int kStQ = 0, kStDO = 16384, kStLse = 32768, kStDelta = 33024;
 constexpr int kOffP = kOffStage + kStages * kStageBytes;   // P^T [128 keys][64 queries] bf16, swizzled
 constexpr int kOffDS = kOffP + 16384;                 // dS^T [128 keys][64 queries] bf16, swizzled
-constexpr int kOffBar = kOffDS + 16384;
+constexpr int kOffDQ = kOffDS + 16384;                // dQ staging: [32 queries][128] fp32
+constexpr int kOffBar = kOffDQ + 16384;
 constexpr int kSmem = kOffBar + 256 + 1024;           // + alignment slack
 
 // Barrier slots (8 bytes each) after kOffBar.
@@ -169,7 +171,7 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 __global__ void __launch_bounds__(kThr, 1)
     causal_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmDO,
                          const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
-                         const __grid_constant__ TcParams p) {
+                         const __grid_constant__ CUtensorMap tmDQ, const __grid_constant__ TcParams p) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char *smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
   const uint32_t sb = smem_u32(smem);
@@ -404,7 +406,8 @@ __global__ void __launch_bounds__(kThr, 1)
     const uint32_t lanebase = static_cast<uint32_t>(32 * qd) << 16;
     for (int n = 0; n < N; ++n) {
       const int s = n & 1, cyc = n >> 1;
-      if (!wt(bar(kBarDQFull + s), cyc & 1)) break;
+      // the four dq warps share named barriers: leave the loop together
+      if (!named_barrier_and(1, 128, wt(bar(kBarDQFull + s), cyc & 1))) break;
       tc::fence_after_sync();
       float v0[32], v1[32];
       tc::ld32x2_wait(tmem + lanebase + (s ? kColS1 : kColS0), tmem + lanebase + (s ? kColS1 : kColS0) + 32, v0, v1);
@@ -412,16 +415,27 @@ __global__ void __launch_bounds__(kThr, 1)
       mbar_arrive(bar(kBarTEmpty + s));
       const int h = kvh * p.G + n / nq;
       const int q0 = (qb0 + n % nq) * kBQ;
-      const size_t rs = static_cast<size_t>(p.Hq) * kD;
-      float *base = p.ws.dq_acc + ((static_cast<size_t>(b) * p.T + q0) * p.Hq + h) * kD + d;
-      const int nv = min(kBQ, p.T - q0);
+      float *stage = reinterpret_cast<float *>(smem + kOffDQ);
 #pragma unroll
-      for (int c = 0; c < 32; ++c)
-        if (c < nv) atomicAdd(base + c * rs, v0[c]);
+      for (int hf = 0; hf < 2; ++hf) {
+        if (hf == 1) {
+          // the first half's reduce must have read the staging tile
+          if (warp == 8 && lane == 0) bulk_wait_group_read0();
+          named_barrier(1, 128);
+        }
 #pragma unroll
-      for (int c = 0; c < 32; ++c)
-        if (32 + c < nv) atomicAdd(base + (32 + c) * rs, v1[c]);
+        for (int c = 0; c < 32; ++c) stage[c * kD + d] = hf ? v1[c] : v0[c];
+        fence_proxy_async_smem();
+        named_barrier(1, 128);
+        if (warp == 8 && lane == 0) {
+          tma_reduce_add_4d(&tmDQ, sb + kOffDQ, 0, h, q0 + 32 * hf, b);
+          bulk_commit_group();
+        }
+      }
+      if (warp == 8 && lane == 0) bulk_wait_group_read0();
+      named_barrier(1, 128);
     }
+    if (warp == 8 && lane == 0) bulk_wait_group0();   // every reduce has landed before the CTA ends
     // ---- dV epilogue
     const int key = k0 + d;   // TMEM lane == key row for dV
     if (wt(bar(kBarDKV), 0)) {
@@ -514,10 +528,19 @@ cudaError_t launch_attn_bwd_causal(const void *q, const void *k, const void *v, 
     const int n = T * (kD / 2);
     causal_rope_table_kernel<<<(n + 255) / 256, 256, 0, st>>>(cw.rope, T, pos0, log2(rope_base));
   }
-  CUtensorMap tq, tdo, tk, tv;
+  CUtensorMap tq, tdo, tk, tv, tdq;
   if (!make_map(&tq, q, Hq, T, B, kBQ, why) || !make_map(&tdo, dout, Hq, T, B, kBQ, why) ||
       !make_map(&tk, k, Hkv, T, B, kBK, why) || !make_map(&tv, v, Hkv, T, B, kBK, why))
     return cudaErrorInvalidValue;
+  {
+    // fp32 dq accumulator [B][T][Hq][D], reduce-added 32 query rows at a time
+    const uint64_t dims[4] = {kD, static_cast<uint64_t>(Hq), static_cast<uint64_t>(T), static_cast<uint64_t>(B)};
+    const uint64_t strides[3] = {kD * 4, static_cast<uint64_t>(Hq) * kD * 4, static_cast<uint64_t>(T) * Hq * kD * 4};
+    const uint32_t box[4] = {kD, 1, 32, 1};
+    if (!encode_tiled(&tdq, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, cw.dq_acc, dims, strides, box,
+                      CU_TENSOR_MAP_SWIZZLE_NONE, why))
+      return cudaErrorInvalidValue;
+  }
   TcParams p;
   p.ws = cw;
   p.dk = dk;
@@ -530,7 +553,7 @@ cudaError_t launch_attn_bwd_causal(const void *q, const void *k, const void *v, 
   p.wait = w;
   e = cudaFuncSetAttribute(causal_bwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
   if (e != cudaSuccess) return e;
-  causal_bwd_tc_kernel<<<static_cast<unsigned>(ctas), kThr, kSmem, st>>>(tq, tdo, tk, tv, p);
+  causal_bwd_tc_kernel<<<static_cast<unsigned>(ctas), kThr, kSmem, st>>>(tq, tdo, tk, tv, tdq, p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const long long npairs = static_cast<long long>(qn / 2);
