@@ -177,6 +177,13 @@ __device__ __forceinline__ float warp_max(float v) {
 __device__ __forceinline__ float bf16_lo(uint32_t u) { return __uint_as_float(u << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t u) { return __uint_as_float(u & 0xffff0000u); }
 
+// Vector fp32 reduction into global memory (four consecutive floats), done
+// in the L2 without returning a value.
+__device__ __forceinline__ void red_add_f4(float *p, float4 v) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w)
+               : "memory");
+}
+
 // Streaming (evict-first) 16-byte store for outputs that are not re-read.
 __device__ __forceinline__ void st_cs_f4(float *p, float4 v) {
   asm volatile("st.global.cs.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(v.x), "f"(v.y), "f"(v.z),

@@ -26,8 +26,10 @@
 //   MMA4  dK  += dS^T Q          same shape
 //   MMA5  dQ^T = K^T dS^T        M=128 (head dim), N=64 queries, K=128 keys,
 //          written over the S columns the softmax warps have finished with;
-//          dq warps stage it in shared memory (32 queries at a time) and a
-//          TMA tensor reduce-add folds it into the fp32 dq accumulator.
+//          dq warps transpose it through shared memory (32 queries at a
+//          time) and fold it into the fp32 dq accumulator with 16-byte
+//          vector reductions (kept off the TMA queue, which carries the
+//          Q/dO loads).
 // Warp roles: 0 TMA producer, 1 MMA issuer, 2 TMEM owner, 4-7 softmax
 // (and the dK epilogue: scale + RoPE), 8-11 dq reduction (and the dV
 // epilogue).  S/dP are double-buffered in TMEM so the tensor core computes
@@ -171,7 +173,7 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 __global__ void __launch_bounds__(kThr, 1)
     causal_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmDO,
                          const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
-                         const __grid_constant__ CUtensorMap tmDQ, const __grid_constant__ TcParams p) {
+                         const __grid_constant__ TcParams p) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char *smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
   const uint32_t sb = smem_u32(smem);
@@ -415,27 +417,27 @@ __global__ void __launch_bounds__(kThr, 1)
       mbar_arrive(bar(kBarTEmpty + s));
       const int h = kvh * p.G + n / nq;
       const int q0 = (qb0 + n % nq) * kBQ;
+      // dQ^T rows (one head-dim index per thread) -> shared memory, transposed
+      // to query rows; each warp then adds whole 512-byte dq rows with
+      // 16-byte vector reductions (32 queries per pass through the buffer)
       float *stage = reinterpret_cast<float *>(smem + kOffDQ);
+      float *dst = p.ws.dq_acc + ((static_cast<size_t>(b) * p.T + q0) * p.Hq + h) * kD + 4 * lane;
+      const size_t rstride = static_cast<size_t>(p.Hq) * kD;
 #pragma unroll
       for (int hf = 0; hf < 2; ++hf) {
-        if (hf == 1) {
-          // the first half's reduce must have read the staging tile
-          if (warp == 8 && lane == 0) bulk_wait_group_read0();
-          named_barrier(1, 128);
-        }
+        if (hf == 1) named_barrier(1, 128);            // first half has been read
 #pragma unroll
         for (int c = 0; c < 32; ++c) stage[c * kD + d] = hf ? v1[c] : v0[c];
-        fence_proxy_async_smem();
         named_barrier(1, 128);
-        if (warp == 8 && lane == 0) {
-          tma_reduce_add_4d(&tmDQ, sb + kOffDQ, 0, h, q0 + 32 * hf, b);
-          bulk_commit_group();
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const int r = qd * 8 + k;                    // query row within the half
+          const int q = q0 + 32 * hf + r;
+          if (q < p.T) red_add_f4(dst + (32 * hf + r) * rstride, *reinterpret_cast<const float4 *>(stage + r * kD + 4 * lane));
         }
       }
-      if (warp == 8 && lane == 0) bulk_wait_group_read0();
       named_barrier(1, 128);
     }
-    if (warp == 8 && lane == 0) bulk_wait_group0();   // every reduce has landed before the CTA ends
     // ---- dV epilogue
     const int key = k0 + d;   // TMEM lane == key row for dV
     if (wt(bar(kBarDKV), 0)) {
@@ -528,19 +530,10 @@ cudaError_t launch_attn_bwd_causal(const void *q, const void *k, const void *v, 
     const int n = T * (kD / 2);
     causal_rope_table_kernel<<<(n + 255) / 256, 256, 0, st>>>(cw.rope, T, pos0, log2(rope_base));
   }
-  CUtensorMap tq, tdo, tk, tv, tdq;
+  CUtensorMap tq, tdo, tk, tv;
   if (!make_map(&tq, q, Hq, T, B, kBQ, why) || !make_map(&tdo, dout, Hq, T, B, kBQ, why) ||
       !make_map(&tk, k, Hkv, T, B, kBK, why) || !make_map(&tv, v, Hkv, T, B, kBK, why))
     return cudaErrorInvalidValue;
-  {
-    // fp32 dq accumulator [B][T][Hq][D], reduce-added 32 query rows at a time
-    const uint64_t dims[4] = {kD, static_cast<uint64_t>(Hq), static_cast<uint64_t>(T), static_cast<uint64_t>(B)};
-    const uint64_t strides[3] = {kD * 4, static_cast<uint64_t>(Hq) * kD * 4, static_cast<uint64_t>(T) * Hq * kD * 4};
-    const uint32_t box[4] = {kD, 1, 32, 1};
-    if (!encode_tiled(&tdq, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, cw.dq_acc, dims, strides, box,
-                      CU_TENSOR_MAP_SWIZZLE_NONE, why))
-      return cudaErrorInvalidValue;
-  }
   TcParams p;
   p.ws = cw;
   p.dk = dk;
@@ -553,7 +546,7 @@ cudaError_t launch_attn_bwd_causal(const void *q, const void *k, const void *v, 
   p.wait = w;
   e = cudaFuncSetAttribute(causal_bwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
   if (e != cudaSuccess) return e;
-  causal_bwd_tc_kernel<<<static_cast<unsigned>(ctas), kThr, kSmem, st>>>(tq, tdo, tk, tv, tdq, p);
+  causal_bwd_tc_kernel<<<static_cast<unsigned>(ctas), kThr, kSmem, st>>>(tq, tdo, tk, tv, p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const long long npairs = static_cast<long long>(qn / 2);
