@@ -57,22 +57,20 @@ constexpr int kThr = 384;  // 12 warps
 // Shared memory (offsets from a 1024-byte aligned base).
 constexpr int kOffK = 0;                 // [2 D-halves][128 keys][128 B], 128B-swizzled
 constexpr int kOffV = 32768;
-constexpr int kStages = 2;               // Q / dO (+ lse / delta) ring depth
+constexpr int kStages = 2;               // Q / dO / lse / delta ring depth
 constexpr int kOffStage = 65536;
-constexpr int kStageBytes = 32768;       // Q 16 KB, dO 16 KB
-constexpr int kStQ = 0, kStDO = 16384;
+constexpr int kStageBytes = 33792;       // Q 16 KB, dO 16 KB, lse2 256 B, delta 256 B (1 KB aligned)
+constexpr int kStQ = 0, kStDO = 16384, kStLse = 32768, kStDelta = 33024;
 constexpr int kOffP = kOffStage + kStages * kStageBytes;   // P^T [128 keys][64 queries] bf16, swizzled
 constexpr int kOffDS = kOffP + 16384;                 // dS^T [128 keys][64 queries] bf16, swizzled
-constexpr int kOffDQ = kOffDS + 16384;                // own dQ rows: 2 slots of [32 queries][128] fp32
-constexpr int kOffRecv = kOffDQ + 32768;              // partner's dQ rows: 2 slots of [32][128] fp32
-constexpr int kOffLD = kOffRecv + 32768;              // per stage: lse2 [64] then delta [64]
-constexpr int kOffBar = kOffLD + kStages * 512;
+constexpr int kOffDQ = kOffDS + 16384;                // dQ staging: [64 queries][128] fp32
+constexpr int kOffBar = kOffDQ + 32768;
 constexpr int kSmem = kOffBar + 256 + 1024;           // + alignment slack
 
 // Barrier slots (8 bytes each) after kOffBar.
 enum {
-  kBarKV = 0, kBarQFull = 1, kBarQEmpty = 3, kBarSFull = 5, kBarPFull = 7, kBarPEmpty = 8,
-  kBarDQFull = 9, kBarTEmpty = 11, kBarDKV = 13, kBarFinal = 14, kBarRecvFull = 15, kBarPeerFree = 17,
+  kBarKV = 0, kBarQFull = 1, kBarQEmpty = 4, kBarSFull = 7, kBarPFull = 9, kBarPEmpty = 10,
+  kBarDQFull = 11, kBarTEmpty = 13, kBarDKV = 15, kBarFinal = 16, kBarStaged = 17, kBarConsumed = 18,
   kNumBars = 19
 };
 constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
@@ -185,14 +183,10 @@ __global__ void __launch_bounds__(kThr, 1)
   const uint32_t sb = smem_u32(smem);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
-  // Work item: a 2-CTA cluster owns key blocks 2 pr and 2 pr + 1 of one
+  // Work item: a 2-CTA cluster owns key blocks 2*pr and 2*pr+1 of one
   // (batch, KV head); pairs of early (heavy) key blocks come first across the
-  // grid.  Both CTAs walk the query blocks they share in the same order and
-  // split the L2 reduction of their dQ partials: each CTA adds half of the
-  // rows of both partials (the other half travels to its partner through
-  // distributed shared memory), halving the fp32 reductions -- the kernel's
-  // bound on this GPU.  The even CTA's two extra (diagonal) query blocks come
-  // last in each head and are reduced by it alone.
+  // grid.  The two CTAs meet on every query block both of them process and
+  // split the reduction of their dQ partials (halving the L2 reductions).
   cg::cluster_group cluster = cg::this_cluster();
   const int rank = static_cast<int>(cluster.block_rank());
   const int per_pair = p.Hkv * p.B;
@@ -208,12 +202,7 @@ __global__ void __launch_bounds__(kThr, 1)
   const int qb_pair = 2 * (2 * pr + 1);  // first query block both CTAs process
   const int nq = active ? p.nqb - qb0 : 0;   // query blocks per head
   const int N = p.G * nq;                // iterations of this CTA
-  const int nlead = (paired && rank == 0) ? qb_pair - qb0 : 0;   // even CTA's unshared blocks
-  auto qblock = [&](int n) -> int {
-    const int i = n % nq;
-    if (nlead == 0) return qb0 + i;
-    return i < nq - nlead ? qb_pair + i : qb0 + (i - (nq - nlead));
-  };
+
   auto bar = [&](int i) -> uint32_t { return sb + kOffBar + i * 8; };
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + kOffAbort);
   auto wt = [&](uint32_t br, uint32_t parity) -> bool {
@@ -239,10 +228,8 @@ __global__ void __launch_bounds__(kThr, 1)
     mbar_init(bar(kBarPEmpty), 1);
     mbar_init(bar(kBarDKV), 1);
     mbar_init(bar(kBarFinal), 1);
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(bar(kBarRecvFull + s), 1);
-      mbar_init(bar(kBarPeerFree + s), 1);
-    }
+    mbar_init(bar(kBarStaged), 1);
+    mbar_init(bar(kBarConsumed), 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -251,8 +238,9 @@ __global__ void __launch_bounds__(kThr, 1)
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = active ? *reinterpret_cast<volatile uint32_t *>(smem + kOffTmemSlot) : 0u;
-  cluster.sync();   // the partner's barriers are initialised before any remote arrive
 
+  // the peer must see initialised barriers before it can arrive on them
+  cluster.sync();
   if (!active) {
     // idle partner of an unpaired final key block
   } else if (warp == 0) {
@@ -272,7 +260,7 @@ __global__ void __launch_bounds__(kThr, 1)
         const int s = n % kStages, cyc = n / kStages;
         if (!wt(bar(kBarQEmpty + s), (cyc & 1) ^ 1)) break;
         const int h = kvh * p.G + n / nq;
-        const int q0 = qblock(n) * kBQ;
+        const int q0 = (qb0 + n % nq) * kBQ;
         const uint32_t st = sb + kOffStage + s * kStageBytes;
         const uint32_t fb = bar(kBarQFull + s);
         mbar_arrive_expect_tx(fb, 2 * 16384 + 2 * 256);
@@ -281,8 +269,8 @@ __global__ void __launch_bounds__(kThr, 1)
           tma_load_4d(st + kStDO + hx * 8192, &tmDO, hx * 64, h, q0, b, fb);
         }
         const size_t ro = (static_cast<size_t>(b) * p.Hq + h) * p.Tp + q0;
-        bulk_load(sb + kOffLD + s * 512, p.ws.lse2 + ro, 256, fb);
-        bulk_load(sb + kOffLD + s * 512 + 256, p.ws.delta + ro, 256, fb);
+        bulk_load(st + kStLse, p.ws.lse2 + ro, 256, fb);
+        bulk_load(st + kStDelta, p.ws.delta + ro, 256, fb);
         issued = n + 1;
       }
       if (*abort_flag) {
@@ -360,12 +348,12 @@ __global__ void __launch_bounds__(kThr, 1)
     const float sl2 = p.scale * 1.4426950408889634f;
     for (int n = 0; n < N; ++n) {
       const int s = n & 1, cyc = n >> 1;
-      const int q0 = qblock(n) * kBQ;
+      const int q0 = (qb0 + n % nq) * kBQ;
       if (!wt(bar(kBarSFull + s), cyc & 1)) break;
       tc::fence_after_sync();
       const int qs = n % kStages;
-      const float *lse2 = reinterpret_cast<const float *>(smem + kOffLD + qs * 512);
-      const float *dl = lse2 + 64;
+      const float *lse2 = reinterpret_cast<const float *>(smem + kOffStage + qs * kStageBytes + kStLse);
+      const float *dl = reinterpret_cast<const float *>(smem + kOffStage + qs * kStageBytes + kStDelta);
       // only the two query blocks that overlap the key block need the causal
       // mask; queries past T have lse = +inf, so their P is exactly 0
       const bool diag = q0 < k0 + kBK;
@@ -438,40 +426,12 @@ __global__ void __launch_bounds__(kThr, 1)
     const int qd = warp & 3;
     const int d = 32 * qd + lane;                       // head-dim row of dQ^T
     const uint32_t lanebase = static_cast<uint32_t>(32 * qd) << 16;
-    float *own = reinterpret_cast<float *>(smem + kOffDQ);            // [2 slots][32][128]
-    float *recv = reinterpret_cast<float *>(smem + kOffRecv);         // [2 slots][32][128]
-    float *peer_recv = cluster.map_shared_rank(recv, rank ^ 1);
+    float *stage = reinterpret_cast<float *>(smem + kOffDQ);          // [64 queries][128] fp32
+    const float *pstage = cluster.map_shared_rank(stage, rank ^ 1);   // the partner's staging
     const size_t rstride = static_cast<size_t>(p.Hq) * kD;
-    const bool lead = warp == 8 && lane == 0;
-    auto fail = [&]() {
-      *abort_flag = 1;
-      atomicOr(p.wait.err, kErrWaitTimeout);
-    };
-    // Adds this CTA's rows of shared iteration j: its own half and the half
-    // its partner sent; then tells the partner the receive slot is free.
-    auto reduce_shared = [&](int j, float *dst, int nrows) -> bool {
-      const int slot = j & 1;
-      bool ok = true;
-      if (lead) ok = mbar_wait_cluster_bounded(bar(kBarRecvFull + slot), (j >> 1) & 1, p.wait.limit_ns);
-      if (!named_barrier_and(1, 128, ok)) return false;
-      const float *a = own + slot * 4096, *c = recv + slot * 4096;
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const int r = qd * 8 + k;                       // row within this CTA's half
-        const float4 x = *reinterpret_cast<const float4 *>(a + r * kD + 4 * lane);
-        const float4 y = *reinterpret_cast<const float4 *>(c + r * kD + 4 * lane);
-        if (r < nrows) red_add_f4(dst + r * rstride, make_float4(x.x + y.x, x.y + y.y, x.z + y.z, x.w + y.w));
-      }
-      named_barrier(1, 128);
-      if (lead) mbar_arrive_remote(bar(kBarPeerFree + slot), rank ^ 1);
-      return true;
-    };
-    int m = 0;                 // shared iterations staged so far
-    int pend = -1;             // staged shared iteration whose reduction is deferred
-    float *pend_dst = nullptr;
-    int pend_rows = 0;
-    bool ok_all = true;
-    for (int n = 0; n < N && ok_all; ++n) {
+    int m = 0;                     // paired iterations done
+    bool pending = false;          // the partner may still be reading this CTA's staging
+    for (int n = 0; n < N; ++n) {
       const int s = n & 1, cyc = n >> 1;
       // the four dq warps share named barriers: leave the loop together
       if (!named_barrier_and(1, 128, wt(bar(kBarDQFull + s), cyc & 1))) break;
@@ -481,56 +441,53 @@ __global__ void __launch_bounds__(kThr, 1)
       tc::fence_before_sync();
       mbar_arrive(bar(kBarTEmpty + s));
       const int h = kvh * p.G + n / nq;
-      const int qb = qblock(n);
+      const int qb = qb0 + n % nq;
       const int q0 = qb * kBQ;
-      float *rows = p.ws.dq_acc + ((static_cast<size_t>(b) * p.T + q0) * p.Hq + h) * kD + 4 * lane;
-      if (paired && qb >= qb_pair) {
-        // ---- shared query block: own half -> own slot, other half -> partner
-        const int slot = m & 1;
-        bool ok = true;
-        if (lead) ok = mbar_wait_cluster_bounded(bar(kBarPeerFree + slot), ((m >> 1) & 1) ^ 1, p.wait.limit_ns);
-        if (!named_barrier_and(1, 128, ok)) { fail(); break; }
-        float *mine = own + slot * 4096 + d;
-        float *theirs = peer_recv + slot * 4096 + d;
+      const bool shared_q = paired && qb >= qb_pair;
+      if (pending) {
+        const bool ok = mbar_wait_cluster_bounded(bar(kBarConsumed), (m - 1) & 1, p.wait.limit_ns);
+        if (!ok) { *abort_flag = 1; atomicOr(p.wait.err, kErrWaitTimeout); }
+        if (!named_barrier_and(1, 128, ok)) break;
+        pending = false;
+      }
+      // dQ^T rows (one head-dim index per thread) -> shared memory as query rows
 #pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          const float lo = v0[c], hi = v1[c];            // query rows c and 32 + c
-          mine[c * kD] = rank == 0 ? lo : hi;
-          theirs[c * kD] = rank == 0 ? hi : lo;
-        }
-        named_barrier(1, 128);
-        if (lead) mbar_arrive_remote(bar(kBarRecvFull + slot), rank ^ 1);
-        // reduce the previous shared block now, giving the partner one block of slack
-        if (pend >= 0) {
-          if (!reduce_shared(pend, pend_dst, pend_rows)) { fail(); break; }
-        }
-        pend = m;
-        const int nrows = min(32, p.T - (q0 + 32 * rank));
-        pend_dst = rows + static_cast<size_t>(32 * rank) * rstride;
-        pend_rows = nrows;
-        ++m;
-      } else {
-        // ---- block only this CTA covers: flush the deferred reduction, then
-        // stage all 64 rows in the two own slots and reduce them
-        if (pend >= 0) {
-          if (!reduce_shared(pend, pend_dst, pend_rows)) { fail(); break; }
-          pend = -1;
-        }
-#pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          own[c * kD + d] = v0[c];
-          own[(32 + c) * kD + d] = v1[c];
-        }
-        named_barrier(1, 128);
+      for (int c = 0; c < 32; ++c) {
+        stage[c * kD + d] = v0[c];
+        stage[(32 + c) * kD + d] = v1[c];
+      }
+      named_barrier(1, 128);
+      float *dst = p.ws.dq_acc + ((static_cast<size_t>(b) * p.T + q0) * p.Hq + h) * kD + 4 * lane;
+      if (!shared_q) {
+        // only this CTA contributes here: add all 64 rows, 16 per warp, as
+        // 16-byte vector reductions of whole 512-byte dq rows
 #pragma unroll
         for (int k = 0; k < 16; ++k) {
           const int r = qd * 16 + k;
-          if (q0 + r < p.T) red_add_f4(rows + r * rstride, *reinterpret_cast<const float4 *>(own + r * kD + 4 * lane));
+          if (q0 + r < p.T) red_add_f4(dst + r * rstride, *reinterpret_cast<const float4 *>(stage + r * kD + 4 * lane));
         }
         named_barrier(1, 128);
+      } else {
+        // both CTAs staged a partial of this query block: this CTA adds rows
+        // [32 rank, 32 rank + 32) of both and reduces them once
+        if (warp == 8 && lane == 0) mbar_arrive_remote(bar(kBarStaged), rank ^ 1);
+        const bool ok = mbar_wait_cluster_bounded(bar(kBarStaged), m & 1, p.wait.limit_ns);
+        if (!ok) { *abort_flag = 1; atomicOr(p.wait.err, kErrWaitTimeout); }
+        if (!named_barrier_and(1, 128, ok)) break;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const int r = 32 * rank + qd * 8 + k;
+          const float4 a = *reinterpret_cast<const float4 *>(stage + r * kD + 4 * lane);
+          const float4 c = *reinterpret_cast<const float4 *>(pstage + r * kD + 4 * lane);
+          if (q0 + r < p.T) red_add_f4(dst + r * rstride, make_float4(a.x + c.x, a.y + c.y, a.z + c.z, a.w + c.w));
+        }
+        named_barrier(1, 128);
+        if (warp == 8 && lane == 0) mbar_arrive_remote(bar(kBarConsumed), rank ^ 1);
+        pending = true;
+        ++m;
       }
     }
-    if (pend >= 0 && !*abort_flag) reduce_shared(pend, pend_dst, pend_rows);
+    if (pending) mbar_wait_cluster_bounded(bar(kBarConsumed), (m - 1) & 1, p.wait.limit_ns);
     // ---- dV epilogue
     const int key = k0 + d;   // TMEM lane == key row for dV
     if (wt(bar(kBarDKV), 0)) {
@@ -553,8 +510,9 @@ __global__ void __launch_bounds__(kThr, 1)
     tc::fence_after_sync();
     tc::tmem_dealloc(tmem, 512);
   }
-  // neither CTA leaves while its partner may still write to or signal it
-  cluster.sync();
+  // neither CTA leaves while its partner may still touch its shared memory
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+  asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
 }
 
 // dq = R(-theta_t) (scale * acc), one thread per rotary pair.
