@@ -38,13 +38,10 @@
 //   [256,384) dV        [384,512) dK
 // Q / dO / lse / delta arrive through a 3-deep TMA ring, so the load for block
 // n+3 is in flight while blocks n+1 and n+2 compute.
-#include <cooperative_groups.h>
 #include <math.h>
 
 #include "abw_host.h"
 #include "tcgen05.cuh"
-
-namespace cg = cooperative_groups;
 
 namespace abw {
 namespace {
@@ -57,21 +54,20 @@ constexpr int kThr = 384;  // 12 warps
 // Shared memory (offsets from a 1024-byte aligned base).
 constexpr int kOffK = 0;                 // [2 D-halves][128 keys][128 B], 128B-swizzled
 constexpr int kOffV = 32768;
-constexpr int kStages = 2;               // Q / dO / lse / delta ring depth
+constexpr int kStages = 3;               // Q / dO / lse / delta ring depth
 constexpr int kOffStage = 65536;
 constexpr int kStageBytes = 33792;       // Q 16 KB, dO 16 KB, lse2 256 B, delta 256 B (1 KB aligned)
 constexpr int kStQ = 0, kStDO = 16384, kStLse = 32768, kStDelta = 33024;
 constexpr int kOffP = kOffStage + kStages * kStageBytes;   // P^T [128 keys][64 queries] bf16, swizzled
 constexpr int kOffDS = kOffP + 16384;                 // dS^T [128 keys][64 queries] bf16, swizzled
-constexpr int kOffDQ = kOffDS + 16384;                // dQ staging: [64 queries][128] fp32
-constexpr int kOffBar = kOffDQ + 32768;
+constexpr int kOffDQ = kOffDS + 16384;                // dQ staging: [32 queries][128] fp32
+constexpr int kOffBar = kOffDQ + 16384;
 constexpr int kSmem = kOffBar + 256 + 1024;           // + alignment slack
 
 // Barrier slots (8 bytes each) after kOffBar.
 enum {
   kBarKV = 0, kBarQFull = 1, kBarQEmpty = 4, kBarSFull = 7, kBarPFull = 9, kBarPEmpty = 10,
-  kBarDQFull = 11, kBarTEmpty = 13, kBarDKV = 15, kBarFinal = 16, kBarStaged = 17, kBarConsumed = 18,
-  kNumBars = 19
+  kBarDQFull = 11, kBarTEmpty = 13, kBarDKV = 15, kBarFinal = 16, kNumBars = 17
 };
 constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
 constexpr int kOffAbort = kOffTmemSlot + 4;
@@ -183,25 +179,24 @@ __global__ void __launch_bounds__(kThr, 1)
   const uint32_t sb = smem_u32(smem);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
-  // Work item: a 2-CTA cluster owns key blocks 2*pr and 2*pr+1 of one
-  // (batch, KV head); pairs of early (heavy) key blocks come first across the
-  // grid.  The two CTAs meet on every query block both of them process and
-  // split the reduction of their dQ partials (halving the L2 reductions).
-  cg::cluster_group cluster = cg::this_cluster();
-  const int rank = static_cast<int>(cluster.block_rank());
-  const int per_pair = p.Hkv * p.B;
-  const int ci = blockIdx.x >> 1;
-  const int pr = ci / per_pair;
-  const int rem = ci - pr * per_pair;
+  // work item: heavy (early) key blocks first across the whole grid
+  const int per_kb = p.Hkv * p.B;
+  const int kb = blockIdx.x / per_kb;
+  const int rem = blockIdx.x - kb * per_kb;
   const int kvh = rem % p.Hkv, b = rem / p.Hkv;
-  const int kb = 2 * pr + rank;
-  const bool active = kb < p.nkb;        // the odd partner of a final unpaired block idles
-  const bool paired = 2 * pr + 1 < p.nkb;
   const int k0 = kb * kBK;
   const int qb0 = k0 / kBQ;
-  const int qb_pair = 2 * (2 * pr + 1);  // first query block both CTAs process
-  const int nq = active ? p.nqb - qb0 : 0;   // query blocks per head
+  const int nq = p.nqb - qb0;            // query blocks per head
   const int N = p.G * nq;                // iterations of this CTA
+  // Query block of iteration n.  Each CTA walks its query blocks from a
+  // different starting point (rotated by its key block), so CTAs of the same
+  // head working at the same time reduce into different dq rows.
+  const int rot = (kb * 5) % nq;
+  auto qblock = [&](int n) -> int {
+    int i = n % nq + rot;
+    if (i >= nq) i -= nq;
+    return qb0 + i;
+  };
 
   auto bar = [&](int i) -> uint32_t { return sb + kOffBar + i * 8; };
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + kOffAbort);
@@ -228,22 +223,16 @@ __global__ void __launch_bounds__(kThr, 1)
     mbar_init(bar(kBarPEmpty), 1);
     mbar_init(bar(kBarDKV), 1);
     mbar_init(bar(kBarFinal), 1);
-    mbar_init(bar(kBarStaged), 1);
-    mbar_init(bar(kBarConsumed), 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
-  if (warp == 2 && active) tc::tmem_alloc(sb + kOffTmemSlot, 512);
+  if (warp == 2) tc::tmem_alloc(sb + kOffTmemSlot, 512);
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
-  const uint32_t tmem = active ? *reinterpret_cast<volatile uint32_t *>(smem + kOffTmemSlot) : 0u;
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + kOffTmemSlot);
 
-  // the peer must see initialised barriers before it can arrive on them
-  cluster.sync();
-  if (!active) {
-    // idle partner of an unpaired final key block
-  } else if (warp == 0) {
+  if (warp == 0) {
     // ============================ TMA producer ============================
     if (lane == 0) {
       prefetch_tensormap(&tmQ);
@@ -260,7 +249,7 @@ __global__ void __launch_bounds__(kThr, 1)
         const int s = n % kStages, cyc = n / kStages;
         if (!wt(bar(kBarQEmpty + s), (cyc & 1) ^ 1)) break;
         const int h = kvh * p.G + n / nq;
-        const int q0 = (qb0 + n % nq) * kBQ;
+        const int q0 = qblock(n) * kBQ;
         const uint32_t st = sb + kOffStage + s * kStageBytes;
         const uint32_t fb = bar(kBarQFull + s);
         mbar_arrive_expect_tx(fb, 2 * 16384 + 2 * 256);
@@ -348,7 +337,7 @@ __global__ void __launch_bounds__(kThr, 1)
     const float sl2 = p.scale * 1.4426950408889634f;
     for (int n = 0; n < N; ++n) {
       const int s = n & 1, cyc = n >> 1;
-      const int q0 = (qb0 + n % nq) * kBQ;
+      const int q0 = qblock(n) * kBQ;
       if (!wt(bar(kBarSFull + s), cyc & 1)) break;
       tc::fence_after_sync();
       const int qs = n % kStages;
@@ -426,11 +415,6 @@ __global__ void __launch_bounds__(kThr, 1)
     const int qd = warp & 3;
     const int d = 32 * qd + lane;                       // head-dim row of dQ^T
     const uint32_t lanebase = static_cast<uint32_t>(32 * qd) << 16;
-    float *stage = reinterpret_cast<float *>(smem + kOffDQ);          // [64 queries][128] fp32
-    const float *pstage = cluster.map_shared_rank(stage, rank ^ 1);   // the partner's staging
-    const size_t rstride = static_cast<size_t>(p.Hq) * kD;
-    int m = 0;                     // paired iterations done
-    bool pending = false;          // the partner may still be reading this CTA's staging
     for (int n = 0; n < N; ++n) {
       const int s = n & 1, cyc = n >> 1;
       // the four dq warps share named barriers: leave the loop together
@@ -441,53 +425,28 @@ __global__ void __launch_bounds__(kThr, 1)
       tc::fence_before_sync();
       mbar_arrive(bar(kBarTEmpty + s));
       const int h = kvh * p.G + n / nq;
-      const int qb = qb0 + n % nq;
-      const int q0 = qb * kBQ;
-      const bool shared_q = paired && qb >= qb_pair;
-      if (pending) {
-        const bool ok = mbar_wait_cluster_bounded(bar(kBarConsumed), (m - 1) & 1, p.wait.limit_ns);
-        if (!ok) { *abort_flag = 1; atomicOr(p.wait.err, kErrWaitTimeout); }
-        if (!named_barrier_and(1, 128, ok)) break;
-        pending = false;
-      }
-      // dQ^T rows (one head-dim index per thread) -> shared memory as query rows
-#pragma unroll
-      for (int c = 0; c < 32; ++c) {
-        stage[c * kD + d] = v0[c];
-        stage[(32 + c) * kD + d] = v1[c];
-      }
-      named_barrier(1, 128);
+      const int q0 = qblock(n) * kBQ;
+      // dQ^T rows (one head-dim index per thread) -> shared memory, transposed
+      // to query rows; each warp then adds whole 512-byte dq rows with
+      // 16-byte vector reductions (32 queries per pass through the buffer)
+      float *stage = reinterpret_cast<float *>(smem + kOffDQ);
       float *dst = p.ws.dq_acc + ((static_cast<size_t>(b) * p.T + q0) * p.Hq + h) * kD + 4 * lane;
-      if (!shared_q) {
-        // only this CTA contributes here: add all 64 rows, 16 per warp, as
-        // 16-byte vector reductions of whole 512-byte dq rows
+      const size_t rstride = static_cast<size_t>(p.Hq) * kD;
 #pragma unroll
-        for (int k = 0; k < 16; ++k) {
-          const int r = qd * 16 + k;
-          if (q0 + r < p.T) red_add_f4(dst + r * rstride, *reinterpret_cast<const float4 *>(stage + r * kD + 4 * lane));
-        }
+      for (int hf = 0; hf < 2; ++hf) {
+        if (hf == 1) named_barrier(1, 128);            // first half has been read
+#pragma unroll
+        for (int c = 0; c < 32; ++c) stage[c * kD + d] = hf ? v1[c] : v0[c];
         named_barrier(1, 128);
-      } else {
-        // both CTAs staged a partial of this query block: this CTA adds rows
-        // [32 rank, 32 rank + 32) of both and reduces them once
-        if (warp == 8 && lane == 0) mbar_arrive_remote(bar(kBarStaged), rank ^ 1);
-        const bool ok = mbar_wait_cluster_bounded(bar(kBarStaged), m & 1, p.wait.limit_ns);
-        if (!ok) { *abort_flag = 1; atomicOr(p.wait.err, kErrWaitTimeout); }
-        if (!named_barrier_and(1, 128, ok)) break;
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
-          const int r = 32 * rank + qd * 8 + k;
-          const float4 a = *reinterpret_cast<const float4 *>(stage + r * kD + 4 * lane);
-          const float4 c = *reinterpret_cast<const float4 *>(pstage + r * kD + 4 * lane);
-          if (q0 + r < p.T) red_add_f4(dst + r * rstride, make_float4(a.x + c.x, a.y + c.y, a.z + c.z, a.w + c.w));
+          const int r = qd * 8 + k;                    // query row within the half
+          const int q = q0 + 32 * hf + r;
+          if (q < p.T) red_add_f4(dst + (32 * hf + r) * rstride, *reinterpret_cast<const float4 *>(stage + r * kD + 4 * lane));
         }
-        named_barrier(1, 128);
-        if (warp == 8 && lane == 0) mbar_arrive_remote(bar(kBarConsumed), rank ^ 1);
-        pending = true;
-        ++m;
       }
+      named_barrier(1, 128);
     }
-    if (pending) mbar_wait_cluster_bounded(bar(kBarConsumed), (m - 1) & 1, p.wait.limit_ns);
     // ---- dV epilogue
     const int key = k0 + d;   // TMEM lane == key row for dV
     if (wt(bar(kBarDKV), 0)) {
@@ -506,13 +465,10 @@ __global__ void __launch_bounds__(kThr, 1)
   }
   tc::fence_before_sync();
   __syncthreads();
-  if (warp == 2 && active) {
+  if (warp == 2) {
     tc::fence_after_sync();
     tc::tmem_dealloc(tmem, 512);
   }
-  // neither CTA leaves while its partner may still touch its shared memory
-  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
-  asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
 }
 
 // dq = R(-theta_t) (scale * acc), one thread per rotary pair.
@@ -562,7 +518,7 @@ cudaError_t launch_attn_bwd_causal(const void *q, const void *k, const void *v, 
   }
   const int nkb = (T + kBK - 1) / kBK;
   const int Tp = padded_T(T);
-  const long long ctas = 2LL * ((nkb + 1) / 2) * Hkv * B;   // 2-CTA clusters over key-block pairs
+  const long long ctas = static_cast<long long>(nkb) * Hkv * B;
   if (ctas > 0x7fffffffLL) {
     *why = "grid too large";
     return cudaErrorNotSupported;
@@ -599,21 +555,8 @@ cudaError_t launch_attn_bwd_causal(const void *q, const void *k, const void *v, 
   p.wait = w;
   e = cudaFuncSetAttribute(causal_bwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
   if (e != cudaSuccess) return e;
-  {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(ctas), 1, 1);
-    cfg.blockDim = dim3(kThr, 1, 1);
-    cfg.dynamicSmemBytes = kSmem;
-    cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, causal_bwd_tc_kernel, tq, tdo, tk, tv, p);
-  }
+  causal_bwd_tc_kernel<<<static_cast<unsigned>(ctas), kThr, kSmem, st>>>(tq, tdo, tk, tv, p);
+  e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const long long npairs = static_cast<long long>(qn / 2);
   causal_dq_finalize<<<static_cast<unsigned>((npairs + 255) / 256), 256, 0, st>>>(cw.dq_acc, cw.rope, dq, npairs, T,
