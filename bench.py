@@ -262,6 +262,84 @@ def recorded_traffic(kernel_key, src_files):
     return e.get("dram_bytes_per_launch")
 
 
+def run_chain(abw, saved_forward, W, dev, stream, args, barrier, max_over_ranks, world, local):
+    """The 30-layer backward chain (GQA 20/5, B=2, T=512, hidden 2560): per
+    layer, in reverse, RMSNorm backward of the saved normed input (bf16 dx is
+    attention's dOut), then causal attention backward with RoPE on dq/dk.
+    The 30 layers are captured into one CUDA graph and replayed."""
+    import torch
+    shape = W.CHAIN_LAYER
+    L = W.CHAIN_LAYERS
+    dh = W.chain_dhidden().to(dev)
+    layers = []
+    for layer in range(L):
+        inp = W.chain_layer_inputs(layer)
+        g = {k: v.to(dev) for k, v in inp.items() if torch.is_tensor(v)}
+        o, lse = saved_forward.causal_forward(g["q"], g["k"], g["v"], shape.scale)
+        g.update(o=o, lse=lse, eps=inp["eps"],
+                 dx=torch.empty(g["x"].shape, dtype=torch.bfloat16, device=dev),
+                 dq=torch.empty(g["q"].shape, dtype=torch.float32, device=dev),
+                 dk=torch.empty(g["k"].shape, dtype=torch.float32, device=dev),
+                 dv=torch.empty(g["v"].shape, dtype=torch.float32, device=dev))
+        layers.append(g)
+    ws = torch.empty(abw.attn_bwd_causal_workspace_bytes(shape.B, shape.T, shape.Hq, shape.D), dtype=torch.uint8,
+                     device=dev)
+
+    def chain_once(st):
+        for g in reversed(layers):
+            abw.rmsnorm_bwd(g["x"], g["gamma"], dh, eps=g["eps"], dx=g["dx"], stream=st)
+            dout = g["dx"].view(shape.B, shape.T, shape.Hq, shape.D)
+            abw.attn_bwd_causal(g["q"], g["k"], g["v"], g["o"], dout, g["lse"], shape.scale, shape.rope_base, 0,
+                                dq=g["dq"], dk=g["dk"], dv=g["dv"], workspace=ws, stream=st)
+
+    for _ in range(2):
+        chain_once(stream)
+    abw.device_check(stream)
+    mode = "cuda_graph"
+    graph = None
+    try:
+        side = torch.cuda.Stream(device=dev)
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            chain_once(side)                       # warm up on the capture stream
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph, stream=side):
+                chain_once(torch.cuda.current_stream())
+        stream.wait_stream(side)
+        torch.cuda.synchronize()
+    except Exception as exc:                       # capture unsupported here: time eager launches
+        graph = None
+        mode = f"eager ({type(exc).__name__})"
+        torch.cuda.synchronize()
+
+    def run():
+        if graph is not None:
+            graph.replay()
+        else:
+            chain_once(stream)
+
+    for _ in range(max(3, args.warmup)):
+        run()
+    torch.cuda.synchronize()
+    abw.device_check(stream)
+    barrier()
+    reps = max(3, args.steps)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(reps):
+        run()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    abw.device_check(stream)
+    ms = max_over_ranks(e0.elapsed_time(e1)) / reps
+    flops = L * causal_flops(shape.B, shape.T, shape.Hq, shape.D)
+    rms_bytes = L * rmsnorm_bytes(shape.B * shape.T, W.CHAIN_HIDDEN, x_es=2, dx_es=2)
+    return {"workload": "chain_30_layers_b2_t512_hq20_hkv5_d128_n2560", "ms_per_chain": round(ms, 4),
+            "us_per_layer": round(1e3 * ms / L, 2), "attn_tflops": round(world * flops / (ms * 1e-3) / 1e12, 2),
+            "launch": mode, "flops_per_chain": flops, "rmsnorm_bytes_per_chain": rms_bytes}
+
+
 def keep_busy(fn, stream, seconds):
     """Runs `fn` back to back for about `seconds` (untimed warm-up load)."""
     import torch
@@ -436,6 +514,12 @@ def run_native(args):
         del cin, o, lse, cq, ck, cv, ws
         torch.cuda.empty_cache()
 
+    # ------------------------------------------------------------ 30-layer chain
+    chain = None
+    if not args.skip_chain:
+        chain = run_chain(abw, saved_forward, W, dev, stream, args, barrier, max_over_ranks, world, local)
+        torch.cuda.empty_cache()
+
     peaks, kind = load_peaks()
     achieved = dec_bytes / (kern_ms * 1e-3) / 1e9
     roofline = {"bound": "hbm", "achieved": round(achieved, 2), "peak": peaks["hbm_gbs"], "unit": "GB/s",
@@ -469,6 +553,7 @@ def run_native(args):
             "gpu_launches": launches,
             "clocks": clocks.summary(h0, h1),
             "causal_t2048": causal,
+            "chain_30_layers": chain,
         }
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -484,6 +569,7 @@ def main():
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
     ap.add_argument("--skip-causal", action="store_true")
     ap.add_argument("--skip-cpu", action="store_true")
+    ap.add_argument("--skip-chain", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "native":
         args.warmup = 3
