@@ -170,6 +170,38 @@ abw_status attn_bwd_causal(const void *q, const void *k, const void *v, const vo
                            float rope_base, int pos0,
                            void *workspace, size_t workspace_bytes, abw_stream stream);
 
+/*
+ * attn_bwd_causal_noalloc -- attn_bwd_causal for callers that cannot allocate
+ * device memory: no workspace argument, and the call allocates nothing.  (The
+ * pages have no counterpart; this is an interface convenience.)
+ *
+ * Who needs it: code that runs where cudaMalloc is off limits -- inside a
+ * CUDA stream capture or a custom allocator's callback, in a process whose
+ * device memory is owned by another framework's pool, or in a plugin given
+ * only the tensors it works on.  Such a caller passes the inputs and outputs
+ * as for attn_bwd_causal; the scratch comes from a 32 MiB array in the
+ * library's device image (a file-scope __device__ variable), which every GPU
+ * that loads the library keeps until the process exits.
+ *
+ *   Arguments, layouts and results: as attn_bwd_causal.
+ *   Limit: the sizes must need at most 32 MiB of scratch
+ *   (attn_bwd_causal_workspace_bytes(B, T, Hq, D) <= 33554432, roughly
+ *   B*T*Hq*D*4 < 32 MiB, e.g. B=2, T=512, Hq=20); larger sizes return
+ *   ABW_EWORKSPACE without launching anything.
+ *   First call on a device: looks up the array's device address on that
+ *   device (cudaGetSymbolAddress) and caches it; make that first call before
+ *   any stream capture that should contain it.
+ *   Sharing: every call on a device uses the same array.  Each call clears
+ *   the part that must start at zero (the dq accumulator) and rewrites the
+ *   rest, so consecutive calls are independent -- but calls that overlap on
+ *   the GPU (different streams, no ordering between them) race on the array.
+ */
+abw_status attn_bwd_causal_noalloc(const void *q, const void *k, const void *v, const void *o,
+                                   const void *dout, const float *lse,
+                                   float *dq, float *dk, float *dv,
+                                   int B, int T, int Hq, int Hkv, int D, float scale,
+                                   float rope_base, int pos0, abw_stream stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -34,6 +34,8 @@ SIGNATURES = {
     "attn_bwd_causal_workspace_bytes": (_sz, [_i, _i, _i, _i]),
     "attn_bwd_causal": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _f, _i,
                              _vp, _sz, _vp]),
+    "attn_bwd_causal_noalloc": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _f, _i,
+                                     _vp]),
 }
 
 

@@ -45,4 +45,11 @@ cudaError_t launch_attn_bwd_causal(const void *q, const void *k, const void *v, 
 
 cudaError_t launch_selftest_wait(const WaitCtl &w, cudaStream_t st);
 
+// Size of the fixed device scratch behind attn_bwd_causal_noalloc.
+constexpr size_t kNoAllocScratchBytes = 32ull << 20;   // 32 MiB
+
+// Device address of that scratch on the current device (resolved once per
+// device).  Never allocates.
+cudaError_t noalloc_scratch(void **ptr, const char **why);
+
 }  // namespace abw

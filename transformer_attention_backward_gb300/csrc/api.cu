@@ -281,4 +281,42 @@ abw_status attn_bwd_causal(const void *q, const void *k, const void *v, const vo
                    "attn_bwd_causal", why);
 }
 
+abw_status attn_bwd_causal_noalloc(const void *q, const void *k, const void *v, const void *o, const void *dout,
+                                   const float *lse, float *dq, float *dk, float *dv, int B, int T, int Hq, int Hkv,
+                                   int D, float scale, float rope_base, int pos0, abw_stream stream) {
+  // Same checks and kernels as attn_bwd_causal; the workspace is the
+  // library's built-in device scratch instead of a caller allocation.
+  if (B < 0 || T < 0 || Hq < 0 || Hkv < 0) return fail(ABW_EINVAL, "attn_bwd_causal_noalloc: negative size");
+  if (Hkv == 0 || Hq % Hkv != 0)
+    return fail(ABW_EINVAL, "attn_bwd_causal_noalloc: Hq=%d not a multiple of Hkv=%d", Hq, Hkv);
+  if (D != 128) return fail(ABW_ENOTSUP, "attn_bwd_causal_noalloc: D=%d unsupported (D == 128)", D);
+  if (rope_base > 0.0f && pos0 < 0) return fail(ABW_EINVAL, "attn_bwd_causal_noalloc: pos0 must be >= 0");
+  if (!(scale == scale)) return fail(ABW_EINVAL, "attn_bwd_causal_noalloc: scale is NaN");
+  if (B == 0 || T == 0 || Hq == 0) return ABW_OK;
+  const size_t need = abw::causal_workspace_bytes(B, T, Hq, D);
+  if (need > abw::kNoAllocScratchBytes)
+    return fail(ABW_EWORKSPACE,
+                "attn_bwd_causal_noalloc: these sizes need %zu bytes of scratch, more than the built-in %zu "
+                "(B*T*Hq*D*4 must stay below about 32 MiB); use attn_bwd_causal with a workspace",
+                need, static_cast<size_t>(abw::kNoAllocScratchBytes));
+  const size_t qn = static_cast<size_t>(B) * T * Hq * D, kn = static_cast<size_t>(B) * T * Hkv * D;
+  Range in[] = {{"q", q, qn * 2},    {"k", k, kn * 2},
+                {"v", v, kn * 2},    {"o", o, qn * 2},
+                {"dout", dout, qn * 2}, {"lse", lse, static_cast<size_t>(B) * Hq * T * 4}};
+  Range out[] = {{"dq", dq, qn * 4}, {"dk", dk, kn * 4}, {"dv", dv, kn * 4}};
+  abw_status st = check_buffers("attn_bwd_causal_noalloc", in, 6, out, 3);
+  if (st != ABW_OK) return st;
+  abw::WaitCtl w = abw::wait_ctl();
+  if (!w.err) return fail(ABW_ECUDA, "attn_bwd_causal_noalloc: no CUDA device");
+  const char *why = nullptr;
+  void *scratch = nullptr;
+  cudaError_t e = abw::noalloc_scratch(&scratch, &why);
+  if (e != cudaSuccess) return from_cuda(e, "attn_bwd_causal_noalloc", why);
+  const double rb = rope_base > 0.0f ? static_cast<double>(rope_base) : 0.0;
+  return from_cuda(abw::launch_attn_bwd_causal(q, k, v, o, dout, lse, dq, dk, dv, B, T, Hq, Hkv, D, scale, rb, pos0,
+                                               scratch, abw::kNoAllocScratchBytes, w,
+                                               reinterpret_cast<cudaStream_t>(stream), &why),
+                   "attn_bwd_causal_noalloc", why);
+}
+
 }  // extern "C"

@@ -40,6 +40,8 @@
 // n+3 is in flight while blocks n+1 and n+2 compute.
 #include <math.h>
 
+#include <mutex>
+
 #include "abw_host.h"
 #include "tcgen05.cuh"
 
@@ -499,7 +501,39 @@ bool make_map(CUtensorMap *m, const void *base, int H, int T, int B, uint32_t ro
                       CU_TENSOR_MAP_SWIZZLE_128B, why);
 }
 
+// Scratch for attn_bwd_causal_noalloc: a fixed device array the library
+// owns, so that entry point never allocates.  Every GPU that loads the
+// library holds it until the process exits.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
 }  // namespace
+
+cudaError_t noalloc_scratch(void **ptr, const char **why) {
+  // Resolved once per device, with that device current.  A symbol's name in
+  // host code is only a host-side stand-in; the device address must come
+  // from the runtime.
+  static std::mutex mu;
+  static void *addr[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) {
+    *why = "device ordinal out of range";
+    return cudaErrorInvalidDevice;
+  }
+  std::lock_guard<std::mutex> lk(mu);
+  if (addr[dev] == nullptr) {
+    void *p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) {
+      *why = "cudaGetSymbolAddress of the built-in scratch failed";
+      return e;
+    }
+    addr[dev] = p;
+  }
+  *ptr = addr[dev];
+  return cudaSuccess;
+}
 
 size_t causal_workspace_bytes(int B, int T, int Hq, int D) {
   const size_t Tp = static_cast<size_t>(padded_T(T));
