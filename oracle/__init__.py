@@ -73,8 +73,9 @@ def softmax_forward(x):
 def softmax_backward(s, dy):
     """dx_i = s_i * (dy_i - sum_j s_j * dy_j), given the probabilities s.
 
-    softmaxBackward states this formula; the Hesper GPU path feeds it the
-    saved probabilities ("Use saved attnBuf for correct softmax backward")."""
+    softmaxBackward states this formula; Hesper's GPU path evaluates it on the
+    probabilities it saved during the forward pass (pull request #1, the
+    softmax-backward fix)."""
     s = _f64(s)
     dy = _f64(dy)
     inner = np.sum(s * dy, axis=-1, keepdims=True)
@@ -375,9 +376,9 @@ def causal_backward(q, k, v, dout, scale, rope_base=0.0, pos0=0, kv_heads=None,
 
 
 # ==========================================================================
-# One layer of the backward chain (Hesper pull request #1: "Complete
-# attention backward chain": ... RMSNorm backward (sub-norm) -> apply
-# backward -> softmax backward -> score backward -> RoPE backward -> dQ)
+# One layer of the backward chain (Hesper pull request #1, the commit that
+# completes the attention backward chain: the sub-norm RMSNorm backward runs
+# first, then the attention steps -- apply, softmax, score -- and RoPE last)
 # ==========================================================================
 def chain_layer_backward(x, gamma, dhidden, q, k, v, eps, scale, rope_base,
                          kv_heads=None):
