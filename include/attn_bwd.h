@@ -143,8 +143,11 @@ abw_status attn_bwd_decode(const float *q, const void *k, const void *v, const f
 
 /*
  * attn_bwd_causal_workspace_bytes -- workspace size attn_bwd_causal needs for
- * these sizes (fp32 dQ accumulator [B][T][Hq][D], delta [B][Hq][T], RoPE
- * table [T][D/2] cos/sin, and 256-byte alignment slack).
+ * these sizes, with Tp = T rounded up to 128 and nb = Tp / 128: delta and
+ * lse * log2(e), each f32 [B][Hq][Tp]; the RoPE table [T][D/2] of
+ * scale * (cos, sin); the bf16 dS tiles of the causal half, 16 KB per
+ * (128-key block, 64-query block) pair, B * Hq * (nb^2 + nb) of them; and
+ * 256-byte alignment slack.  About B * Hq * Tp * (Tp + 136) bytes.
  */
 size_t attn_bwd_causal_workspace_bytes(int B, int T, int Hq, int D);
 
@@ -186,15 +189,15 @@ abw_status attn_bwd_causal(const void *q, const void *k, const void *v, const vo
  *   Arguments, layouts and results: as attn_bwd_causal.
  *   Limit: the sizes must need at most 32 MiB of scratch
  *   (attn_bwd_causal_workspace_bytes(B, T, Hq, D) <= 33554432, roughly
- *   B*T*Hq*D*4 < 32 MiB, e.g. B=2, T=512, Hq=20); larger sizes return
- *   ABW_EWORKSPACE without launching anything.
+ *   B * Hq * T^2 < 32 MiB, e.g. B=2, T=512, Hq=20 needs about 13 MB); larger
+ *   sizes return ABW_EWORKSPACE without launching anything.
  *   First call on a device: looks up the array's device address on that
  *   device (cudaGetSymbolAddress) and caches it; make that first call before
  *   any stream capture that should contain it.
- *   Sharing: every call on a device uses the same array.  Each call clears
- *   the part that must start at zero (the dq accumulator) and rewrites the
- *   rest, so consecutive calls are independent -- but calls that overlap on
- *   the GPU (different streams, no ordering between them) race on the array.
+ *   Sharing: every call on a device uses the same array.  Each call writes
+ *   every part of it that it later reads, so consecutive calls are
+ *   independent -- but calls that overlap on the GPU (different streams, no
+ *   ordering between them) race on the array.
  */
 abw_status attn_bwd_causal_noalloc(const void *q, const void *k, const void *v, const void *o,
                                    const void *dout, const float *lse,

@@ -60,7 +60,9 @@ def test_noalloc_matches_workspace_version_twice():
 
 def test_noalloc_rejects_sizes_beyond_the_scratch():
     lib = B.load()
-    # B=4, T=2048, Hq=20 needs ~168 MB of scratch: refused before any launch
+    # B=4, T=2048, Hq=20 needs ~360 MB of scratch (mostly the bf16 dS tiles
+    # of the causal half): refused before any launch
+    assert lib.attn_bwd_causal_workspace_bytes(4, 2048, 20, 128) > 32 << 20
     status = lib.attn_bwd_causal_noalloc(None, None, None, None, None, None, None, None, None,
                                          4, 2048, 20, 20, 128, 0.088, 0.0, 0, None)
     assert status == B.EWORKSPACE

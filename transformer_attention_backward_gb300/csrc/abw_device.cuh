@@ -14,6 +14,7 @@ namespace abw {
 enum : unsigned int {
   kErrWaitTimeout = 1u,   // a bounded barrier wait ran out
   kErrSelfTest = 2u,      // the self-test kernel's wait ran out (expected)
+  kErrSmemAlign = 4u,     // a kernel found its shared memory misaligned and did no work
 };
 
 // Everything a kernel needs to report a failed wait.
@@ -164,6 +165,13 @@ __device__ __forceinline__ void tma_reduce_add_4d(const CUtensorMap *map, uint32
           reinterpret_cast<uint64_t>(map)),
       "r"(src), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
       : "memory");
+}
+// Plain bulk copy shared -> global, tracked by bulk groups (both addresses
+// 16-byte aligned, size a multiple of 16 bytes).
+__device__ __forceinline__ void bulk_store(void *dst, uint32_t src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(reinterpret_cast<uint64_t>(dst)),
+               "r"(src), "r"(bytes)
+               : "memory");
 }
 __device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_group_read0() {

@@ -152,6 +152,8 @@ abw_status abw_device_check(abw_stream stream) {
   if (e != cudaSuccess) return from_cuda(e, "abw_device_check");
   if (word & (abw::kErrWaitTimeout | abw::kErrSelfTest))
     return fail(ABW_ETIMEOUT, "a device-side bounded wait ran out (error word 0x%x)", word);
+  if (word & abw::kErrSmemAlign)
+    return fail(ABW_ECUDA, "a kernel's dynamic shared memory was not 1024-byte aligned; it did no work");
   return ABW_OK;
 }
 
@@ -297,7 +299,7 @@ abw_status attn_bwd_causal_noalloc(const void *q, const void *k, const void *v, 
   if (need > abw::kNoAllocScratchBytes)
     return fail(ABW_EWORKSPACE,
                 "attn_bwd_causal_noalloc: these sizes need %zu bytes of scratch, more than the built-in %zu "
-                "(B*T*Hq*D*4 must stay below about 32 MiB); use attn_bwd_causal with a workspace",
+                "(about B*Hq*T^2 bytes); use attn_bwd_causal with a workspace",
                 need, static_cast<size_t>(abw::kNoAllocScratchBytes));
   const size_t qn = static_cast<size_t>(B) * T * Hq * D, kn = static_cast<size_t>(B) * T * Hkv * D;
   Range in[] = {{"q", q, qn * 2},    {"k", k, kn * 2},
