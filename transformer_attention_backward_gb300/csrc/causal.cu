@@ -14,7 +14,7 @@
 //   2. kv   : tcgen05 kernel, one CTA per (128-key block, KV head, batch):
 //             dK and dV accumulate in TMEM over every query block at or after
 //             the key block; each bf16 dS tile leaves for the workspace
-//   3. dq   : tcgen05 kernel, one CTA per (128-query block, head, batch):
+//   3. dq   : persistent tcgen05 kernel over (128-query block, head, batch):
 //             dQ^T = K^T dS^T accumulates in TMEM over the key blocks at or
 //             before the query block; dq is written once, scaled and rotated
 //
@@ -29,27 +29,33 @@
 //   MMA1  S^T  = K Q^T          M=128 keys, N=64 queries, K=128 (TMEM)
 //   MMA2  dP^T = V dO^T         same shape
 //   softmax warps: P = exp2(S scale log2e - lse log2e) (causal mask),
-//          dS = P (dP - delta), both rounded to bf16 into swizzled smem
-//   MMA3  dV  += P^T dO          M=128 keys, N=128, K=64 queries
+//          dS = P (dP - delta), both rounded to bf16 and written back into
+//          TMEM over the S / dP values just read; dS also goes straight to
+//          the workspace as a 128B-swizzled tile
+//   MMA3  dV  += P^T dO          M=128 keys, N=128, K=64 queries, A in TMEM
 //   MMA4  dK  += dS^T Q          same shape
-//   dS store warp: the 16 KB dS^T tile -> workspace (bulk async copy)
-// Warp roles: 0 TMA producer, 1 MMA issuer, 2 TMEM owner, 3 dS store, 4-11
-// softmax (8 warps: four 32-key lane quarters x two 32-query halves), then
-// the dK (4-7: scale + RoPE) and dV (8-11) epilogues.  S/dP are
-// double-buffered in TMEM so the tensor core computes block n+1 while the
-// softmax warps work on block n.  TMEM (512 columns):
-//   [0,64) S0   [64,128) dP0   [128,192) S1   [192,256) dP1
+// Warp roles: 0 TMA producer, 1 MMA issuer, 2 TMEM owner, 4-11 softmax (two
+// groups of four warps, one per 32-key lane quarter, taking even / odd
+// iterations), then the dK (4-7: scale + RoPE) and dV (8-11) epilogues.  S/dP are double-buffered in TMEM
+// so the tensor core computes block n+1 while the softmax warps work on
+// block n.  TMEM (512 columns):
+//   [0,64) S0 / P0   [64,128) dP0 / dS0   [128,192) S1 / P1   [192,256) dP1 / dS1
 //   [256,384) dV   [384,512) dK
-// Q / dO / lse / delta arrive through a 4-deep TMA ring.
+// Keeping P and dS out of shared memory matters: the MMAs' operand reads
+// alone come close to the shared-memory bandwidth, and the Q / dO copies
+// share it.  Q / dO / lse / delta arrive through a 5-deep TMA ring.
 //
-// dq kernel (12 warps, one CTA per SM): per key block the K block (32 KB)
-// and the two dS^T tiles of the CTA's query blocks (2 x 16 KB, adjacent in
-// the workspace) arrive through a 3-deep ring; MMA dQ^T += K^T dS^T with
-// M=128 (head dim), N=128 queries, K=128 keys.  Epilogue warps 4-11 read
-// dQ^T from TMEM (lane = head-dim index), pair lanes d and d^1 for RoPE and
-// store dq rows.
+// dq kernel (persistent, 12 warps, one CTA per SM): for each work item (128
+// queries of one head) and each key block at or before it, the K block
+// (32 KB) and the item's two dS^T tiles (2 x 16 KB, adjacent in the
+// workspace) arrive through a 3-deep ring that runs on across items; MMA
+// dQ^T += K^T dS^T with M=128 (head dim), N=128 queries, K=128 keys into one
+// of two TMEM accumulators.  Epilogue warps 4-11 read dQ^T (lane = head-dim
+// index), free the accumulator, pair lanes d and d^1 for RoPE and store dq
+// rows while the next item accumulates.
 #include <math.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "abw_host.h"
@@ -63,6 +69,7 @@ constexpr int kBK = 128;   // keys per kv CTA, queries per dq CTA
 constexpr int kBQ = 64;    // queries per block (one dS tile)
 constexpr int kThr = 384;  // 12 warps
 constexpr int kTileBytes = kBK * kBQ * 2;   // one bf16 dS^T tile
+constexpr int kHeadGroup = 8;               // kv kernel: (batch, KV head) pairs per scheduling group
 
 // kv kernel shared memory.  It fills all but a few hundred bytes of the 227
 // KB a CTA may have, so there is no slack to align the base by hand: the
@@ -70,20 +77,18 @@ constexpr int kTileBytes = kBK * kBQ * 2;   // one bf16 dS^T tile
 // (which the 128B-swizzled tiles need) and otherwise reports and returns.
 constexpr int kOffK = 0;                 // [2 D-halves][128 keys][128 B], 128B-swizzled
 constexpr int kOffV = 32768;
-constexpr int kStages = 4;               // Q / dO / lse / delta ring depth
+constexpr int kStages = 5;               // Q / dO / lse / delta ring depth
 constexpr int kOffStage = 65536;
 constexpr int kStageBytes = 32768;       // Q 16 KB, dO 16 KB
 constexpr int kStQ = 0, kStDO = 16384;
-constexpr int kOffP = kOffStage + kStages * kStageBytes;   // P^T [128 keys][64 queries] bf16, swizzled
-constexpr int kOffDS = kOffP + 16384;                 // dS^T [128 keys][64 queries] bf16, swizzled
-constexpr int kOffLD = kOffDS + 16384;                // per stage: lse2 [64] f32, delta [64] f32
+constexpr int kOffLD = kOffStage + kStages * kStageBytes;   // per stage: lse2 [64] f32, delta [64] f32
 constexpr int kOffBar = kOffLD + kStages * 512;
 constexpr int kSmem = kOffBar + 256;
 
 // kv kernel barrier slots (8 bytes each) after kOffBar.
 enum {
-  kBarKV = 0, kBarQFull = 1, kBarQEmpty = 5, kBarSFull = 9, kBarPFull = 11, kBarPEmpty = 12,
-  kBarTEmpty = 13, kBarDKV = 15, kBarFinal = 16, kNumBars = 17
+  kBarKV = 0, kBarQFull = 1, kBarQEmpty = kBarQFull + kStages, kBarSFull = kBarQEmpty + kStages,
+  kBarPFull = kBarSFull + 2, kBarDKV = kBarPFull + 2, kBarFinal = kBarDKV + 1, kNumBars = kBarFinal + 1
 };
 constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
 constexpr int kOffAbort = kOffTmemSlot + 4;
@@ -96,7 +101,7 @@ constexpr int kQStages = 3;
 constexpr int kQStageBytes = 65536;
 constexpr int kQOffDS = 32768;
 constexpr int kQOffBar = kQStages * kQStageBytes;
-enum { kQBarFull = 0, kQBarEmpty = 3, kQBarDone = 6, kQNumBars = 7 };
+enum { kQBarFull = 0, kQBarEmpty = 3, kQBarAccFull = 6, kQBarAccEmpty = 8, kQBarFinal = 10, kQNumBars = 11 };
 constexpr int kQOffTmemSlot = kQOffBar + kQNumBars * 8;
 constexpr int kQOffAbort = kQOffTmemSlot + 4;
 constexpr int kQSmem = kQOffBar + 256 + 1024;
@@ -133,52 +138,89 @@ CausalWs carve(void *ws, int B, int T, int Hq, int D) {
   return w;
 }
 
-// One warp per (b, t, h) row, t < Tp: delta and lse*log2(e) (padding rows:
-// 0 and +inf) and -- for b = h = 0, with RoPE -- the row of the table
-// scale * (cos, sin) of theta = (pos0 + t) * base^(-2i/D).  The angle is
+// delta and lse*log2(e) per (b, h, t < Tp) and, with RoPE, the table
+// scale * (cos, sin) of theta = (pos0 + t) * base^(-2i/D).  A half-warp takes
+// kPrepRows consecutive (b, t, h) rows of o and dout (16 bytes per lane and
+// tensor, all loads issued before the first reduction); padding entries
+// t in [T, Tp) get delta 0 and lse +inf, one per thread.  The RoPE angle is
 // formed and reduced modulo 2 pi in double and rounded to float only for
 // sincosf.
+constexpr int kPrepRows = 4;
+
+__device__ __forceinline__ float dot8_bf16(uint4 a, uint4 g) {
+  return bf16_lo(a.x) * bf16_lo(g.x) + bf16_hi(a.x) * bf16_hi(g.x) + bf16_lo(a.y) * bf16_lo(g.y) +
+         bf16_hi(a.y) * bf16_hi(g.y) + bf16_lo(a.z) * bf16_lo(g.z) + bf16_hi(a.z) * bf16_hi(g.z) +
+         bf16_lo(a.w) * bf16_lo(g.w) + bf16_hi(a.w) * bf16_hi(g.w);
+}
+
+struct PrepRope {
+  double inv_freq[kD / 2];   // base^(-2i/D), formed on the host in double
+  float scale;
+  int use_rope, pos0;
+};
+
 __global__ void __launch_bounds__(256) causal_prep_kernel(const __nv_bfloat16 *__restrict__ o,
                                                           const __nv_bfloat16 *__restrict__ dout,
                                                           const float *__restrict__ lse, float *__restrict__ delta,
                                                           float *__restrict__ lse2, float2 *__restrict__ rope, int B,
-                                                          int T, int Tp, int Hq, float scale, int use_rope, int pos0,
-                                                          double log2_base) {
-  const long long row = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
-  if (row >= static_cast<long long>(B) * Tp * Hq) return;
-  const int h = static_cast<int>(row % Hq);
-  const long long bt = row / Hq;
-  const int t = static_cast<int>(bt % Tp);
-  const int b = static_cast<int>(bt / Tp);
-  const size_t out = (static_cast<size_t>(b) * Hq + h) * Tp + t;
-  if (t >= T) {
-    if (lane == 0) {
-      delta[out] = 0.f;
-      lse2[out] = INFINITY;
-    }
-    return;
+                                                          int T, int Tp, int Hq, const __grid_constant__ PrepRope rp) {
+  const long long gid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int sub = threadIdx.x & 15;
+  // padding entries
+  const long long npad = static_cast<long long>(B) * Hq * (Tp - T);
+  if (gid < npad) {
+    const long long bh = gid / (Tp - T);
+    const int t = T + static_cast<int>(gid % (Tp - T));
+    delta[bh * Tp + t] = 0.f;
+    lse2[bh * Tp + t] = INFINITY;
   }
-  const size_t src = ((static_cast<size_t>(b) * T + t) * Hq + h) * kD;
-  const uint2 a = reinterpret_cast<const uint2 *>(o + src)[lane];
-  const uint2 g = reinterpret_cast<const uint2 *>(dout + src)[lane];
-  float s = bf16_lo(a.x) * bf16_lo(g.x) + bf16_hi(a.x) * bf16_hi(g.x) + bf16_lo(a.y) * bf16_lo(g.y) +
-            bf16_hi(a.y) * bf16_hi(g.y);
-  s = warp_sum(s);
-  if (lane == 0) {
-    delta[out] = s;
-    lse2[out] = lse[(static_cast<size_t>(b) * Hq + h) * T + t] * 1.4426950408889634f;
-  }
-  if (use_rope && b == 0 && h == 0) {
-    const double twopi = 6.283185307179586476925286766559;
+  const long long nrows = static_cast<long long>(B) * T * Hq;
+  const long long r0 = (gid >> 4) * kPrepRows;
+  uint4 a[kPrepRows], g[kPrepRows];
+  float l[kPrepRows];
 #pragma unroll
-    for (int k = 0; k < 2; ++k) {
-      const int i = lane + 32 * k;
-      const double a_ = static_cast<double>(pos0 + t) * exp2(-log2_base * (2.0 * i / kD));
-      const float th = static_cast<float>(a_ - twopi * rint(a_ / twopi));
-      float sn, c;
-      sincosf(th, &sn, &c);
-      rope[t * (kD / 2) + i] = make_float2(scale * c, scale * sn);
+  for (int k = 0; k < kPrepRows; ++k) {
+    const long long r = r0 + k;
+    if (r < nrows) {
+      a[k] = reinterpret_cast<const uint4 *>(o + r * kD)[sub];
+      g[k] = reinterpret_cast<const uint4 *>(dout + r * kD)[sub];
+      const int h = static_cast<int>(r % Hq);
+      const long long bt = r / Hq;
+      l[k] = lse[(static_cast<size_t>(bt / T) * Hq + h) * T + bt % T];
+    } else {
+      a[k] = make_uint4(0, 0, 0, 0);
+      g[k] = a[k];
+      l[k] = 0.f;
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < kPrepRows; ++k) {
+    float v = dot8_bf16(a[k], g[k]);
+#pragma unroll
+    for (int off = 8; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);   // within the half-warp
+    const long long r = r0 + k;
+    if (r < nrows) {
+      const int h = static_cast<int>(r % Hq);
+      const long long bt = r / Hq;
+      const int t = static_cast<int>(bt % T);
+      const int b = static_cast<int>(bt / T);
+      const size_t out = (static_cast<size_t>(b) * Hq + h) * Tp + t;
+      if (sub == 0) {
+        delta[out] = v;
+        lse2[out] = l[k] * 1.4426950408889634f;
+      }
+      if (rp.use_rope && b == 0 && h == 0) {
+        const double twopi = 6.283185307179586476925286766559, inv_twopi = 0.15915494309189533576888376337251;
+#pragma unroll
+        for (int k2 = 0; k2 < 4; ++k2) {
+          const int i = sub + 16 * k2;
+          const double ang = static_cast<double>(rp.pos0 + t) * rp.inv_freq[i];
+          const float th = static_cast<float>(fma(-twopi, rint(ang * inv_twopi), ang));
+          float sn, c;
+          sincosf(th, &sn, &c);
+          rope[t * (kD / 2) + i] = make_float2(rp.scale * c, rp.scale * sn);
+        }
+      }
     }
   }
 }
@@ -214,6 +256,7 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 __global__ void __launch_bounds__(kThr, 1)
     causal_kv_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmDO,
                         const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                        const __grid_constant__ CUtensorMap tmdK, const __grid_constant__ CUtensorMap tmdV,
                         const __grid_constant__ TcParams p) {
   extern __shared__ __align__(1024) unsigned char smem[];
   const uint32_t sb = smem_u32(smem);
@@ -223,11 +266,17 @@ __global__ void __launch_bounds__(kThr, 1)
     return;
   }
 
-  // work item: heavy (early) key blocks first across the whole grid
-  const int per_kb = p.Hkv * p.B;
-  const int kb = blockIdx.x / per_kb;
-  const int rem = blockIdx.x - kb * per_kb;
-  const int kvh = rem % p.Hkv, b = rem / p.Hkv;
+  // Work item.  The (batch, KV head) pairs go in groups of kHeadGroup; within
+  // a group the heavy (early) key blocks come first.  The CTAs that run at
+  // one time then cover few heads, whose Q and dO (every key block of a head
+  // re-reads them) stay in L2 between the key blocks.
+  const int nh = p.Hkv * p.B;
+  const int grp = blockIdx.x / (kHeadGroup * p.nkb);
+  const int gsz = min(kHeadGroup, nh - grp * kHeadGroup);
+  const int in_grp = blockIdx.x - grp * kHeadGroup * p.nkb;
+  const int kb = in_grp / gsz;
+  const int hb = grp * kHeadGroup + in_grp % gsz;   // b * Hkv + kvh
+  const int kvh = hb % p.Hkv, b = hb / p.Hkv;
   const int k0 = kb * kBK;
   const int qb0 = k0 / kBQ;
   const int nq = p.nqb - qb0;            // query blocks per head
@@ -249,12 +298,8 @@ __global__ void __launch_bounds__(kThr, 1)
       mbar_init(bar(kBarQFull + s), 1);
       mbar_init(bar(kBarQEmpty + s), 1);
     }
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(bar(kBarSFull + s), 1);
-      mbar_init(bar(kBarTEmpty + s), 256);   // the eight softmax warps have read S and dP
-    }
-    mbar_init(bar(kBarPFull), 256);
-    mbar_init(bar(kBarPEmpty), 2);           // MMA3/4 done + dS tile copied out
+    for (int s = 0; s < 2; ++s) mbar_init(bar(kBarSFull + s), 1);
+    for (int s = 0; s < 2; ++s) mbar_init(bar(kBarPFull + s), 128);   // a softmax group has put P and dS in TMEM
     mbar_init(bar(kBarDKV), 1);
     mbar_init(bar(kBarFinal), 1);
     *abort_flag = 0;
@@ -305,169 +350,176 @@ __global__ void __launch_bounds__(kThr, 1)
     }
   } else if (warp == 1) {
     // ============================ MMA issuer ==============================
-    if (lane == 0) {
+    // The whole warp runs this loop in step (so descriptors and addresses stay
+    // warp-uniform); one elected lane issues each MMA and commit.
+    auto wtw = [&](uint32_t br, uint32_t parity) -> bool { return __shfl_sync(0xffffffffu, wt(br, parity), 0); };
+    {
       constexpr uint32_t id_sdp = tc::idesc_bf16_f32(128, 64, 0, 0);    // S^T, dP^T
-      constexpr uint32_t id_kv = tc::idesc_bf16_f32(128, 128, 0, 1);    // dV, dK
-      bool ok = wt(bar(kBarKV), 0);
+      constexpr uint32_t id_kv = tc::idesc_bf16_f32(128, 128, 0, 1);    // dV, dK (A from TMEM)
+      // Descriptors are built once; moving by a byte offset inside shared
+      // memory adds offset / 16 to the address field (all offsets stay below
+      // 256 KB, so the 14-bit field never carries).
+      const uint64_t dK = tc::sdesc_sw128(sb + kOffK, 16, 1024), dV = tc::sdesc_sw128(sb + kOffV, 16, 1024);
+      const uint64_t dQk = tc::sdesc_sw128(sb + kOffStage + kStQ, 16, 1024);     // Q as K-major B of S^T
+      const uint64_t dOk = tc::sdesc_sw128(sb + kOffStage + kStDO, 16, 1024);    // dO as K-major B of dP^T
+      const uint64_t dQm = tc::sdesc_sw128(sb + kOffStage + kStQ, 8192, 1024);   // Q as MN-major B of dK
+      const uint64_t dOm = tc::sdesc_sw128(sb + kOffStage + kStDO, 8192, 1024);  // dO as MN-major B of dV
+      bool ok = wtw(bar(kBarKV), 0);
       tc::fence_after_sync();
+      // S/dP(n) go to TMEM buffer n & 1.  That buffer last held P/dS(n - 2),
+      // which MMA3/4(n - 2) read; those were issued before this (the loop
+      // below waits for P/dS(n - 2) and issues MMA3/4(n - 2) before it issues
+      // S/dP(n)), and tcgen05 MMAs of one thread run in issue order.
       auto issue_sdp = [&](int n) -> bool {
-        const int s = n & 1, cyc = n >> 1;                       // TMEM buffer
+        const int s = n & 1;                                      // TMEM buffer
         const int qs = n % kStages, qc = n / kStages;             // smem stage
-        if (!wt(bar(kBarQFull + qs), qc & 1)) return false;
-        if (!wt(bar(kBarTEmpty + s), (cyc & 1) ^ 1)) return false;
+        if (!wtw(bar(kBarQFull + qs), qc & 1)) return false;
         tc::fence_after_sync();
-        const uint32_t st = sb + kOffStage + qs * kStageBytes;
-        const uint32_t dS = tmem + (s ? kColS1 : kColS0), dP = tmem + (s ? kColDP1 : kColDP0);
+        const uint64_t so = static_cast<uint64_t>(qs * kStageBytes) >> 4;
+        const uint32_t tS = tmem + (s ? kColS1 : kColS0), tP = tmem + (s ? kColDP1 : kColDP0);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t ko = (kk >> 2) * 16384 + (kk & 3) * 32, qo = (kk >> 2) * 8192 + (kk & 3) * 32;
-          tc::mma_bf16(dS, tc::sdesc_sw128(sb + kOffK + ko, 16, 1024), tc::sdesc_sw128(st + kStQ + qo, 16, 1024),
-                       id_sdp, kk > 0);
+          const uint32_t ko = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4, qo = ((kk >> 2) * 8192 + (kk & 3) * 32) >> 4;
+          tc::mma_bf16_w(tS, dK + ko, dQk + so + qo, id_sdp, kk > 0);
         }
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t ko = (kk >> 2) * 16384 + (kk & 3) * 32, qo = (kk >> 2) * 8192 + (kk & 3) * 32;
-          tc::mma_bf16(dP, tc::sdesc_sw128(sb + kOffV + ko, 16, 1024), tc::sdesc_sw128(st + kStDO + qo, 16, 1024),
-                       id_sdp, kk > 0);
+          const uint32_t ko = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4, qo = ((kk >> 2) * 8192 + (kk & 3) * 32) >> 4;
+          tc::mma_bf16_w(tP, dV + ko, dOk + so + qo, id_sdp, kk > 0);
         }
-        tc::commit(bar(kBarSFull + s));
+        tc::commit_w(bar(kBarSFull + s));
         return true;
       };
       if (ok && N > 0) ok = issue_sdp(0);
       for (int n = 0; ok && n < N; ++n) {
         if (n + 1 < N && !issue_sdp(n + 1)) break;
-        if (!wt(bar(kBarPFull), n & 1)) break;
+        if (!wtw(bar(kBarPFull + (n & 1)), (n >> 1) & 1)) break;
         tc::fence_after_sync();
         const int qs = n % kStages;
-        const uint32_t st = sb + kOffStage + qs * kStageBytes;
+        const uint64_t so = static_cast<uint64_t>(qs * kStageBytes) >> 4;
+        // P^T / dS^T sit in TMEM: queries 32 h .. 32 h + 31 (h = 0, 1) in the
+        // 16 columns from 32 h of the S (P) and dP (dS) columns of the buffer
+        const uint32_t tP = tmem + ((n & 1) ? kColS1 : kColS0), tD = tmem + ((n & 1) ? kColDP1 : kColDP0);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)   // dV += P^T dO
-          tc::mma_bf16(tmem + kColDV, tc::sdesc_sw128(sb + kOffP + kk * 32, 16, 1024),
-                       tc::sdesc_sw128(st + kStDO + kk * 2048, 8192, 1024), id_kv, (n > 0 || kk > 0));
+          tc::mma_bf16_ts_w(tmem + kColDV, tP + (kk >> 1) * 32 + (kk & 1) * 8, dOm + so + ((kk * 2048) >> 4), id_kv,
+                          (n > 0 || kk > 0));
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)   // dK += dS^T Q
-          tc::mma_bf16(tmem + kColDK, tc::sdesc_sw128(sb + kOffDS + kk * 32, 16, 1024),
-                       tc::sdesc_sw128(st + kStQ + kk * 2048, 8192, 1024), id_kv, (n > 0 || kk > 0));
-        tc::commit(bar(kBarQEmpty + qs));
-        tc::commit(bar(kBarPEmpty));
+          tc::mma_bf16_ts_w(tmem + kColDK, tD + (kk >> 1) * 32 + (kk & 1) * 8, dQm + so + ((kk * 2048) >> 4), id_kv,
+                          (n > 0 || kk > 0));
+        tc::commit_w(bar(kBarQEmpty + qs));
       }
-      tc::commit(bar(kBarDKV));
-      tc::commit(bar(kBarFinal));
+      tc::commit_w(bar(kBarDKV));
+      tc::commit_w(bar(kBarFinal));
       mbar_wait_bounded(bar(kBarFinal), 0, 2000000000ull);   // every MMA has completed
-    }
-  } else if (warp == 3) {
-    // ============================ dS store ================================
-    if (lane == 0) {
-      for (int n = 0; n < N; ++n) {
-        if (!wt(bar(kBarPFull), n & 1)) break;
-        const int h = kvh * p.G + n / nq;
-        const int qb = qb0 + n % nq;
-        __nv_bfloat16 *head_tiles = p.ws.ds + (static_cast<size_t>(b) * p.Hq + h) * p.tph * (kTileBytes / 2);
-        bulk_store(head_tiles + tile_index(kb, qb, p.nqb) * (kTileBytes / 2), sb + kOffDS, kTileBytes);
-        bulk_commit_group();
-        bulk_wait_group_read0();   // the dS buffer may be rewritten
-        mbar_arrive(bar(kBarPEmpty));
-      }
-      bulk_wait_group0();          // the tiles are in global memory
     }
   } else if (warp >= 4) {
     // ============================ softmax warps ===========================
+    // Two groups of four warps take alternate iterations (group g: n = g,
+    // g + 2, ...; TMEM buffer g), so one group's TMEM / memory latencies
+    // overlap the other group's arithmetic.  Each warp covers a 32-key lane
+    // quarter and all 64 queries, in two halves of 32.
     const int qd = warp & 3;                            // TMEM lane quarter
-    const int ch = (warp - 4) >> 2;                     // 32-query half
+    const int ch = (warp - 4) >> 2;                     // group: iteration parity (then dK / dV epilogue)
     const int j = 32 * qd + lane;                       // key row in the block
     const int key = k0 + j;
     const uint32_t lanebase = static_cast<uint32_t>(32 * qd) << 16;
     const float sl2 = p.scale * 1.4426950408889634f;
-    for (int n = 0; n < N; ++n) {
-      const int s = n & 1, cyc = n >> 1;
+    for (int n = ch; n < N; n += 2) {
+      const int cyc = n >> 1;
       const int q0 = (qb0 + n % nq) * kBQ;
-      if (!wt(bar(kBarSFull + s), cyc & 1)) break;
+      if (!wt(bar(kBarSFull + ch), cyc & 1)) break;
       tc::fence_after_sync();
       const int qs = n % kStages;
-      const float *lse2 = reinterpret_cast<const float *>(smem + kOffLD + qs * 512) + 32 * ch;
-      const float *dl = reinterpret_cast<const float *>(smem + kOffLD + qs * 512 + 256) + 32 * ch;
-      float sv[32], pv[32];
-      tc::ld32x2_wait(tmem + lanebase + (s ? kColS1 : kColS0) + 32 * ch,
-                      tmem + lanebase + (s ? kColDP1 : kColDP0) + 32 * ch, sv, pv);
-      tc::fence_before_sync();
-      mbar_arrive(bar(kBarTEmpty + s));                 // S/dP buffer free for block n + 2
+      const int h = kvh * p.G + n / nq;
+      const int qb = qb0 + n % nq;
+      unsigned char *row = reinterpret_cast<unsigned char *>(
+          p.ws.ds + ((static_cast<size_t>(b) * p.Hq + h) * p.tph + tile_index(kb, qb, p.nqb)) * (kTileBytes / 2)) +
+          j * 128;
       // only the two query blocks that overlap the key block need the causal
       // mask; queries past T have lse = +inf, so their P is exactly 0
       const bool diag = q0 < k0 + kBK;
-      uint32_t pk[16], dk[16];
+#pragma unroll 1
+      for (int hf = 0; hf < 2; ++hf) {
+        const float *lse2 = reinterpret_cast<const float *>(smem + kOffLD + qs * 512) + 32 * hf;
+        const float *dl = reinterpret_cast<const float *>(smem + kOffLD + qs * 512 + 256) + 32 * hf;
+        float sv[32], pv[32];
+        const uint32_t tS = tmem + lanebase + (ch ? kColS1 : kColS0) + 32 * hf;
+        const uint32_t tD = tmem + lanebase + (ch ? kColDP1 : kColDP0) + 32 * hf;
+        tc::ld32x2_wait(tS, tD, sv, pv);
+        uint32_t pk[16], dk[16];
 #pragma unroll
-      for (int c = 0; c < 32; c += 4) {
-        const float4 l4 = *reinterpret_cast<const float4 *>(lse2 + c);
-        const float4 d4 = *reinterpret_cast<const float4 *>(dl + c);
-        float P0 = fast_exp2(fmaf(sv[c], sl2, -l4.x));
-        float P1 = fast_exp2(fmaf(sv[c + 1], sl2, -l4.y));
-        float P2 = fast_exp2(fmaf(sv[c + 2], sl2, -l4.z));
-        float P3 = fast_exp2(fmaf(sv[c + 3], sl2, -l4.w));
-        if (diag) {
-          const int q = q0 + 32 * ch + c;
-          P0 = key <= q ? P0 : 0.f;
-          P1 = key <= q + 1 ? P1 : 0.f;
-          P2 = key <= q + 2 ? P2 : 0.f;
-          P3 = key <= q + 3 ? P3 : 0.f;
+        for (int c = 0; c < 32; c += 4) {
+          const float4 l4 = *reinterpret_cast<const float4 *>(lse2 + c);
+          const float4 d4 = *reinterpret_cast<const float4 *>(dl + c);
+          float P0 = fast_exp2(fmaf(sv[c], sl2, -l4.x));
+          float P1 = fast_exp2(fmaf(sv[c + 1], sl2, -l4.y));
+          float P2 = fast_exp2(fmaf(sv[c + 2], sl2, -l4.z));
+          float P3 = fast_exp2(fmaf(sv[c + 3], sl2, -l4.w));
+          if (diag) {
+            const int q = q0 + 32 * hf + c;
+            P0 = key <= q ? P0 : 0.f;
+            P1 = key <= q + 1 ? P1 : 0.f;
+            P2 = key <= q + 2 ? P2 : 0.f;
+            P3 = key <= q + 3 ? P3 : 0.f;
+          }
+          const float dS0 = P0 * (pv[c] - d4.x), dS1 = P1 * (pv[c + 1] - d4.y);
+          const float dS2 = P2 * (pv[c + 2] - d4.z), dS3 = P3 * (pv[c + 3] - d4.w);
+          pk[c / 2] = pack_bf16x2(P0, P1);
+          pk[c / 2 + 1] = pack_bf16x2(P2, P3);
+          dk[c / 2] = pack_bf16x2(dS0, dS1);
+          dk[c / 2 + 1] = pack_bf16x2(dS2, dS3);
         }
-        const float dS0 = P0 * (pv[c] - d4.x), dS1 = P1 * (pv[c + 1] - d4.y);
-        const float dS2 = P2 * (pv[c + 2] - d4.z), dS3 = P3 * (pv[c + 3] - d4.w);
-        pk[c / 2] = pack_bf16x2(P0, P1);
-        pk[c / 2 + 1] = pack_bf16x2(P2, P3);
-        dk[c / 2] = pack_bf16x2(dS0, dS1);
-        dk[c / 2 + 1] = pack_bf16x2(dS2, dS3);
-      }
-      if (!wt(bar(kBarPEmpty), (n & 1) ^ 1)) break;
-      unsigned char *prow = smem + kOffP + j * 128;
-      unsigned char *drow = smem + kOffDS + j * 128;
+        // P^T and dS^T (bf16 pairs) over the first 16 of the 32 S / dP
+        // columns just read: the A operands of MMA3/4
+        tc::st16x2_wait(tS, pk, tD, dk);
+        // dS^T row j of tile (kb, qb) to the workspace, in the 128B-swizzled
+        // layout the dq kernel copies into shared memory unchanged
 #pragma unroll
-      for (int c4 = 0; c4 < 4; ++c4) {
-        const int o = ((4 * ch + c4) ^ (j & 7)) << 4;   // 128B swizzle of 16-byte chunk 4 ch + c4
-        *reinterpret_cast<uint4 *>(prow + o) = make_uint4(pk[4 * c4], pk[4 * c4 + 1], pk[4 * c4 + 2], pk[4 * c4 + 3]);
-        *reinterpret_cast<uint4 *>(drow + o) = make_uint4(dk[4 * c4], dk[4 * c4 + 1], dk[4 * c4 + 2], dk[4 * c4 + 3]);
+        for (int c4 = 0; c4 < 4; ++c4)
+          *reinterpret_cast<uint4 *>(row + (((4 * hf + c4) ^ (j & 7)) << 4)) =
+              make_uint4(dk[4 * c4], dk[4 * c4 + 1], dk[4 * c4 + 2], dk[4 * c4 + 3]);
+      }
+      tc::fence_before_sync();
+      mbar_arrive(bar(kBarPFull + ch));
+    }
+    // ---- dK (group 0: scale + RoPE backward) and dV (group 1) epilogues.
+    // Every MMA has completed once DKV fires, and the producer has nothing
+    // left to load, so the Q / dO stages are free: each group stages its
+    // 128 x 128 fp32 block there as four 128B-swizzled [128 rows][32] tiles
+    // and one lane stores them with TMA (rows past T are not written).
+    // (the group agrees on the outcome of the wait: its named barriers must
+    // be reached by all four warps or by none)
+    if (named_barrier_and(1 + ch, 128, wt(bar(kBarDKV), 0))) {
+      tc::fence_after_sync();
+      const uint32_t stage = sb + kOffStage + ch * 65536;
+      unsigned char *stage_p = smem + kOffStage + ch * 65536;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        float v[32];
+        tc::ld32_wait(tmem + lanebase + (ch ? kColDV : kColDK) + 32 * c, v);
+        float4 cs[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          cs[i] = (ch == 0 && p.rope && key < p.T)
+                      ? *reinterpret_cast<const float4 *>(p.ws.rope + key * (kD / 2) + 16 * c + 2 * i)
+                      : make_float4(ch == 0 ? p.scale : 1.f, 0.f, ch == 0 ? p.scale : 1.f, 0.f);
+        unsigned char *trow = stage_p + c * 16384 + j * 128;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float *x = v + 4 * i;   // pairs (4i, 4i+1), (4i+2, 4i+3); the table holds scale * (cos, sin)
+          *reinterpret_cast<float4 *>(trow + ((i ^ (j & 7)) << 4)) =
+              make_float4(x[0] * cs[i].x + x[1] * cs[i].y, -x[0] * cs[i].y + x[1] * cs[i].x,
+                          x[2] * cs[i].z + x[3] * cs[i].w, -x[2] * cs[i].w + x[3] * cs[i].z);
+        }
       }
       fence_proxy_async_smem();
-      tc::fence_before_sync();
-      mbar_arrive(bar(kBarPFull));
-    }
-    if (wt(bar(kBarDKV), 0)) {
-      tc::fence_after_sync();
-      if (ch == 0) {
-        // ---- dK epilogue: scale, RoPE backward, store
-        for (int c = 0; c < 4; ++c) {
-          float v[32];
-          tc::ld32_wait(tmem + lanebase + kColDK + 32 * c, v);
-          if (key < p.T) {
-            float *dst = p.dk + ((static_cast<size_t>(b) * p.T + key) * p.Hkv + kvh) * kD + 32 * c;
-            // scale * (cos, sin) of the chunk's 16 pairs; the table holds
-            // the scale already.  All loads come before the first store: a
-            // load after a store to possibly the same memory would wait for it.
-            float4 cs[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-              cs[i] = p.rope ? *reinterpret_cast<const float4 *>(p.ws.rope + key * (kD / 2) + 16 * c + 2 * i)
-                             : make_float4(p.scale, 0.f, p.scale, 0.f);
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              const float *x = v + 4 * i;
-              *reinterpret_cast<float4 *>(dst + 4 * i) =
-                  make_float4(x[0] * cs[i].x + x[1] * cs[i].y, -x[0] * cs[i].y + x[1] * cs[i].x,
-                              x[2] * cs[i].z + x[3] * cs[i].w, -x[2] * cs[i].w + x[3] * cs[i].z);
-            }
-          }
-        }
-      } else {
-        // ---- dV epilogue
-        for (int c = 0; c < 4; ++c) {
-          float v[32];
-          tc::ld32_wait(tmem + lanebase + kColDV + 32 * c, v);
-          if (key < p.T) {
-            float *dst = p.dv + ((static_cast<size_t>(b) * p.T + key) * p.Hkv + kvh) * kD + 32 * c;
-#pragma unroll
-            for (int i = 0; i < 32; i += 4)
-              *reinterpret_cast<float4 *>(dst + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
-          }
-        }
+      named_barrier(1 + ch, 128);
+      if (qd == 0 && lane == 0) {
+        for (int c = 0; c < 4; ++c) tma_store_4d(ch ? &tmdV : &tmdK, stage + c * 16384, 32 * c, kvh, k0, b);
+        bulk_commit_group();
+        bulk_wait_group0();
       }
     }
   }
@@ -486,14 +538,21 @@ __global__ void __launch_bounds__(kThr, 1)
   const uint32_t sb = smem_u32(smem);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
-  // work item: query block pair m (queries 128 m .. 128 m + 127), heavy first
+  // Persistent: work items are (query block pair m, head, batch), heaviest
+  // (largest m) first, dealt round-robin to the CTAs.  Item j of a CTA
+  // accumulates into TMEM buffer j & 1, so its epilogue overlaps the loads
+  // and products of item j + 1.
   const int per_m = p.Hq * p.B;
-  const int m = p.nkb - 1 - static_cast<int>(blockIdx.x / per_m);
-  const int rem = blockIdx.x % per_m;
-  const int h = rem % p.Hq, b = rem / p.Hq;
-  const int kvh = h / p.G;
-  const int nsteps = m + 1;              // key blocks 0 .. m
-  const __nv_bfloat16 *head_tiles = p.ws.ds + (static_cast<size_t>(b) * p.Hq + h) * p.tph * (kTileBytes / 2);
+  const int items = p.nkb * per_m;
+  struct Item { int m, h, b; };
+  auto item = [&](int it) -> Item {
+    Item r;
+    r.m = p.nkb - 1 - it / per_m;
+    const int rem = it % per_m;
+    r.h = rem % p.Hq;
+    r.b = rem / p.Hq;
+    return r;
+  };
 
   auto bar = [&](int i) -> uint32_t { return sb + kQOffBar + i * 8; };
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + kQOffAbort);
@@ -510,11 +569,15 @@ __global__ void __launch_bounds__(kThr, 1)
       mbar_init(bar(kQBarFull + s), 1);
       mbar_init(bar(kQBarEmpty + s), 1);
     }
-    mbar_init(bar(kQBarDone), 1);
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(bar(kQBarAccFull + a), 1);
+      mbar_init(bar(kQBarAccEmpty + a), 256);
+    }
+    mbar_init(bar(kQBarFinal), 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
-  if (warp == 2) tc::tmem_alloc(sb + kQOffTmemSlot, 128);
+  if (warp == 2) tc::tmem_alloc(sb + kQOffTmemSlot, 256);
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
@@ -524,41 +587,69 @@ __global__ void __launch_bounds__(kThr, 1)
     // ============================ producer ================================
     if (lane == 0) {
       prefetch_tensormap(&tmK);
-      int issued = 0;
-      for (int i = 0; i < nsteps; ++i) {
-        const int s = i % kQStages, cyc = i / kQStages;
-        if (!wt(bar(kQBarEmpty + s), (cyc & 1) ^ 1)) break;
-        const uint32_t st = sb + s * kQStageBytes;
-        const uint32_t fb = bar(kQBarFull + s);
-        mbar_arrive_expect_tx(fb, 2 * 16384 + 2 * kTileBytes);
-        for (int hx = 0; hx < 2; ++hx) tma_load_4d(st + hx * 16384, &tmK, hx * 64, kvh, i * kBK, b, fb);
-        // tiles (i, 2m) and (i, 2m + 1) are adjacent
-        bulk_load(st + kQOffDS, head_tiles + tile_index(i, 2 * m, p.nqb) * (kTileBytes / 2), 2 * kTileBytes, fb);
-        issued = i + 1;
+      const uint64_t keep = l2_evict_last(), stream = l2_evict_first();
+      int g = 0;   // steps issued so far (ring position)
+      bool ok = true;
+      for (int it = blockIdx.x; ok && it < items; it += gridDim.x) {
+        const Item w = item(it);
+        const int kvh = w.h / p.G;
+        const __nv_bfloat16 *tiles = p.ws.ds + (static_cast<size_t>(w.b) * p.Hq + w.h) * p.tph * (kTileBytes / 2);
+        for (int i = 0; i <= w.m; ++i, ++g) {
+          const int s = g % kQStages, cyc = g / kQStages;
+          if (!wt(bar(kQBarEmpty + s), (cyc & 1) ^ 1)) {
+            ok = false;
+            break;
+          }
+          const uint32_t st = sb + s * kQStageBytes;
+          const uint32_t fb = bar(kQBarFull + s);
+          mbar_arrive_expect_tx(fb, 2 * 16384 + 2 * kTileBytes);
+          for (int hx = 0; hx < 2; ++hx)
+            tma_load_4d_hint(st + hx * 16384, &tmK, hx * 64, kvh, i * kBK, w.b, fb, keep);
+          // tiles (i, 2m) and (i, 2m + 1) are adjacent; each is read once
+          bulk_load_hint(st + kQOffDS, tiles + tile_index(i, 2 * w.m, p.nqb) * (kTileBytes / 2), 2 * kTileBytes,
+                         fb, stream);
+        }
       }
-      if (*abort_flag) {
+      if (!ok) {
         // let copies already in flight land before the CTA can exit
-        for (int i = (issued > kQStages ? issued - kQStages : 0); i < issued; ++i)
+        for (int i = (g > kQStages ? g - kQStages : 0); i < g; ++i)
           mbar_wait_bounded(bar(kQBarFull + i % kQStages), (i / kQStages) & 1, 2000000000ull);
       }
     }
   } else if (warp == 1) {
     // ============================ MMA issuer ==============================
-    if (lane == 0) {
+    // whole warp in step, one elected lane issues
+    auto wtw = [&](uint32_t br, uint32_t parity) -> bool { return __shfl_sync(0xffffffffu, wt(br, parity), 0); };
+    {
       constexpr uint32_t id_dq = tc::idesc_bf16_f32(128, 128, 1, 1);    // dQ^T += K^T dS^T
-      for (int i = 0; i < nsteps; ++i) {
-        const int s = i % kQStages, cyc = i / kQStages;
-        if (!wt(bar(kQBarFull + s), cyc & 1)) break;
+      // built once; a byte offset inside shared memory adds offset / 16
+      const uint64_t dKt = tc::sdesc_sw128(sb, 16384, 1024);                  // K^T, MN-major A
+      const uint64_t dSt = tc::sdesc_sw128(sb + kQOffDS, kTileBytes, 1024);   // dS^T, MN-major B
+      int g = 0, j = 0;
+      bool ok = true;
+      for (int it = blockIdx.x; ok && it < items; it += gridDim.x, ++j) {
+        const Item w = item(it);
+        const int a = j & 1;
+        if (!wtw(bar(kQBarAccEmpty + a), ((j >> 1) & 1) ^ 1)) break;
         tc::fence_after_sync();
-        const uint32_t st = sb + s * kQStageBytes;
+        for (int i = 0; i <= w.m; ++i, ++g) {
+          const int s = g % kQStages, cyc = g / kQStages;
+          if (!wtw(bar(kQBarFull + s), cyc & 1)) {
+            ok = false;
+            break;
+          }
+          tc::fence_after_sync();
+          const uint64_t so = static_cast<uint64_t>(s * kQStageBytes) >> 4;
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          tc::mma_bf16(tmem, tc::sdesc_sw128(st + kk * 2048, 16384, 1024),
-                       tc::sdesc_sw128(st + kQOffDS + kk * 2048, kTileBytes, 1024), id_dq, (i > 0 || kk > 0));
-        tc::commit(bar(kQBarEmpty + s));
+          for (int kk = 0; kk < 8; ++kk)
+            tc::mma_bf16_w(tmem + a * 128, dKt + so + ((kk * 2048) >> 4), dSt + so + ((kk * 2048) >> 4), id_dq,
+                         (i > 0 || kk > 0));
+          tc::commit_w(bar(kQBarEmpty + s));
+        }
+        if (ok) tc::commit_w(bar(kQBarAccFull + a));
       }
-      tc::commit(bar(kQBarDone));
-      mbar_wait_bounded(bar(kQBarDone), 0, 2000000000ull);   // every MMA has completed
+      tc::commit_w(bar(kQBarFinal));
+      mbar_wait_bounded(bar(kQBarFinal), 0, 2000000000ull);   // every MMA has completed
     }
   } else if (warp >= 4) {
     // ============================ epilogue ================================
@@ -567,12 +658,20 @@ __global__ void __launch_bounds__(kThr, 1)
     const int d = 32 * qd + lane;
     const uint32_t lanebase = static_cast<uint32_t>(32 * qd) << 16;
     const bool odd = d & 1;
-    if (wt(bar(kQBarDone), 0)) {
+    const size_t qstride = static_cast<size_t>(p.Hq) * kD;
+    int j = 0;
+    for (int it = blockIdx.x; it < items; it += gridDim.x, ++j) {
+      const Item w = item(it);
+      const int a = j & 1;
+      if (!wt(bar(kQBarAccFull + a), (j >> 1) & 1)) break;
       tc::fence_after_sync();
+      float v[2][32];
+      tc::ld32x2_wait(tmem + lanebase + a * 128 + 64 * ch, tmem + lanebase + a * 128 + 64 * ch + 32, v[0], v[1]);
+      tc::fence_before_sync();
+      mbar_arrive(bar(kQBarAccEmpty + a));   // the accumulator may be reused
+#pragma unroll
       for (int cc = 0; cc < 2; ++cc) {
-        float v[32];
-        tc::ld32_wait(tmem + lanebase + 64 * ch + 32 * cc, v);
-        const int qbase = m * kBK + 64 * ch + 32 * cc;
+        const int qbase = w.m * kBK + 64 * ch + 32 * cc;
         // pair (2i, 2i+1) rotated by -theta; the table holds scale * (cos,
         // sin).  All 32 loads come before the first store: a load after a
         // store to possibly the same memory would wait for it.
@@ -583,12 +682,12 @@ __global__ void __launch_bounds__(kThr, 1)
           cs[c] = !p.rope ? make_float2(p.scale, 0.f)
                   : q < p.T ? p.ws.rope[q * (kD / 2) + (d >> 1)] : make_float2(0.f, 0.f);
         }
-        float *dst = p.dq + ((static_cast<size_t>(b) * p.T + qbase) * p.Hq + h) * kD + d;
-        const size_t qstride = static_cast<size_t>(p.Hq) * kD;
+        float *dst = p.dq + ((static_cast<size_t>(w.b) * p.T + qbase) * p.Hq + w.h) * kD + d;
 #pragma unroll
         for (int c = 0; c < 32; ++c) {
-          const float partner = __shfl_xor_sync(0xffffffffu, v[c], 1);
-          if (qbase + c < p.T) dst[c * qstride] = v[c] * cs[c].x + (odd ? -partner : partner) * cs[c].y;
+          const float x = v[cc][c];
+          const float partner = __shfl_xor_sync(0xffffffffu, x, 1);
+          if (qbase + c < p.T) dst[c * qstride] = x * cs[c].x + (odd ? -partner : partner) * cs[c].y;
         }
       }
     }
@@ -597,7 +696,7 @@ __global__ void __launch_bounds__(kThr, 1)
   __syncthreads();
   if (warp == 2) {
     tc::fence_after_sync();
-    tc::tmem_dealloc(tmem, 128);
+    tc::tmem_dealloc(tmem, 256);
   }
 }
 
@@ -607,6 +706,15 @@ bool make_map(CUtensorMap *m, const void *base, int H, int T, int B, uint32_t ro
   const uint32_t box[4] = {64, 1, rows, 1};
   return encode_tiled(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, base, dims, strides, box,
                       CU_TENSOR_MAP_SWIZZLE_128B, why);
+}
+
+// fp32 [B][T][H][128] tensor stored in [128 rows][32 floats] 128B-swizzled tiles.
+bool make_map_f32(CUtensorMap *m, void *base, int H, int T, int B, const char **why) {
+  const uint64_t dims[4] = {kD, static_cast<uint64_t>(H), static_cast<uint64_t>(T), static_cast<uint64_t>(B)};
+  const uint64_t strides[3] = {kD * 4, static_cast<uint64_t>(H) * kD * 4, static_cast<uint64_t>(T) * H * kD * 4};
+  const uint32_t box[4] = {32, 1, static_cast<uint32_t>(kBK), 1};
+  return encode_tiled(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B,
+                      why);
 }
 
 // Scratch for attn_bwd_causal_noalloc: a fixed device array the library
@@ -669,18 +777,26 @@ cudaError_t launch_attn_bwd_causal(const void *q, const void *k, const void *v, 
   }
   CausalWs cw = carve(ws, B, T, Hq, D);
   const int rope = rope_base > 0.0;
+  PrepRope rp;
+  for (int i = 0; i < kD / 2; ++i) rp.inv_freq[i] = rope ? pow(rope_base, -2.0 * i / kD) : 0.0;
+  rp.scale = scale;
+  rp.use_rope = rope;
+  rp.pos0 = pos0;
   {
-    const long long rows = static_cast<long long>(B) * Tp * Hq;
-    const long long blocks = (rows * 32 + 255) / 256;
+    const long long rows = static_cast<long long>(B) * T * Hq;
+    const long long threads = std::max((rows + kPrepRows - 1) / kPrepRows * 16,
+                                       static_cast<long long>(B) * Hq * (Tp - T));
+    const long long blocks = (threads + 255) / 256;
     causal_prep_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(
         static_cast<const __nv_bfloat16 *>(o), static_cast<const __nv_bfloat16 *>(dout), lse, cw.delta, cw.lse2,
-        cw.rope, B, T, Tp, Hq, scale, rope, pos0, rope ? log2(rope_base) : 0.0);
+        cw.rope, B, T, Tp, Hq, rp);
   }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  CUtensorMap tq, tdo, tk, tv;
+  CUtensorMap tq, tdo, tk, tv, tdk, tdv;
   if (!make_map(&tq, q, Hq, T, B, kBQ, why) || !make_map(&tdo, dout, Hq, T, B, kBQ, why) ||
-      !make_map(&tk, k, Hkv, T, B, kBK, why) || !make_map(&tv, v, Hkv, T, B, kBK, why))
+      !make_map(&tk, k, Hkv, T, B, kBK, why) || !make_map(&tv, v, Hkv, T, B, kBK, why) ||
+      !make_map_f32(&tdk, dk, Hkv, T, B, why) || !make_map_f32(&tdv, dv, Hkv, T, B, why))
     return cudaErrorInvalidValue;
   TcParams p;
   p.ws = cw;
@@ -696,12 +812,17 @@ cudaError_t launch_attn_bwd_causal(const void *q, const void *k, const void *v, 
   p.wait = w;
   e = cudaFuncSetAttribute(causal_kv_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
   if (e != cudaSuccess) return e;
-  causal_kv_tc_kernel<<<static_cast<unsigned>(kv_ctas), kThr, kSmem, st>>>(tq, tdo, tk, tv, p);
+  causal_kv_tc_kernel<<<static_cast<unsigned>(kv_ctas), kThr, kSmem, st>>>(tq, tdo, tk, tv, tdk, tdv, p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(causal_dq_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kQSmem);
   if (e != cudaSuccess) return e;
-  causal_dq_tc_kernel<<<static_cast<unsigned>(dq_ctas), kThr, kQSmem, st>>>(tk, p);
+  int dev = 0, sms = 0;
+  e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  const long long dq_grid = std::min<long long>(dq_ctas, sms);
+  causal_dq_tc_kernel<<<static_cast<unsigned>(dq_grid), kThr, kQSmem, st>>>(tk, p);
   return cudaGetLastError();
 }
 
