@@ -176,6 +176,28 @@ __global__ void __launch_bounds__(256) causal_prep_kernel(const __nv_bfloat16 *_
   }
   const long long nrows = static_cast<long long>(B) * T * Hq;
   const long long r0 = (gid >> 4) * kPrepRows;
+  // (b, t, h) of row r0, then stepped to the next rows with carries (one
+  // division per thread instead of several per row)
+  int hh = static_cast<int>(r0 % Hq), tt, bb;
+  {
+    const long long bt = r0 / Hq;
+    tt = static_cast<int>(bt % T);
+    bb = static_cast<int>(bt / T);
+  }
+  int rh[kPrepRows], rt[kPrepRows], rb[kPrepRows];
+#pragma unroll
+  for (int k = 0; k < kPrepRows; ++k) {
+    rh[k] = hh;
+    rt[k] = tt;
+    rb[k] = bb;
+    if (++hh == Hq) {
+      hh = 0;
+      if (++tt == T) {
+        tt = 0;
+        ++bb;
+      }
+    }
+  }
   uint4 a[kPrepRows], g[kPrepRows];
   float l[kPrepRows];
 #pragma unroll
@@ -184,9 +206,7 @@ __global__ void __launch_bounds__(256) causal_prep_kernel(const __nv_bfloat16 *_
     if (r < nrows) {
       a[k] = reinterpret_cast<const uint4 *>(o + r * kD)[sub];
       g[k] = reinterpret_cast<const uint4 *>(dout + r * kD)[sub];
-      const int h = static_cast<int>(r % Hq);
-      const long long bt = r / Hq;
-      l[k] = lse[(static_cast<size_t>(bt / T) * Hq + h) * T + bt % T];
+      l[k] = lse[(static_cast<size_t>(rb[k]) * Hq + rh[k]) * T + rt[k]];
     } else {
       a[k] = make_uint4(0, 0, 0, 0);
       g[k] = a[k];
@@ -198,12 +218,8 @@ __global__ void __launch_bounds__(256) causal_prep_kernel(const __nv_bfloat16 *_
     float v = dot8_bf16(a[k], g[k]);
 #pragma unroll
     for (int off = 8; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);   // within the half-warp
-    const long long r = r0 + k;
-    if (r < nrows) {
-      const int h = static_cast<int>(r % Hq);
-      const long long bt = r / Hq;
-      const int t = static_cast<int>(bt % T);
-      const int b = static_cast<int>(bt / T);
+    if (r0 + k < nrows) {
+      const int h = rh[k], t = rt[k], b = rb[k];
       const size_t out = (static_cast<size_t>(b) * Hq + h) * Tp + t;
       if (sub == 0) {
         delta[out] = v;
@@ -229,6 +245,7 @@ struct TcParams {
   CausalWs ws;
   float *dq, *dk, *dv;
   int B, T, Tp, Hq, Hkv, G, nkb, nqb;
+  int hsplit, gs;  // kv kernel: each KV head's G query heads go to hsplit CTAs, gs = G / hsplit each
   long long tph;   // dS^T tiles per head
   float scale;
   int rope;
@@ -266,21 +283,24 @@ __global__ void __launch_bounds__(kThr, 1)
     return;
   }
 
-  // Work item.  The (batch, KV head) pairs go in groups of kHeadGroup; within
-  // a group the heavy (early) key blocks come first.  The CTAs that run at
-  // one time then cover few heads, whose Q and dO (every key block of a head
-  // re-reads them) stay in L2 between the key blocks.
-  const int nh = p.Hkv * p.B;
+  // Work item: (key block, batch, KV head, head split).  The (batch, KV head,
+  // split) units go in groups of kHeadGroup; within a group the heavy (early)
+  // key blocks come first.  The CTAs that run at one time then cover few
+  // heads, whose Q and dO (every key block of a head re-reads them) stay in
+  // L2 between the key blocks.
+  const int nh = p.Hkv * p.B * p.hsplit;
   const int grp = blockIdx.x / (kHeadGroup * p.nkb);
   const int gsz = min(kHeadGroup, nh - grp * kHeadGroup);
   const int in_grp = blockIdx.x - grp * kHeadGroup * p.nkb;
   const int kb = in_grp / gsz;
-  const int hb = grp * kHeadGroup + in_grp % gsz;   // b * Hkv + kvh
-  const int kvh = hb % p.Hkv, b = hb / p.Hkv;
+  const int hb = grp * kHeadGroup + in_grp % gsz;   // (b * Hkv + kvh) * hsplit + split
+  const int split = hb % p.hsplit;
+  const int kvh = (hb / p.hsplit) % p.Hkv, b = hb / (p.hsplit * p.Hkv);
+  const int h_first = kvh * p.G + split * p.gs;     // query heads h_first .. h_first + gs - 1
   const int k0 = kb * kBK;
   const int qb0 = k0 / kBQ;
   const int nq = p.nqb - qb0;            // query blocks per head
-  const int N = p.G * nq;                // iterations of this CTA
+  const int N = p.gs * nq;               // iterations of this CTA
 
   auto bar = [&](int i) -> uint32_t { return sb + kOffBar + i * 8; };
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + kOffAbort);
@@ -327,7 +347,7 @@ __global__ void __launch_bounds__(kThr, 1)
       for (int n = 0; n < N; ++n) {
         const int s = n % kStages, cyc = n / kStages;
         if (!wt(bar(kBarQEmpty + s), (cyc & 1) ^ 1)) break;
-        const int h = kvh * p.G + n / nq;
+        const int h = h_first + n / nq;
         const int q0 = (qb0 + n % nq) * kBQ;
         const uint32_t st = sb + kOffStage + s * kStageBytes;
         const uint32_t fb = bar(kBarQFull + s);
@@ -432,7 +452,7 @@ __global__ void __launch_bounds__(kThr, 1)
       if (!wt(bar(kBarSFull + ch), cyc & 1)) break;
       tc::fence_after_sync();
       const int qs = n % kStages;
-      const int h = kvh * p.G + n / nq;
+      const int h = h_first + n / nq;
       const int qb = qb0 + n % nq;
       unsigned char *row = reinterpret_cast<unsigned char *>(
           p.ws.ds + ((static_cast<size_t>(b) * p.Hq + h) * p.tph + tile_index(kb, qb, p.nqb)) * (kTileBytes / 2)) +
@@ -517,7 +537,14 @@ __global__ void __launch_bounds__(kThr, 1)
       fence_proxy_async_smem();
       named_barrier(1 + ch, 128);
       if (qd == 0 && lane == 0) {
-        for (int c = 0; c < 4; ++c) tma_store_4d(ch ? &tmdV : &tmdK, stage + c * 16384, 32 * c, kvh, k0, b);
+        // with the head group split over CTAs, each adds its partial sums
+        // into the zeroed outputs
+        for (int c = 0; c < 4; ++c) {
+          if (p.hsplit > 1)
+            tma_reduce_add_4d(ch ? &tmdV : &tmdK, stage + c * 16384, 32 * c, kvh, k0, b);
+          else
+            tma_store_4d(ch ? &tmdV : &tmdK, stage + c * 16384, 32 * c, kvh, k0, b);
+        }
         bulk_commit_group();
         bulk_wait_group0();
       }
@@ -769,7 +796,16 @@ cudaError_t launch_attn_bwd_causal(const void *q, const void *k, const void *v, 
   }
   const int Tp = padded_T(T);
   const int nkb = Tp / kBK;
-  const long long kv_ctas = static_cast<long long>(nkb) * Hkv * B;
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  // Split each KV head's query heads over more CTAs while the grid would not
+  // fill the GPU (partial dK / dV are then added into zeroed outputs).
+  const int G = Hq / Hkv;
+  int hsplit = 1;
+  while (hsplit < G && G % (2 * hsplit) == 0 && static_cast<long long>(nkb) * Hkv * B * hsplit < sms) hsplit *= 2;
+  const long long kv_ctas = static_cast<long long>(nkb) * Hkv * B * hsplit;
   const long long dq_ctas = static_cast<long long>(nkb) * Hq * B;
   if (kv_ctas > 0x7fffffffLL || dq_ctas > 0x7fffffffLL) {
     *why = "grid too large";
@@ -791,8 +827,14 @@ cudaError_t launch_attn_bwd_causal(const void *q, const void *k, const void *v, 
         static_cast<const __nv_bfloat16 *>(o), static_cast<const __nv_bfloat16 *>(dout), lse, cw.delta, cw.lse2,
         cw.rope, B, T, Tp, Hq, rp);
   }
-  cudaError_t e = cudaGetLastError();
+  e = cudaGetLastError();
   if (e != cudaSuccess) return e;
+  if (hsplit > 1) {
+    const size_t kvn = static_cast<size_t>(B) * T * Hkv * kD * 4;
+    e = cudaMemsetAsync(dk, 0, kvn, st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(dv, 0, kvn, st);
+    if (e != cudaSuccess) return e;
+  }
   CUtensorMap tq, tdo, tk, tv, tdk, tdv;
   if (!make_map(&tq, q, Hq, T, B, kBQ, why) || !make_map(&tdo, dout, Hq, T, B, kBQ, why) ||
       !make_map(&tk, k, Hkv, T, B, kBK, why) || !make_map(&tv, v, Hkv, T, B, kBK, why) ||
@@ -807,6 +849,8 @@ cudaError_t launch_attn_bwd_causal(const void *q, const void *k, const void *v, 
   p.nkb = nkb;
   p.nqb = Tp / kBQ;
   p.tph = tiles_per_head(nkb);
+  p.hsplit = hsplit;
+  p.gs = G / hsplit;
   p.scale = scale;
   p.rope = rope;
   p.wait = w;
@@ -816,10 +860,6 @@ cudaError_t launch_attn_bwd_causal(const void *q, const void *k, const void *v, 
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(causal_dq_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kQSmem);
-  if (e != cudaSuccess) return e;
-  int dev = 0, sms = 0;
-  e = cudaGetDevice(&dev);
-  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
   const long long dq_grid = std::min<long long>(dq_ctas, sms);
   causal_dq_tc_kernel<<<static_cast<unsigned>(dq_grid), kThr, kQSmem, st>>>(tk, p);
