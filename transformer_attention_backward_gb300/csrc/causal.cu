@@ -36,7 +36,8 @@
 //   MMA4  dK  += dS^T Q          same shape
 // Warp roles: 0 TMA producer, 1 MMA issuer, 2 TMEM owner, 4-11 softmax (two
 // groups of four warps, one per 32-key lane quarter, taking even / odd
-// iterations), then the dK (4-7: scale + RoPE) and dV (8-11) epilogues.  S/dP are double-buffered in TMEM
+// iterations), then the dK (scale + RoPE) and dV epilogues, each group
+// taking half the columns of both.  S/dP are double-buffered in TMEM
 // so the tensor core computes block n+1 while the softmax warps work on
 // block n.  TMEM (512 columns):
 //   [0,64) S0 / P0   [64,128) dP0 / dS0   [128,192) S1 / P1   [192,256) dP1 / dS1
@@ -504,34 +505,42 @@ __global__ void __launch_bounds__(kThr, 1)
       tc::fence_before_sync();
       mbar_arrive(bar(kBarPFull + ch));
     }
-    // ---- dK (group 0: scale + RoPE backward) and dV (group 1) epilogues.
-    // Every MMA has completed once DKV fires, and the producer has nothing
-    // left to load, so the Q / dO stages are free: each group stages its
-    // 128 x 128 fp32 block there as four 128B-swizzled [128 rows][32] tiles
-    // and one lane stores them with TMA (rows past T are not written).
-    // (the group agrees on the outcome of the wait: its named barriers must
-    // be reached by all four warps or by none)
+    // ---- dK (scale + RoPE backward) and dV epilogues.  Group g takes the
+    // 32-column chunks 2g and 2g + 1 of both.  Every MMA has completed once
+    // DKV fires, and the producer has nothing left to load, so the Q / dO
+    // stages are free: dK and dV are staged there as 128B-swizzled [128 rows]
+    // [32] fp32 tiles and one lane per group stores its four with TMA (rows
+    // past T are not written).  The RoPE table entries are fetched before the
+    // wait.  The group agrees on the outcome of the wait: its named barriers
+    // must be reached by all four warps or by none.
+    float4 cs[2][8];
+#pragma unroll
+    for (int cc = 0; cc < 2; ++cc)
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        cs[cc][i] = (p.rope && key < p.T)
+                        ? *reinterpret_cast<const float4 *>(p.ws.rope + key * (kD / 2) + 16 * (2 * ch + cc) + 2 * i)
+                        : make_float4(p.scale, 0.f, p.scale, 0.f);
     if (named_barrier_and(1 + ch, 128, wt(bar(kBarDKV), 0))) {
       tc::fence_after_sync();
-      const uint32_t stage = sb + kOffStage + ch * 65536;
-      unsigned char *stage_p = smem + kOffStage + ch * 65536;
+      const uint32_t stage = sb + kOffStage;
+      unsigned char *stage_p = smem + kOffStage;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        float v[32];
-        tc::ld32_wait(tmem + lanebase + (ch ? kColDV : kColDK) + 32 * c, v);
-        float4 cs[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-          cs[i] = (ch == 0 && p.rope && key < p.T)
-                      ? *reinterpret_cast<const float4 *>(p.ws.rope + key * (kD / 2) + 16 * c + 2 * i)
-                      : make_float4(ch == 0 ? p.scale : 1.f, 0.f, ch == 0 ? p.scale : 1.f, 0.f);
-        unsigned char *trow = stage_p + c * 16384 + j * 128;
+      for (int cc = 0; cc < 2; ++cc) {
+        const int c = 2 * ch + cc;
+        float v[32], u[32];
+        tc::ld32x2_wait(tmem + lanebase + kColDK + 32 * c, tmem + lanebase + kColDV + 32 * c, v, u);
+        unsigned char *krow = stage_p + c * 16384 + j * 128;
+        unsigned char *vrow = stage_p + 65536 + c * 16384 + j * 128;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           const float *x = v + 4 * i;   // pairs (4i, 4i+1), (4i+2, 4i+3); the table holds scale * (cos, sin)
-          *reinterpret_cast<float4 *>(trow + ((i ^ (j & 7)) << 4)) =
-              make_float4(x[0] * cs[i].x + x[1] * cs[i].y, -x[0] * cs[i].y + x[1] * cs[i].x,
-                          x[2] * cs[i].z + x[3] * cs[i].w, -x[2] * cs[i].w + x[3] * cs[i].z);
+          const float4 t = cs[cc][i];
+          const int o = (i ^ (j & 7)) << 4;
+          *reinterpret_cast<float4 *>(krow + o) =
+              make_float4(x[0] * t.x + x[1] * t.y, -x[0] * t.y + x[1] * t.x, x[2] * t.z + x[3] * t.w,
+                          -x[2] * t.w + x[3] * t.z);
+          *reinterpret_cast<float4 *>(vrow + o) = make_float4(u[4 * i], u[4 * i + 1], u[4 * i + 2], u[4 * i + 3]);
         }
       }
       fence_proxy_async_smem();
@@ -539,14 +548,18 @@ __global__ void __launch_bounds__(kThr, 1)
       if (qd == 0 && lane == 0) {
         // with the head group split over CTAs, each adds its partial sums
         // into the zeroed outputs
-        for (int c = 0; c < 4; ++c) {
-          if (p.hsplit > 1)
-            tma_reduce_add_4d(ch ? &tmdV : &tmdK, stage + c * 16384, 32 * c, kvh, k0, b);
-          else
-            tma_store_4d(ch ? &tmdV : &tmdK, stage + c * 16384, 32 * c, kvh, k0, b);
+        for (int cc = 0; cc < 2; ++cc) {
+          const int c = 2 * ch + cc;
+          if (p.hsplit > 1) {
+            tma_reduce_add_4d(&tmdK, stage + c * 16384, 32 * c, kvh, k0, b);
+            tma_reduce_add_4d(&tmdV, stage + 65536 + c * 16384, 32 * c, kvh, k0, b);
+          } else {
+            tma_store_4d(&tmdK, stage + c * 16384, 32 * c, kvh, k0, b);
+            tma_store_4d(&tmdV, stage + 65536 + c * 16384, 32 * c, kvh, k0, b);
+          }
         }
         bulk_commit_group();
-        bulk_wait_group0();
+        bulk_wait_group_read0();   // shared memory may be released; the writes complete on their own
       }
     }
   }
