@@ -264,6 +264,9 @@ __global__ void __launch_bounds__(kThreads, GMAX >= 8 ? 1 : (DT > 0 ? 3 : 2))
   __syncthreads();
   if (tid == 0)
     for (int t = 0; t < min(kStages, ntiles); ++t) issue(t);
+  // announce that this CTA runs (its shared memory may be written by its
+  // peers once they have waited on this phase of the cluster barrier)
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
 
   // ---- scale*q and dout for the dot products
   const size_t qrow0 = (static_cast<size_t>(b) * p.Hq + static_cast<size_t>(kvh) * G) * D;
@@ -553,15 +556,18 @@ __global__ void __launch_bounds__(kThreads, GMAX >= 8 ? 1 : (DT > 0 ? 3 : 2))
       xb[idx] = c;
     }
   }
+  // every CTA pushes its statistics into slot `rank` of each CTA's table, so
+  // after the cluster barrier the merge reads only local shared memory (every
+  // peer has started: the first cluster-barrier phase has completed)
+  __syncthreads();
+  asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+  if (tid < p.ncl * G) {
+    const int r = tid / G, h = tid - r * G;
+    cluster.map_shared_rank(rstat, r)[rank * GMAX + h] = make_float4(xm[h], xl[h], xc[h], 0.f);
+  }
   cluster.sync();
 
   // ======================= merge the softmax statistics ====================
-  if (tid < p.ncl * G) {
-    const int r = tid / G, h = tid - r * G;
-    rstat[r * GMAX + h] = make_float4(cluster.map_shared_rank(xm, r)[h], cluster.map_shared_rank(xl, r)[h],
-                                       cluster.map_shared_rank(xc, r)[h], 0.f);
-  }
-  __syncthreads();
   if (tid < G) {
     const int h = tid;
     float M = -INFINITY;
@@ -603,74 +609,8 @@ __global__ void __launch_bounds__(kThreads, GMAX >= 8 ? 1 : (DT > 0 ? 3 : 2))
   // stalls on the other.
   float *slots = reinterpret_cast<float *>(smem + L.kv + kStages * tile_bytes);   // [ncl][G*D] in rank 0
   const int half = D >> 1;
-  if (resident) {
-    const int dc = tid % D4, rsp = tid / D4;           // (row split, 4-dim chunk)
-    // row splits, capped so nrs * G * D floats fit the K tiles once consumed
-    const int nrs = min(kThreads / D4, 32 * ES / GMAX);
-    float2 aq[GMAX][2];
-#pragma unroll
-    for (int h = 0; h < GMAX; ++h) aq[h][0] = aq[h][1] = make_float2(0.f, 0.f);
-    if (rsp < nrs) {
-      for (int j = rsp; j < nkeys; j += nrs) {
-        const float4 kv = load4(elem(ktile(j / kTile), j % kTile, 4 * dc), static_cast<KV *>(nullptr));
-        const float2 k01 = make_float2(kv.x, kv.y), k23 = make_float2(kv.z, kv.w);
-        float dSh[GMAX];
-        ld_heads<GMAX>(pbuf + j * GMAX, dSh);
-#pragma unroll
-        for (int h = 0; h < GMAX; ++h) {
-          const float2 w = make_float2(dSh[h], dSh[h]);
-          aq[h][0] = __ffma2_rn(w, k01, aq[h][0]);
-          aq[h][1] = __ffma2_rn(w, k23, aq[h][1]);
-        }
-      }
-    }
-    __syncthreads();                                   // K tiles consumed
-    float *red = reinterpret_cast<float *>(smem + L.kv);
-    if (rsp < nrs) {
-#pragma unroll
-      for (int h = 0; h < GMAX; ++h)
-        if (h < G)
-          *reinterpret_cast<float4 *>(red + (rsp * G + h) * D + 4 * dc) =
-              make_float4(aq[h][0].x, aq[h][0].y, aq[h][1].x, aq[h][1].y);
-    }
-    __syncthreads();
-    float *dst0 = cluster.map_shared_rank(slots, 0) + rank * G * D;
-    for (int idx = tid; idx < G * D; idx += kThreads) {
-      float a = 0.f;
-      for (int r = 0; r < nrs; ++r) a += red[r * G * D + idx];
-      dst0[idx] = a;
-    }
-  } else if (rank == 0) {
-    for (int pr = tid; pr < G * half; pr += kThreads) {
-      const int h = pr / half, pi = pr - h * half;
-      const int idx = h * D + 2 * pi;
-      float a0 = 0.f, a1 = 0.f, b0 = 0.f, b1 = 0.f;
-#pragma unroll
-      for (int r = 0; r < kMaxCluster; ++r) {
-        if (r < p.ncl) {
-          const float w = rsc[r * kMaxG + h];
-          const float2 ra = *reinterpret_cast<const float2 *>(cluster.map_shared_rank(xa, r) + idx);
-          const float2 rb = *reinterpret_cast<const float2 *>(cluster.map_shared_rank(xb, r) + idx);
-          a0 = fmaf(w, ra.x, a0); a1 = fmaf(w, ra.y, a1);
-          b0 = fmaf(w, rb.x, b0); b1 = fmaf(w, rb.y, b1);
-        }
-      }
-      const float4 g = glob[h];
-      const float y0 = p.scale * (a0 - g.z * b0) * g.y;
-      const float y1 = p.scale * (a1 - g.z * b1) * g.y;
-      float z0 = y0, z1 = y1;
-      if (p.rope) {
-        const float c = p.rcos[pi], sn = p.rsin[pi];
-        z0 = y0 * c + y1 * sn;
-        z1 = -y0 * sn + y1 * c;
-      }
-      *reinterpret_cast<float2 *>(p.dq + qrow0 + idx) = make_float2(z0, z1);
-    }
-  }
-  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
-
-  // ======================= phase 2: dK / dV rows ===========================
-  {
+  // phase 2: dK / dV rows of this CTA's keys, over the warps [w0, w0 + nw)
+  auto store_rows = [&](int w0, int nw) {
     const int F4 = D >> 2;                                  // float4 per output row
     int olog = 0;
     while ((1 << olog) < F4 && olog < 5) ++olog;
@@ -695,7 +635,7 @@ __global__ void __launch_bounds__(kThreads, GMAX >= 8 ? 1 : (DT > 0 ? 3 : 2))
       float *dkp = p.dk + ((static_cast<size_t>(b) * p.S + key0) * p.Hkv + kvh) * D + 4 * f;
       float *dvp = p.dv + ((static_cast<size_t>(b) * p.S + key0) * p.Hkv + kvh) * D + 4 * f;
       const size_t rstride = static_cast<size_t>(p.Hkv) * D;
-      for (int j = warp * orows_w + ogrp; j < nkeys; j += kWarps * orows_w) {
+      for (int j = (warp - w0) * orows_w + ogrp; j < nkeys; j += nw * orows_w) {
         float2 k0 = make_float2(0.f, 0.f), k1 = k0, v0 = k0, v1 = k0;
         float Ph[GMAX], dSh[GMAX];
         ld_heads<GMAX>(sbuf + j * GMAX, Ph);
@@ -714,6 +654,89 @@ __global__ void __launch_bounds__(kThreads, GMAX >= 8 ? 1 : (DT > 0 ? 3 : 2))
         }
       }
     }
+  };
+  if (resident) {
+    // Resident K: warps 0-3 form sum_j dS'_hj K_j over this CTA's keys and
+    // push it into a slot of rank 0's (consumed) V tiles while warps 4-7
+    // write the dK / dV rows; the two use different units (shared memory and
+    // ALU against the store path) and overlap.  The cluster barrier that
+    // publishes the slots is split: every warp arrives once (warps 0-3 after
+    // their push, with release), and all wait after their own work.
+    if (warp < 4) {
+      const int dc = tid % D4, rsp = tid / D4;           // (row split, 4-dim chunk)
+      // row splits among the 128 threads, capped so nrs * G * D floats fit
+      // the K tiles once consumed
+      const int nrs = min(128 / D4, 32 * ES / GMAX);
+      float2 aq[GMAX][2];
+#pragma unroll
+      for (int h = 0; h < GMAX; ++h) aq[h][0] = aq[h][1] = make_float2(0.f, 0.f);
+      if (rsp < nrs) {
+        for (int j = rsp; j < nkeys; j += nrs) {
+          const float4 kv = load4(elem(ktile(j / kTile), j % kTile, 4 * dc), static_cast<KV *>(nullptr));
+          const float2 k01 = make_float2(kv.x, kv.y), k23 = make_float2(kv.z, kv.w);
+          float dSh[GMAX];
+          ld_heads<GMAX>(pbuf + j * GMAX, dSh);
+#pragma unroll
+          for (int h = 0; h < GMAX; ++h) {
+            const float2 w = make_float2(dSh[h], dSh[h]);
+            aq[h][0] = __ffma2_rn(w, k01, aq[h][0]);
+            aq[h][1] = __ffma2_rn(w, k23, aq[h][1]);
+          }
+        }
+      }
+      named_barrier(1, 128);                             // K tiles consumed
+      float *red = reinterpret_cast<float *>(smem + L.kv);
+      if (rsp < nrs) {
+#pragma unroll
+        for (int h = 0; h < GMAX; ++h)
+          if (h < G)
+            *reinterpret_cast<float4 *>(red + (rsp * G + h) * D + 4 * dc) =
+                make_float4(aq[h][0].x, aq[h][0].y, aq[h][1].x, aq[h][1].y);
+      }
+      named_barrier(1, 128);
+      float *dst0 = cluster.map_shared_rank(slots, 0) + rank * G * D;
+      for (int idx = tid; idx < G * D; idx += 128) {
+        float a = 0.f;
+        for (int r = 0; r < nrs; ++r) a += red[r * G * D + idx];
+        dst0[idx] = a;
+      }
+      asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+    } else {
+      asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+      store_rows(4, kWarps - 4);
+    }
+  } else {
+    // Streaming: rank 0 merges the running partials of every CTA, then all
+    // warps write their dK / dV rows.
+    if (rank == 0) {
+      for (int pr = tid; pr < G * half; pr += kThreads) {
+        const int h = pr / half, pi = pr - h * half;
+        const int idx = h * D + 2 * pi;
+        float a0 = 0.f, a1 = 0.f, b0 = 0.f, b1 = 0.f;
+#pragma unroll
+        for (int r = 0; r < kMaxCluster; ++r) {
+          if (r < p.ncl) {
+            const float w = rsc[r * kMaxG + h];
+            const float2 ra = *reinterpret_cast<const float2 *>(cluster.map_shared_rank(xa, r) + idx);
+            const float2 rb = *reinterpret_cast<const float2 *>(cluster.map_shared_rank(xb, r) + idx);
+            a0 = fmaf(w, ra.x, a0); a1 = fmaf(w, ra.y, a1);
+            b0 = fmaf(w, rb.x, b0); b1 = fmaf(w, rb.y, b1);
+          }
+        }
+        const float4 g = glob[h];
+        const float y0 = p.scale * (a0 - g.z * b0) * g.y;
+        const float y1 = p.scale * (a1 - g.z * b1) * g.y;
+        float z0 = y0, z1 = y1;
+        if (p.rope) {
+          const float c = p.rcos[pi], sn = p.rsin[pi];
+          z0 = y0 * c + y1 * sn;
+          z1 = -y0 * sn + y1 * c;
+        }
+        *reinterpret_cast<float2 *>(p.dq + qrow0 + idx) = make_float2(z0, z1);
+      }
+    }
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+    store_rows(0, kWarps);
   }
   asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 
