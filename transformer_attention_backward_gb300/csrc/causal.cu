@@ -461,47 +461,57 @@ __global__ void __launch_bounds__(kThr, 1)
       // only the two query blocks that overlap the key block need the causal
       // mask; queries past T have lse = +inf, so their P is exactly 0
       const bool diag = q0 < k0 + kBK;
-#pragma unroll 1
-      for (int hf = 0; hf < 2; ++hf) {
-        const float *lse2 = reinterpret_cast<const float *>(smem + kOffLD + qs * 512) + 32 * hf;
-        const float *dl = reinterpret_cast<const float *>(smem + kOffLD + qs * 512 + 256) + 32 * hf;
-        float sv[32], pv[32];
-        const uint32_t tS = tmem + lanebase + (ch ? kColS1 : kColS0) + 32 * hf;
-        const uint32_t tD = tmem + lanebase + (ch ? kColDP1 : kColDP0) + 32 * hf;
-        tc::ld32x2_wait(tS, tD, sv, pv);
-        uint32_t pk[16], dk[16];
+      const float *lse2 = reinterpret_cast<const float *>(smem + kOffLD + qs * 512);
+      const float *dl = reinterpret_cast<const float *>(smem + kOffLD + qs * 512 + 256);
+      const uint32_t tS = tmem + lanebase + (ch ? kColS1 : kColS0);
+      const uint32_t tD = tmem + lanebase + (ch ? kColDP1 : kColDP0);
+      // Four chunks of 16 queries, software-pipelined: the TMEM load of chunk
+      // c + 1 is in flight while chunk c is computed, and the P / dS stores to
+      // TMEM complete once, before the arrive.  P / dS of chunk c (16 bf16
+      // pairs = 8 columns each) go to columns 32 (c / 2) + 8 (c % 2) of the
+      // S / dP block: the A-operand layout of MMA3/4, and only over columns
+      // that chunks <= c have already read.
+      uint32_t buf[2][32];
+      tc::ld16x2_async(tS, tD, buf[0]);
 #pragma unroll
-        for (int c = 0; c < 32; c += 4) {
-          const float4 l4 = *reinterpret_cast<const float4 *>(lse2 + c);
-          const float4 d4 = *reinterpret_cast<const float4 *>(dl + c);
-          float P0 = fast_exp2(fmaf(sv[c], sl2, -l4.x));
-          float P1 = fast_exp2(fmaf(sv[c + 1], sl2, -l4.y));
-          float P2 = fast_exp2(fmaf(sv[c + 2], sl2, -l4.z));
-          float P3 = fast_exp2(fmaf(sv[c + 3], sl2, -l4.w));
+      for (int c = 0; c < 4; ++c) {
+        uint32_t (&cur)[32] = buf[c & 1];
+        tc::wait_ld16x2(cur);
+        if (c < 3) tc::ld16x2_async(tS + 16 * (c + 1), tD + 16 * (c + 1), buf[(c + 1) & 1]);
+        uint32_t pk[8], dk[8];
+#pragma unroll
+        for (int e = 0; e < 16; e += 4) {
+          const float4 l4 = *reinterpret_cast<const float4 *>(lse2 + 16 * c + e);
+          const float4 d4 = *reinterpret_cast<const float4 *>(dl + 16 * c + e);
+          float P0 = fast_exp2(fmaf(__uint_as_float(cur[e]), sl2, -l4.x));
+          float P1 = fast_exp2(fmaf(__uint_as_float(cur[e + 1]), sl2, -l4.y));
+          float P2 = fast_exp2(fmaf(__uint_as_float(cur[e + 2]), sl2, -l4.z));
+          float P3 = fast_exp2(fmaf(__uint_as_float(cur[e + 3]), sl2, -l4.w));
           if (diag) {
-            const int q = q0 + 32 * hf + c;
+            const int q = q0 + 16 * c + e;
             P0 = key <= q ? P0 : 0.f;
             P1 = key <= q + 1 ? P1 : 0.f;
             P2 = key <= q + 2 ? P2 : 0.f;
             P3 = key <= q + 3 ? P3 : 0.f;
           }
-          const float dS0 = P0 * (pv[c] - d4.x), dS1 = P1 * (pv[c + 1] - d4.y);
-          const float dS2 = P2 * (pv[c + 2] - d4.z), dS3 = P3 * (pv[c + 3] - d4.w);
-          pk[c / 2] = pack_bf16x2(P0, P1);
-          pk[c / 2 + 1] = pack_bf16x2(P2, P3);
-          dk[c / 2] = pack_bf16x2(dS0, dS1);
-          dk[c / 2 + 1] = pack_bf16x2(dS2, dS3);
+          const float dS0 = P0 * (__uint_as_float(cur[16 + e]) - d4.x);
+          const float dS1 = P1 * (__uint_as_float(cur[16 + e + 1]) - d4.y);
+          const float dS2 = P2 * (__uint_as_float(cur[16 + e + 2]) - d4.z);
+          const float dS3 = P3 * (__uint_as_float(cur[16 + e + 3]) - d4.w);
+          pk[e / 2] = pack_bf16x2(P0, P1);
+          pk[e / 2 + 1] = pack_bf16x2(P2, P3);
+          dk[e / 2] = pack_bf16x2(dS0, dS1);
+          dk[e / 2 + 1] = pack_bf16x2(dS2, dS3);
         }
-        // P^T and dS^T (bf16 pairs) over the first 16 of the 32 S / dP
-        // columns just read: the A operands of MMA3/4
-        tc::st16x2_wait(tS, pk, tD, dk);
-        // dS^T row j of tile (kb, qb) to the workspace, in the 128B-swizzled
-        // layout the dq kernel copies into shared memory unchanged
-#pragma unroll
-        for (int c4 = 0; c4 < 4; ++c4)
-          *reinterpret_cast<uint4 *>(row + (((4 * hf + c4) ^ (j & 7)) << 4)) =
-              make_uint4(dk[4 * c4], dk[4 * c4 + 1], dk[4 * c4 + 2], dk[4 * c4 + 3]);
+        const int pc = 32 * (c >> 1) + 8 * (c & 1);
+        tc::st8x2_async(tS + pc, pk, tD + pc, dk);
+        // dS^T row j, queries 16 c .. 16 c + 15 (16-byte units 2c, 2c + 1) of
+        // tile (kb, qb), in the 128B-swizzled layout the dq kernel copies
+        // into shared memory unchanged
+        *reinterpret_cast<uint4 *>(row + (((2 * c) ^ (j & 7)) << 4)) = make_uint4(dk[0], dk[1], dk[2], dk[3]);
+        *reinterpret_cast<uint4 *>(row + (((2 * c + 1) ^ (j & 7)) << 4)) = make_uint4(dk[4], dk[5], dk[6], dk[7]);
       }
+      tc::wait_st();
       tc::fence_before_sync();
       mbar_arrive(bar(kBarPFull + ch));
     }

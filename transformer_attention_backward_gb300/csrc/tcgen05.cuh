@@ -166,7 +166,46 @@ __device__ __forceinline__ void ld32x2_wait(uint32_t ta, uint32_t tb, float (&va
 }
 #undef ABW_TC_R32
 
+// Asynchronous form: two 16-column loads with no wait.  The destination
+// registers must not be read before wait_ld16x2 on the same arrays, which
+// names them as operands so that no use can be scheduled ahead of it.
+#define ABW_TC_R16(o) \
+  "=r"(r[o + 0]), "=r"(r[o + 1]), "=r"(r[o + 2]), "=r"(r[o + 3]), "=r"(r[o + 4]), "=r"(r[o + 5]), \
+  "=r"(r[o + 6]), "=r"(r[o + 7]), "=r"(r[o + 8]), "=r"(r[o + 9]), "=r"(r[o + 10]), "=r"(r[o + 11]), \
+  "=r"(r[o + 12]), "=r"(r[o + 13]), "=r"(r[o + 14]), "=r"(r[o + 15])
+__device__ __forceinline__ void ld16x2_async(uint32_t ta, uint32_t tb, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%32];\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%33];"
+      : ABW_TC_R16(0), ABW_TC_R16(16)
+      : "r"(ta), "r"(tb)
+      : "memory");
+}
+#undef ABW_TC_R16
+#define ABW_TC_RW16(o) \
+  "+r"(r[o + 0]), "+r"(r[o + 1]), "+r"(r[o + 2]), "+r"(r[o + 3]), "+r"(r[o + 4]), "+r"(r[o + 5]), \
+  "+r"(r[o + 6]), "+r"(r[o + 7]), "+r"(r[o + 8]), "+r"(r[o + 9]), "+r"(r[o + 10]), "+r"(r[o + 11]), \
+  "+r"(r[o + 12]), "+r"(r[o + 13]), "+r"(r[o + 14]), "+r"(r[o + 15])
+__device__ __forceinline__ void wait_ld16x2(uint32_t (&r)[32]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" : ABW_TC_RW16(0), ABW_TC_RW16(16) : : "memory");
+}
+#undef ABW_TC_RW16
+
 // ------------------------------------------------------------ TMEM stores
+// Asynchronous 8-column stores of two operands; complete them with wait_st().
+__device__ __forceinline__ void st8x2_async(uint32_t ta, const uint32_t (&ra)[8], uint32_t tb,
+                                            const uint32_t (&rb)[8]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%2, %3, %4, %5, %6, %7, %8, %9};\n\t"
+      "tcgen05.st.sync.aligned.32x32b.x8.b32 [%1], {%10, %11, %12, %13, %14, %15, %16, %17};" ::"r"(ta),
+      "r"(tb), "r"(ra[0]), "r"(ra[1]), "r"(ra[2]), "r"(ra[3]), "r"(ra[4]), "r"(ra[5]), "r"(ra[6]), "r"(ra[7]),
+      "r"(rb[0]), "r"(rb[1]), "r"(rb[2]), "r"(rb[3]), "r"(rb[4]), "r"(rb[5]), "r"(rb[6]), "r"(rb[7])
+      : "memory");
+}
+__device__ __forceinline__ void wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
 // 32 lanes x 32 bits, 16 consecutive columns from 16 registers per thread
 // (thread i writes row lane base + i), then wait until the stores are done.
 __device__ __forceinline__ void st16_wait(uint32_t taddr, const uint32_t (&r)[16]) {
