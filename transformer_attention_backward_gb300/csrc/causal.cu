@@ -312,6 +312,9 @@ __global__ void __launch_bounds__(kThr, 1)
     atomicOr(p.wait.err, kErrWaitTimeout);
     return false;
   };
+  // Whole-warp form: lane 0's outcome for every lane, so that a warp never
+  // splits in front of a warp-collective tcgen05 instruction.
+  auto wtw = [&](uint32_t br, uint32_t parity) -> bool { return __shfl_sync(0xffffffffu, wt(br, parity), 0); };
 
   if (tid == 0) {
     mbar_init(bar(kBarKV), 1);
@@ -373,7 +376,6 @@ __global__ void __launch_bounds__(kThr, 1)
     // ============================ MMA issuer ==============================
     // The whole warp runs this loop in step (so descriptors and addresses stay
     // warp-uniform); one elected lane issues each MMA and commit.
-    auto wtw = [&](uint32_t br, uint32_t parity) -> bool { return __shfl_sync(0xffffffffu, wt(br, parity), 0); };
     {
       constexpr uint32_t id_sdp = tc::idesc_bf16_f32(128, 64, 0, 0);    // S^T, dP^T
       constexpr uint32_t id_kv = tc::idesc_bf16_f32(128, 128, 0, 1);    // dV, dK (A from TMEM)
@@ -450,7 +452,7 @@ __global__ void __launch_bounds__(kThr, 1)
     for (int n = ch; n < N; n += 2) {
       const int cyc = n >> 1;
       const int q0 = (qb0 + n % nq) * kBQ;
-      if (!wt(bar(kBarSFull + ch), cyc & 1)) break;
+      if (!wtw(bar(kBarSFull + ch), cyc & 1)) break;
       tc::fence_after_sync();
       const int qs = n % kStages;
       const int h = h_first + n / nq;
@@ -531,7 +533,7 @@ __global__ void __launch_bounds__(kThr, 1)
         cs[cc][i] = (p.rope && key < p.T)
                         ? *reinterpret_cast<const float4 *>(p.ws.rope + key * (kD / 2) + 16 * (2 * ch + cc) + 2 * i)
                         : make_float4(p.scale, 0.f, p.scale, 0.f);
-    if (named_barrier_and(1 + ch, 128, wt(bar(kBarDKV), 0))) {
+    if (named_barrier_and(1 + ch, 128, wtw(bar(kBarDKV), 0))) {
       tc::fence_after_sync();
       const uint32_t stage = sb + kOffStage;
       unsigned char *stage_p = smem + kOffStage;
@@ -613,6 +615,9 @@ __global__ void __launch_bounds__(kThr, 1)
     atomicOr(p.wait.err, kErrWaitTimeout);
     return false;
   };
+  // Whole-warp form: lane 0's outcome for every lane, so that a warp never
+  // splits in front of a warp-collective tcgen05 instruction.
+  auto wtw = [&](uint32_t br, uint32_t parity) -> bool { return __shfl_sync(0xffffffffu, wt(br, parity), 0); };
 
   if (tid == 0) {
     for (int s = 0; s < kQStages; ++s) {
@@ -669,7 +674,6 @@ __global__ void __launch_bounds__(kThr, 1)
   } else if (warp == 1) {
     // ============================ MMA issuer ==============================
     // whole warp in step, one elected lane issues
-    auto wtw = [&](uint32_t br, uint32_t parity) -> bool { return __shfl_sync(0xffffffffu, wt(br, parity), 0); };
     {
       constexpr uint32_t id_dq = tc::idesc_bf16_f32(128, 128, 1, 1);    // dQ^T += K^T dS^T
       // built once; a byte offset inside shared memory adds offset / 16
@@ -713,7 +717,7 @@ __global__ void __launch_bounds__(kThr, 1)
     for (int it = blockIdx.x; it < items; it += gridDim.x, ++j) {
       const Item w = item(it);
       const int a = j & 1;
-      if (!wt(bar(kQBarAccFull + a), (j >> 1) & 1)) break;
+      if (!wtw(bar(kQBarAccFull + a), (j >> 1) & 1)) break;
       tc::fence_after_sync();
       float v[2][32];
       tc::ld32x2_wait(tmem + lanebase + a * 128 + 64 * ch, tmem + lanebase + a * 128 + 64 * ch + 32, v[0], v[1]);
