@@ -508,7 +508,10 @@ def run_native(args):
                   "ms_per_call": round(cms, 4), "flops_per_call": flops,
                   "roofline": {"bound": "tensor", "achieved": round(ctf / world, 3),
                                "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                               "frac": round(ctf / world / peaks["bf16_tflops"], 4), "traffic": None,
+                               "frac": round(ctf / world / peaks["bf16_tflops"], 4),
+                               "traffic": recorded_traffic("causal_kv_tc_kernel",
+                                                           ["causal.cu", "abw_device.cuh", "tcgen05.cuh"]),
+                               "traffic_kernel": "causal_kv_tc_kernel",
                                "peak_kind": kind + " (burst)", "scope": "whole call"},
                   "clocks": cclocks.summary(ch0, ch1)}
         del cin, o, lse, cq, ck, cv, ws
