@@ -141,11 +141,11 @@ CausalWs carve(void *ws, int B, int T, int Hq, int D) {
 
 // delta and lse*log2(e) per (b, h, t < Tp) and, with RoPE, the table
 // scale * (cos, sin) of theta = (pos0 + t) * base^(-2i/D).  A half-warp takes
-// kPrepRows consecutive (b, t, h) rows of o and dout (16 bytes per lane and
-// tensor, all loads issued before the first reduction); padding entries
-// t in [T, Tp) get delta 0 and lse +inf, one per thread.  The RoPE angle is
-// formed and reduced modulo 2 pi in double and rounded to float only for
-// sincosf.
+// kPrepRows rows of o and dout, consecutive in (b, h, t) order (16 bytes per
+// lane and tensor, all loads issued before the first reduction), and a share
+// of the table rows; padding entries t in [T, Tp) get delta 0 and lse +inf,
+// one per thread.  The RoPE angle is formed and reduced modulo 2 pi in
+// double and rounded to float only for sincosf.
 constexpr int kPrepRows = 4;
 
 __device__ __forceinline__ float dot8_bf16(uint4 a, uint4 g) {
@@ -175,15 +175,16 @@ __global__ void __launch_bounds__(256) causal_prep_kernel(const __nv_bfloat16 *_
     delta[bh * Tp + t] = 0.f;
     lse2[bh * Tp + t] = INFINITY;
   }
+  // Rows are taken in (b, h, t) order: a half-warp's rows are consecutive
+  // positions of one head, so the delta / lse accesses are contiguous; each
+  // row of o and dout is still one 256-byte segment.
   const long long nrows = static_cast<long long>(B) * T * Hq;
   const long long r0 = (gid >> 4) * kPrepRows;
-  // (b, t, h) of row r0, then stepped to the next rows with carries (one
-  // division per thread instead of several per row)
-  int hh = static_cast<int>(r0 % Hq), tt, bb;
+  int tt = static_cast<int>(r0 % T), hh, bb;
   {
-    const long long bt = r0 / Hq;
-    tt = static_cast<int>(bt % T);
-    bb = static_cast<int>(bt / T);
+    const long long bh = r0 / T;
+    hh = static_cast<int>(bh % Hq);
+    bb = static_cast<int>(bh / Hq);
   }
   int rh[kPrepRows], rt[kPrepRows], rb[kPrepRows];
 #pragma unroll
@@ -191,10 +192,10 @@ __global__ void __launch_bounds__(256) causal_prep_kernel(const __nv_bfloat16 *_
     rh[k] = hh;
     rt[k] = tt;
     rb[k] = bb;
-    if (++hh == Hq) {
-      hh = 0;
-      if (++tt == T) {
-        tt = 0;
+    if (++tt == T) {
+      tt = 0;
+      if (++hh == Hq) {
+        hh = 0;
         ++bb;
       }
     }
@@ -203,10 +204,10 @@ __global__ void __launch_bounds__(256) causal_prep_kernel(const __nv_bfloat16 *_
   float l[kPrepRows];
 #pragma unroll
   for (int k = 0; k < kPrepRows; ++k) {
-    const long long r = r0 + k;
-    if (r < nrows) {
-      a[k] = reinterpret_cast<const uint4 *>(o + r * kD)[sub];
-      g[k] = reinterpret_cast<const uint4 *>(dout + r * kD)[sub];
+    if (r0 + k < nrows) {
+      const size_t src = ((static_cast<size_t>(rb[k]) * T + rt[k]) * Hq + rh[k]) * kD;
+      a[k] = reinterpret_cast<const uint4 *>(o + src)[sub];
+      g[k] = reinterpret_cast<const uint4 *>(dout + src)[sub];
       l[k] = lse[(static_cast<size_t>(rb[k]) * Hq + rh[k]) * T + rt[k]];
     } else {
       a[k] = make_uint4(0, 0, 0, 0);
@@ -220,14 +221,21 @@ __global__ void __launch_bounds__(256) causal_prep_kernel(const __nv_bfloat16 *_
 #pragma unroll
     for (int off = 8; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);   // within the half-warp
     if (r0 + k < nrows) {
-      const int h = rh[k], t = rt[k], b = rb[k];
-      const size_t out = (static_cast<size_t>(b) * Hq + h) * Tp + t;
+      const size_t out = (static_cast<size_t>(rb[k]) * Hq + rh[k]) * Tp + rt[k];
       if (sub == 0) {
         delta[out] = v;
         lse2[out] = l[k] * 1.4426950408889634f;
       }
-      if (rp.use_rope && b == 0 && h == 0) {
-        const double twopi = 6.283185307179586476925286766559, inv_twopi = 0.15915494309189533576888376337251;
+    }
+  }
+  // RoPE table rows, spread evenly over the half-warps of the grid: half-warp
+  // hw of nhw takes rows ceil(hw T / nhw) .. ceil((hw + 1) T / nhw) - 1
+  if (rp.use_rope) {
+    const long long nhw = (nrows + kPrepRows - 1) / kPrepRows, hw = gid >> 4;
+    if (hw < nhw) {
+      const int t0 = static_cast<int>((hw * T + nhw - 1) / nhw), t1 = static_cast<int>(((hw + 1) * T + nhw - 1) / nhw);
+      const double twopi = 6.283185307179586476925286766559, inv_twopi = 0.15915494309189533576888376337251;
+      for (int t = t0; t < t1; ++t) {
 #pragma unroll
         for (int k2 = 0; k2 < 4; ++k2) {
           const int i = sub + 16 * k2;
