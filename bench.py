@@ -548,7 +548,7 @@ def run_native(args):
             "data": "synthetic",
             "config": {"workload": DECODE_WORKLOAD, "global_batch": 64 * world, "seq_len": 1024,
                        "parallelism": f"replicas{world}", "l2": "inputs larger than L2 (505 MB per step)",
-                       "compute": "fp32 arithmetic on bf16 K/V, fp32 q/dout/gradients"},
+                       "compute": "bf16 K/V; scores and dP on the tensor core with q/dout split into bf16 high+low parts, fp32 accumulation; fp32 elsewhere"},
             "roofline": roofline,
             "cpu_baseline": cpu,
             "e2e": {"value": round(e2e_value, 3), "unit": "GB/s", "h2d_bytes_per_step": h2d,

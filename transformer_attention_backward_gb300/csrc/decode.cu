@@ -37,6 +37,7 @@
 #include <type_traits>
 
 #include "abw_host.h"
+#include "tcgen05.cuh"
 
 namespace cg = cooperative_groups;
 
@@ -63,6 +64,7 @@ struct DecodeParams {
   int lpr_log2;   // generic dot phase: log2(lanes per K/V row), 16 bytes per lane
   int rs_log2;    // streaming: log2(row splits) of the dq partial sums
   int rowbytes;   // D * sizeof(kv)
+  int tc;         // bf16, D = 128, 128 keys per CTA: score / dP products on the tensor core
   float scale;
   int rope;
   float rcos[128];
@@ -74,7 +76,7 @@ struct DecodeParams {
 // Per-key scalars are key-major with a stride of gs (the kernel's
 // power-of-two head capacity), so one vector load fetches all heads of a key.
 struct Layout {
-  int kv, qs, sbuf, pbuf, etile, edp, xm, xl, xc, xa, xb, glob, rstat, alpha, runm, runl, runc, rsc, bars, total;
+  int kv, qs, sbuf, pbuf, etile, edp, xm, xl, xc, xa, xb, glob, rstat, alpha, runm, runl, runc, rsc, bars, tcs, total;
   __host__ __device__ static int up(int x, int a) { return (x + a - 1) / a * a; }
   // swz: the quarter-row layout of scale*q / dout is used; resident: the
   // streaming-only regions (running statistics, tile exponentials, dq
@@ -103,6 +105,7 @@ struct Layout {
     runc = o;  o += kMaxG * 4;
     rsc = o;   o += kMaxCluster * kMaxG * 4;  o = up(o, 16);
     bars = o;  o += kStages * 8;
+    tcs = o;   o += 16;                                     // tensor-core path: mbarrier, TMEM address
     total = up(o, 16);
   }
 };
@@ -219,6 +222,21 @@ __global__ void __launch_bounds__(kThreads, GMAX >= 8 ? 1 : (DT > 0 ? 3 : 2))
   float *dsm = qsm + GMAX * 4 * (D / 4 + 4);              // same for dout
   const uint32_t bar0 = smem_u32(smem + L.bars);
   const uint32_t kv0 = smem_u32(smem + L.kv);
+  // Tensor-core path (bf16, D = 128, a full 128-key chunk): K and V arrive as
+  // one 128-row block each, [2 halves of 64 dims][128 rows][128 B] swizzled,
+  // and s = K (scale q)^T, dP = V dout^T come from two M=128, N=16, K=128
+  // MMA chains whose B operands carry each head's vector split into bf16
+  // high and low parts (q = hi + lo to ~2^-17), so the fp32 results match
+  // fp32 dot products closely.  The B operands [16 rows][128 dims] sit in the
+  // q/dout staging area, which the score buffers overlap once the products
+  // are done.
+  constexpr bool TCP = (DT == 128);
+  const bool tc = TCP && p.tc != 0;
+  const uint32_t tcbar = smem_u32(smem + L.tcs);
+  auto kelem_tc = [&](int r, int d) -> const unsigned char * {
+    const int off = d * ES;
+    return smem + L.kv + (off >> 7) * 16384 + r * 128 + ((((off & 127) >> 4) ^ (r & 7)) << 4) + (off & 15);
+  };
   auto ktile = [&](int st) -> const unsigned char * { return smem + L.kv + st * tile_bytes; };
   auto vtile = [&](int st) -> const unsigned char * { return smem + L.kv + (kStages + st) * tile_bytes; };
   // address of element d of row r in a tile
@@ -254,6 +272,7 @@ __global__ void __launch_bounds__(kThreads, GMAX >= 8 ? 1 : (DT > 0 ? 3 : 2))
     prefetch_tensormap(&tmK);
     prefetch_tensormap(&tmV);
     for (int s = 0; s < kStages; ++s) mbar_init(bar0 + s * 8, 1);
+    mbar_init(tcbar, 1);
     fence_barrier_init();
   }
   if (tid < kMaxG) {
@@ -261,9 +280,23 @@ __global__ void __launch_bounds__(kThreads, GMAX >= 8 ? 1 : (DT > 0 ? 3 : 2))
     runl[tid] = 0.f;
     runc[tid] = 0.f;
   }
+  if (tc && warp == 0) tc::tmem_alloc(tcbar + 8, 32);
+  tc::fence_before_sync();
   __syncthreads();
-  if (tid == 0)
-    for (int t = 0; t < min(kStages, ntiles); ++t) issue(t);
+  tc::fence_after_sync();
+  const uint32_t tmem = tc ? *reinterpret_cast<volatile uint32_t *>(smem + L.tcs + 8) : 0u;
+  if (tid == 0) {
+    if (tc) {
+      mbar_arrive_expect_tx(bar0, 4 * 16384);
+#pragma unroll
+      for (int hx = 0; hx < 2; ++hx) {
+        tma_load_4d(kv0 + hx * 16384, &tmK, hx * 64, kvh, key0, b, bar0);
+        tma_load_4d(kv0 + 32768 + hx * 16384, &tmV, hx * 64, kvh, key0, b, bar0);
+      }
+    } else {
+      for (int t = 0; t < min(kStages, ntiles); ++t) issue(t);
+    }
+  }
   // announce that this CTA runs (its shared memory may be written by its
   // peers once they have waited on this phase of the cluster barrier)
   asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
@@ -278,7 +311,28 @@ __global__ void __launch_bounds__(kThreads, GMAX >= 8 ? 1 : (DT > 0 ? 3 : 2))
   const bool lane_on = sub * 16 < rowbytes;
   constexpr int QR = SWZ ? 1 : GMAX;                    // register copies (generic only)
   float qr[QR][EPL], dr[QR][EPL];
-  if constexpr (SWZ) {
+  if (tc) {
+    // B operands: row n < GMAX holds the bf16 high part of head n's vector,
+    // row GMAX + n its low part, rows past 2 GMAX (and heads >= G) zero
+    unsigned char *qb = smem + L.qs, *db = qb + 4096;
+    for (int idx = tid; idx < 16 * 128; idx += kThreads) {
+      const int n = idx >> 7, d = idx & 127;
+      const int h = n < GMAX ? n : n - GMAX;
+      float xq = 0.f, xd = 0.f;
+      if (n < 2 * GMAX && h < G) {
+        xq = p.q[qrow0 + static_cast<size_t>(h) * D + d] * p.scale;
+        xd = p.dout[qrow0 + static_cast<size_t>(h) * D + d];
+      }
+      const __nv_bfloat16 qh = __float2bfloat16_rn(xq), dh = __float2bfloat16_rn(xd);
+      const __nv_bfloat16 vq = n < GMAX ? qh : __float2bfloat16_rn(xq - __bfloat162float(qh));
+      const __nv_bfloat16 vd = n < GMAX ? dh : __float2bfloat16_rn(xd - __bfloat162float(dh));
+      const int off = (d >> 6) * 2048 + n * 128 + ((((d & 63) >> 3) ^ (n & 7)) << 4) + (d & 7) * 2;
+      *reinterpret_cast<__nv_bfloat16 *>(qb + off) = vq;
+      *reinterpret_cast<__nv_bfloat16 *>(db + off) = vd;
+    }
+    fence_proxy_async_smem();
+    __syncthreads();
+  } else if constexpr (SWZ) {
     constexpr int DPL = DT / 4;
     for (int idx = tid; idx < GMAX * DT; idx += kThreads) {
       const int h = idx / DT, d = idx - h * DT;
@@ -417,7 +471,45 @@ __global__ void __launch_bounds__(kThreads, GMAX >= 8 ? 1 : (DT > 0 ? 3 : 2))
   // ======================= phase 1 =========================================
   const int D4 = D >> 2;
   if (resident) {
-    if (SWZ && ntiles == 2) {
+    if (tc) {
+      if (warp == 0) {
+        mbar_wait_or_flag(bar0, 0, p.wait);
+        tc::fence_after_sync();
+        if (lane == 0) {
+          constexpr uint32_t id = tc::idesc_bf16_f32(128, 16, 0, 0);
+          const uint32_t qb = smem_u32(smem + L.qs), db = qb + 4096;
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t ao = (kk >> 2) * 16384 + (kk & 3) * 32, bo = (kk >> 2) * 2048 + (kk & 3) * 32;
+            tc::mma_bf16(tmem, tc::sdesc_sw128(kv0 + ao, 16, 1024), tc::sdesc_sw128(qb + bo, 16, 1024), id, kk > 0);
+          }
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t ao = (kk >> 2) * 16384 + (kk & 3) * 32, bo = (kk >> 2) * 2048 + (kk & 3) * 32;
+            tc::mma_bf16(tmem + 16, tc::sdesc_sw128(kv0 + 32768 + ao, 16, 1024), tc::sdesc_sw128(db + bo, 16, 1024),
+                         id, kk > 0);
+          }
+          tc::commit(tcbar);
+        }
+        __syncwarp();
+      }
+      mbar_wait_or_flag(tcbar, 0, p.wait);
+      tc::fence_after_sync();
+      if (warp < 4) {
+        // TMEM lane = key; columns: s hi | s lo | pad (16), dP hi | dP lo | pad (16)
+        float v[32];
+        tc::ld32_wait(tmem + (static_cast<uint32_t>(32 * warp) << 16), v);
+        const int key = 32 * warp + lane;
+        if (key < nkeys) {
+#pragma unroll
+          for (int h = 0; h < GMAX; ++h) {
+            sbuf[key * GMAX + h] = h < G ? v[h] + v[GMAX + h] : 0.f;
+            pbuf[key * GMAX + h] = h < G ? v[16 + h] + v[16 + GMAX + h] : 0.f;
+          }
+        }
+      }
+      tc::fence_before_sync();
+    } else if (SWZ && ntiles == 2) {
       mbar_wait_or_flag(bar0, 0, p.wait);
       mbar_wait_or_flag(bar0 + 8, 0, p.wait);
       dots_swz(std::integral_constant<int, 2>{}, 0, kTile, nkeys - kTile);
@@ -672,7 +764,8 @@ __global__ void __launch_bounds__(kThreads, GMAX >= 8 ? 1 : (DT > 0 ? 3 : 2))
       for (int h = 0; h < GMAX; ++h) aq[h][0] = aq[h][1] = make_float2(0.f, 0.f);
       if (rsp < nrs) {
         for (int j = rsp; j < nkeys; j += nrs) {
-          const float4 kv = load4(elem(ktile(j / kTile), j % kTile, 4 * dc), static_cast<KV *>(nullptr));
+          const float4 kv = load4(tc ? kelem_tc(j, 4 * dc) : elem(ktile(j / kTile), j % kTile, 4 * dc),
+                                  static_cast<KV *>(nullptr));
           const float2 k01 = make_float2(kv.x, kv.y), k23 = make_float2(kv.z, kv.w);
           float dSh[GMAX];
           ld_heads<GMAX>(pbuf + j * GMAX, dSh);
@@ -760,6 +853,13 @@ __global__ void __launch_bounds__(kThreads, GMAX >= 8 ? 1 : (DT > 0 ? 3 : 2))
       *reinterpret_cast<float2 *>(p.dq + qrow0 + idx) = make_float2(z0, z1);
     }
   }
+  if (tc) {
+    __syncthreads();   // every TMEM read has completed (waited on, fenced) before this
+    if (warp == 0) {
+      tc::fence_after_sync();
+      tc::tmem_dealloc(tmem, 32);
+    }
+  }
 }
 
 template <typename KV, int GMAX, int DT>
@@ -835,6 +935,7 @@ cudaError_t launch_attn_bwd_decode(const float *q, const void *k, const void *v,
   p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.S = S; p.D = D; p.G = G;
   p.chunk = chunk; p.ncl = ncl; p.resident = resident ? 1 : 0;
   p.lpr_log2 = lpr_log2; p.rs_log2 = rs_log2; p.rowbytes = rowbytes;
+  p.tc = (dt == 128 && chunk == 2 * kTile) ? 1 : 0;
   p.scale = scale;
   p.rope = rope_base > 0.0 && q_pos >= 0;
   for (int i = 0; i < 128; ++i) {
@@ -854,7 +955,8 @@ cudaError_t launch_attn_bwd_decode(const float *q, const void *k, const void *v,
                             static_cast<uint64_t>(B)};
   const uint64_t strides[3] = {static_cast<uint64_t>(rowbytes), static_cast<uint64_t>(Hkv) * rowbytes,
                                static_cast<uint64_t>(S) * Hkv * rowbytes};
-  const uint32_t box[4] = {static_cast<uint32_t>(dt ? 128 / es : D), 1, kTile, 1};
+  const uint32_t box[4] = {static_cast<uint32_t>(dt ? 128 / es : D), 1, static_cast<uint32_t>(p.tc ? 2 * kTile : kTile),
+                           1};
   const CUtensorMapDataType dtp = kv_bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
   const CUtensorMapSwizzle sw = dt ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE;
   if (!encode_tiled(&tk, dtp, 4, k, dims, strides, box, sw, why) ||
