@@ -280,7 +280,7 @@ __global__ void __launch_bounds__(kThreads, GMAX >= 8 ? 1 : (DT > 0 ? 3 : 2))
     runl[tid] = 0.f;
     runc[tid] = 0.f;
   }
-  if (tc && warp == 0) tc::tmem_alloc(tcbar + 8, 32);
+  if (tc && warp == 0) tc::tmem_alloc(tcbar + 8, 64);
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
@@ -754,7 +754,48 @@ __global__ void __launch_bounds__(kThreads, GMAX >= 8 ? 1 : (DT > 0 ? 3 : 2))
     // ALU against the store path) and overlap.  The cluster barrier that
     // publishes the slots is split: every warp arrives once (warps 0-3 after
     // their push, with release), and all wait after their own work.
-    if (warp < 4) {
+    if (tc && warp < 4) {
+      // dq^T [128 dims][16] = K^T dS on the tensor core: A = the resident K
+      // block read MN-major (M = head dims), B = [16 rows][128 keys] with
+      // row n < GMAX the bf16 high part of head n's scale * dS, row GMAX + n
+      // its low part; the result (TMEM lane = head dim) goes to rank 0.
+      unsigned char *bq = smem + L.qs;                   // free since the score / dP products completed
+      for (int idx = tid; idx < 16 * 128; idx += 128) {
+        const int n = idx >> 7, j = idx & 127;
+        const int h = n < GMAX ? n : n - GMAX;
+        const float x = (n < 2 * GMAX && j < nkeys) ? pbuf[j * GMAX + h] : 0.f;
+        const __nv_bfloat16 hi = __float2bfloat16_rn(x);
+        const __nv_bfloat16 val = n < GMAX ? hi : __float2bfloat16_rn(x - __bfloat162float(hi));
+        *reinterpret_cast<__nv_bfloat16 *>(bq + (j >> 6) * 2048 + n * 128 + ((((j & 63) >> 3) ^ (n & 7)) << 4) +
+                                           (j & 7) * 2) = val;
+      }
+      fence_proxy_async_smem();
+      named_barrier(1, 128);
+      if (warp == 0) {
+        tc::fence_after_sync();
+        if (lane == 0) {
+          constexpr uint32_t id = tc::idesc_bf16_f32(128, 16, 1, 0);
+          const uint32_t bqa = smem_u32(bq);
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            tc::mma_bf16(tmem + 32, tc::sdesc_sw128(kv0 + kk * 2048, 16384, 1024),
+                         tc::sdesc_sw128(bqa + (kk >> 2) * 2048 + (kk & 3) * 32, 16, 1024), id, kk > 0);
+          tc::commit(tcbar);
+        }
+        __syncwarp();
+      }
+      mbar_wait_or_flag(tcbar, 1, p.wait);
+      tc::fence_after_sync();
+      float v[32];
+      tc::ld32_wait(tmem + (static_cast<uint32_t>(32 * warp) << 16) + 32, v);
+      tc::fence_before_sync();
+      const int d = 32 * warp + lane;
+      float *dst0 = cluster.map_shared_rank(slots, 0) + rank * G * D;
+#pragma unroll
+      for (int h = 0; h < GMAX; ++h)
+        if (h < G) dst0[h * D + d] = v[h] + v[GMAX + h];
+      asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+    } else if (warp < 4) {
       const int dc = tid % D4, rsp = tid / D4;           // (row split, 4-dim chunk)
       // row splits among the 128 threads, capped so nrs * G * D floats fit
       // the K tiles once consumed
@@ -857,7 +898,7 @@ __global__ void __launch_bounds__(kThreads, GMAX >= 8 ? 1 : (DT > 0 ? 3 : 2))
     __syncthreads();   // every TMEM read has completed (waited on, fenced) before this
     if (warp == 0) {
       tc::fence_after_sync();
-      tc::tmem_dealloc(tmem, 32);
+      tc::tmem_dealloc(tmem, 64);
     }
   }
 }
