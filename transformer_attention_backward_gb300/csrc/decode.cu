@@ -274,6 +274,15 @@ __global__ void __launch_bounds__(kThreads, GMAX >= 8 ? 1 : (DT > 0 ? 3 : 2))
     for (int s = 0; s < kStages; ++s) mbar_init(bar0 + s * 8, 1);
     mbar_init(tcbar, 1);
     fence_barrier_init();
+    if (tc) {
+      // the K / V copies go out first; everything below overlaps them
+      mbar_arrive_expect_tx(bar0, 4 * 16384);
+#pragma unroll
+      for (int hx = 0; hx < 2; ++hx) {
+        tma_load_4d(kv0 + hx * 16384, &tmK, hx * 64, kvh, key0, b, bar0);
+        tma_load_4d(kv0 + 32768 + hx * 16384, &tmV, hx * 64, kvh, key0, b, bar0);
+      }
+    }
   }
   if (tid < kMaxG) {
     runm[tid] = -INFINITY;
@@ -285,18 +294,8 @@ __global__ void __launch_bounds__(kThreads, GMAX >= 8 ? 1 : (DT > 0 ? 3 : 2))
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = tc ? *reinterpret_cast<volatile uint32_t *>(smem + L.tcs + 8) : 0u;
-  if (tid == 0) {
-    if (tc) {
-      mbar_arrive_expect_tx(bar0, 4 * 16384);
-#pragma unroll
-      for (int hx = 0; hx < 2; ++hx) {
-        tma_load_4d(kv0 + hx * 16384, &tmK, hx * 64, kvh, key0, b, bar0);
-        tma_load_4d(kv0 + 32768 + hx * 16384, &tmV, hx * 64, kvh, key0, b, bar0);
-      }
-    } else {
-      for (int t = 0; t < min(kStages, ntiles); ++t) issue(t);
-    }
-  }
+  if (tid == 0 && !tc)
+    for (int t = 0; t < min(kStages, ntiles); ++t) issue(t);
   // announce that this CTA runs (its shared memory may be written by its
   // peers once they have waited on this phase of the cluster barrier)
   asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
