@@ -233,10 +233,7 @@ __global__ void __launch_bounds__(kThreads, GMAX >= 8 ? 1 : (DT > 0 ? 3 : 2))
   constexpr bool TCP = (DT == 128);
   const bool tc = TCP && p.tc != 0;
   const uint32_t tcbar = smem_u32(smem + L.tcs);
-  auto kelem_tc = [&](int r, int d) -> const unsigned char * {
-    const int off = d * ES;
-    return smem + L.kv + (off >> 7) * 16384 + r * 128 + ((((off & 127) >> 4) ^ (r & 7)) << 4) + (off & 15);
-  };
+
   auto ktile = [&](int st) -> const unsigned char * { return smem + L.kv + st * tile_bytes; };
   auto vtile = [&](int st) -> const unsigned char * { return smem + L.kv + (kStages + st) * tile_bytes; };
   // address of element d of row r in a tile
@@ -804,8 +801,7 @@ __global__ void __launch_bounds__(kThreads, GMAX >= 8 ? 1 : (DT > 0 ? 3 : 2))
       for (int h = 0; h < GMAX; ++h) aq[h][0] = aq[h][1] = make_float2(0.f, 0.f);
       if (rsp < nrs) {
         for (int j = rsp; j < nkeys; j += nrs) {
-          const float4 kv = load4(tc ? kelem_tc(j, 4 * dc) : elem(ktile(j / kTile), j % kTile, 4 * dc),
-                                  static_cast<KV *>(nullptr));
+          const float4 kv = load4(elem(ktile(j / kTile), j % kTile, 4 * dc), static_cast<KV *>(nullptr));
           const float2 k01 = make_float2(kv.x, kv.y), k23 = make_float2(kv.z, kv.w);
           float dSh[GMAX];
           ld_heads<GMAX>(pbuf + j * GMAX, dSh);
