@@ -142,8 +142,8 @@ CausalWs carve(void *ws, int B, int T, int Hq, int D) {
 // delta and lse*log2(e) per (b, h, t < Tp) and, with RoPE, the table
 // scale * (cos, sin) of theta = (pos0 + t) * base^(-2i/D).  A half-warp takes
 // kPrepRows rows of o and dout, consecutive in (b, h, t) order (16 bytes per
-// lane and tensor, all loads issued before the first reduction), and a share
-// of the table rows; padding entries t in [T, Tp) get delta 0 and lse +inf,
+// lane and tensor, all loads issued before the first reduction); table
+// entries are strided over the grid's threads; padding entries t in [T, Tp) get delta 0 and lse +inf,
 // one per thread.  The RoPE angle is formed and reduced modulo 2 pi in
 // double and rounded to float only for sincosf.
 constexpr int kPrepRows = 4;
@@ -228,24 +228,19 @@ __global__ void __launch_bounds__(256) causal_prep_kernel(const __nv_bfloat16 *_
       }
     }
   }
-  // RoPE table rows, spread evenly over the half-warps of the grid: half-warp
-  // hw of nhw takes rows ceil(hw T / nhw) .. ceil((hw + 1) T / nhw) - 1
+  // RoPE table: (t, i) entries strided over every thread of the grid (one
+  // each once B * Hq >= 16), so the double-precision angle reduction is
+  // spread over all SMs instead of a few half-warps
   if (rp.use_rope) {
-    const long long nhw = (nrows + kPrepRows - 1) / kPrepRows, hw = gid >> 4;
-    if (hw < nhw) {
-      const int t0 = static_cast<int>((hw * T + nhw - 1) / nhw), t1 = static_cast<int>(((hw + 1) * T + nhw - 1) / nhw);
-      const double twopi = 6.283185307179586476925286766559, inv_twopi = 0.15915494309189533576888376337251;
-      for (int t = t0; t < t1; ++t) {
-#pragma unroll
-        for (int k2 = 0; k2 < 4; ++k2) {
-          const int i = sub + 16 * k2;
-          const double ang = static_cast<double>(rp.pos0 + t) * rp.inv_freq[i];
-          const float th = static_cast<float>(fma(-twopi, rint(ang * inv_twopi), ang));
-          float sn, c;
-          sincosf(th, &sn, &c);
-          rope[t * (kD / 2) + i] = make_float2(rp.scale * c, rp.scale * sn);
-        }
-      }
+    const long long nthr = static_cast<long long>(gridDim.x) * blockDim.x;
+    const double twopi = 6.283185307179586476925286766559, inv_twopi = 0.15915494309189533576888376337251;
+    for (long long e = gid; e < static_cast<long long>(T) * (kD / 2); e += nthr) {
+      const int t = static_cast<int>(e / (kD / 2)), i = static_cast<int>(e % (kD / 2));
+      const double ang = static_cast<double>(rp.pos0 + t) * rp.inv_freq[i];
+      const float th = static_cast<float>(fma(-twopi, rint(ang * inv_twopi), ang));
+      float sn, c;
+      __sincosf(th, &sn, &c);   // |th| <= pi: absolute error ~1e-6, far below the bf16 inputs' rounding
+      rope[e] = make_float2(rp.scale * c, rp.scale * sn);
     }
   }
 }
