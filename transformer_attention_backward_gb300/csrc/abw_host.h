@@ -21,6 +21,12 @@ bool encode_tiled(CUtensorMap *map, CUtensorMapDataType dt, uint32_t rank, const
                   const uint64_t *dims, const uint64_t *strides_bytes, const uint32_t *box,
                   CUtensorMapSwizzle swizzle, const char **why);
 
+// Raises a kernel's dynamic shared-memory limit on the current device to at
+// least `bytes`, calling the runtime only when the limit has to grow: calls
+// after the first make no runtime call for it (which keeps them free of
+// anything but launches, e.g. under stream capture).
+cudaError_t ensure_dynamic_smem(const void *func, int bytes);
+
 // Launchers: validate nothing (api.cu has done it), enqueue, and return the
 // launch error.
 cudaError_t launch_softmax_bwd(const float *s, const float *dy, float *dx, int rows, int n,

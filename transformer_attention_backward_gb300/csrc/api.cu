@@ -81,6 +81,30 @@ size_t dt_size(abw_dtype d) { return d == ABW_BF16 ? 2 : 4; }
 
 namespace abw {
 
+cudaError_t ensure_dynamic_smem(const void *func, int bytes) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  struct Entry {
+    const void *func;
+    int dev, bytes;
+  };
+  static std::mutex mu;
+  static Entry seen[64];
+  static int nseen = 0;
+  std::lock_guard<std::mutex> lock(mu);
+  for (int i = 0; i < nseen; ++i) {
+    if (seen[i].func != func || seen[i].dev != dev) continue;
+    if (seen[i].bytes >= bytes) return cudaSuccess;
+    e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess) seen[i].bytes = bytes;
+    return e;
+  }
+  e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && nseen < 64) seen[nseen++] = Entry{func, dev, bytes};
+  return e;
+}
+
 WaitCtl wait_ctl() {
   WaitCtl w{nullptr, g_wait_limit_ns.load()};
   int dev = 0;

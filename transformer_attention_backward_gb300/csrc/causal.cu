@@ -884,12 +884,12 @@ cudaError_t launch_attn_bwd_causal(const void *q, const void *k, const void *v, 
   p.scale = scale;
   p.rope = rope;
   p.wait = w;
-  e = cudaFuncSetAttribute(causal_kv_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+  e = ensure_dynamic_smem(reinterpret_cast<const void *>(causal_kv_tc_kernel), kSmem);
   if (e != cudaSuccess) return e;
   causal_kv_tc_kernel<<<static_cast<unsigned>(kv_ctas), kThr, kSmem, st>>>(tq, tdo, tk, tv, tdk, tdv, p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(causal_dq_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kQSmem);
+  e = ensure_dynamic_smem(reinterpret_cast<const void *>(causal_dq_tc_kernel), kQSmem);
   if (e != cudaSuccess) return e;
   const long long dq_grid = std::min<long long>(dq_ctas, sms);
   causal_dq_tc_kernel<<<static_cast<unsigned>(dq_grid), kThr, kQSmem, st>>>(tk, p);

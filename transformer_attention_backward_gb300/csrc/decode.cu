@@ -902,7 +902,7 @@ template <typename KV, int GMAX, int DT>
 cudaError_t launch_typed(const CUtensorMap &tk, const CUtensorMap &tv, const DecodeParams &p, int smem,
                          cudaStream_t st) {
   auto kern = decode_bwd_kernel<KV, GMAX, DT>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void *>(kern), smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.ncl, p.Hkv, p.B);
