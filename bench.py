@@ -198,10 +198,37 @@ def cpu_cores():
 
 
 # ----------------------------------------------------------------------------
+# rank aggregation (one process per GPU; torchrun sets the environment)
+# ----------------------------------------------------------------------------
+def rank_env():
+    """(world, rank, local rank) from the launcher's environment; 1, 0, 0 alone."""
+    return (int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def rank_max(x, world, device):
+    """Largest of one float over all ranks: the slowest rank sets the time of a
+    step every rank ran.  Needs an initialised process group when world > 1."""
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(units_per_rank, world, ms):
+    """Whole-job rate: every rank processed `units_per_rank` in `ms` (the
+    max over ranks), so the job did world times that."""
+    return world * units_per_rank / (ms * 1e-3)
+
+
+# ----------------------------------------------------------------------------
 # reference arm
 # ----------------------------------------------------------------------------
 def run_reference(args):
-    rank = int(os.environ.get("RANK", "0"))
+    _, rank, _ = rank_env()
     if rank != 0:
         return 0
     cores = cpu_cores()
@@ -357,9 +384,7 @@ def run_native(args):
     import torch
     import torch.distributed as dist
 
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
+    world, rank, local = rank_env()
     if world > 1:
         dist.init_process_group("nccl", init_method="env://")
     torch.cuda.set_device(local)
@@ -377,11 +402,7 @@ def run_native(args):
         torch.cuda.synchronize()
 
     def max_over_ranks(x):
-        if world == 1:
-            return x
-        t = torch.tensor([x], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
+        return rank_max(x, world, dev)
 
     # ------------------------------------------------------------ decode step
     shape = W.DECODE_GQA
@@ -458,7 +479,7 @@ def run_native(args):
     total_ms = max_over_ranks(t_start.elapsed_time(t_end))
     ms_step = total_ms / args.steps
     kern_ms = statistics.mean(a.elapsed_time(b) for a, b in kern_ev)
-    value = world * step_bytes / (ms_step * 1e-3) / 1e9
+    value = job_rate(step_bytes, world, ms_step) / 1e9
     launches = 2 * args.steps
 
     # ------------------------------------------------------------ end to end (host buffers)
@@ -520,7 +541,7 @@ def run_native(args):
     barrier()
     abw.device_check(stream)
     e2e_ms = max_over_ranks(e0.elapsed_time(e1)) / args.steps
-    e2e_value = world * step_bytes / (e2e_ms * 1e-3) / 1e9
+    e2e_value = job_rate(step_bytes, world, e2e_ms) / 1e9
     del g, gbuf, obuf, dq, dk, dv, dx, hout
     torch.cuda.empty_cache()
 
