@@ -117,8 +117,13 @@ def test_rope_pair_vjp_and_roundtrip():
         assert abs(math.hypot(*y) - math.hypot(*x)) < 1e-13
         z = O.rope_backward_pair(dy[0], dy[1], theta)
         assert abs(math.hypot(*z) - math.hypot(*dy)) < 1e-13
-    # theta = 0 is the identity
+    # theta = 0 is the identity; theta = pi/2 maps (dy0, dy1) to (dy1, -dy0)
     assert O.rope_backward_pair(0.3, -0.7, 0.0) == (0.3, -0.7)
+    z0, z1 = O.rope_backward_pair(0.3, -0.7, math.pi / 2)
+    assert abs(z0 - (-0.7)) < 1e-15 and abs(z1 - (-0.3)) < 1e-15
+    # and the forward rotation the other way: (x0, x1) -> (-x1, x0)
+    y0, y1 = O.rope_forward_pair(0.3, -0.7, math.pi / 2)
+    assert abs(y0 - 0.7) < 1e-15 and abs(y1 - 0.3) < 1e-15
 
 
 @pytest.mark.parametrize("interleaved", [True, False])
@@ -184,6 +189,28 @@ def test_rmsnorm_scale_identity():
 # --------------------------------------------------------------------------
 # Scaled dot product and single-query attention
 # --------------------------------------------------------------------------
+@pytest.mark.parametrize("causal", [False, True])
+def test_contraction_adjoints(causal):
+    """Each product of the backward is the adjoint of its forward product:
+    <dO, P V'> = <dV, V'> for any V' (dV = P^T dO), and with dS = the softmax
+    backward of dP = dO V^T, <dS, scale Q' K^T> = <dQ, Q'> and
+    <dS, scale Q K'^T> = <dK, K'> for any Q', K'.  A transposed or swapped
+    operand in dQ, dK or dV breaks one of these."""
+    r = rng(41 + causal)
+    Tq, S, D, scale = 5, 7, 4, 0.4
+    Q, K, V, dO = r.normal(size=(Tq, D)), r.normal(size=(S, D)), r.normal(size=(S, D)), r.normal(size=(Tq, D))
+    off = S - Tq if causal else 0
+    _, _, P = O.attention_head_forward(Q, K, V, scale, causal, off)
+    dQ, dK, dV = O.attention_head_backward(Q, K, V, dO, scale, causal, off)
+    dS = O.softmax_backward(P, dO @ V.T)
+    Qp, Kp, Vp = r.normal(size=Q.shape), r.normal(size=K.shape), r.normal(size=V.shape)
+    assert abs(np.sum(dO * (P @ Vp)) - np.sum(dV * Vp)) < 1e-12
+    assert abs(np.sum(dS * (scale * Qp @ K.T)) - np.sum(dQ * Qp)) < 1e-12
+    assert abs(np.sum(dS * (scale * Q @ Kp.T)) - np.sum(dK * Kp)) < 1e-12
+    if causal:   # masked pairs carry no gradient
+        assert np.all(dS[~(np.arange(S)[None, :] <= np.arange(Tq)[:, None] + off)] == 0.0)
+
+
 def test_scaled_dot_vjp():
     r = rng(31)
     q, k = r.normal(size=6), r.normal(size=6)
