@@ -31,11 +31,11 @@
  *   - A non-OK status leaves the outputs unspecified; abw_last_error() returns
  *     a message for the last non-OK status of the calling thread.
  *   - Nothing crosses the ABI as a C++ exception, and nothing aborts.
- *   - Calls make no host-device synchronisation and, after the first call of
- *     an operation on a device (which resolves per-device state and raises
- *     the kernels' shared-memory limits), no runtime call but kernel launches
- *     (and, for GQA-split causal shapes, memsets) on `stream`.  They can
- *     therefore be captured into CUDA graphs; make one call of each operation
+ *   - Calls neither synchronise nor allocate: the work they enqueue on
+ *     `stream` is kernel launches (and, for GQA-split causal shapes,
+ *     memsets).  The first call of an operation on a device also resolves
+ *     per-device state and raises the kernels' shared-memory limits.  So the
+ *     calls can be captured into CUDA graphs; make one call of each operation
  *     on the device before capturing.
  *
  * Notation: B batch, Hq query heads, Hkv KV heads (Hq % Hkv == 0; query head
