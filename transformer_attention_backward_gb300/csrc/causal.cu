@@ -42,9 +42,9 @@
 // block n.  TMEM (512 columns):
 //   [0,64) S0 / P0   [64,128) dP0 / dS0   [128,192) S1 / P1   [192,256) dP1 / dS1
 //   [256,384) dV   [384,512) dK
-// Keeping P and dS out of shared memory matters: the MMAs' operand reads
-// alone come close to the shared-memory bandwidth, and the Q / dO copies
-// share it.  Q / dO / lse / delta arrive through a 5-deep TMA ring.
+// P and dS stay in TMEM (a variant staging dS in shared memory, copied out in
+// bulk and read there by the dK product, measured slower).  Q / dO / lse /
+// delta arrive through a 5-deep TMA ring.
 //
 // dq kernel (persistent, 12 warps, one CTA per SM): for each work item (128
 // queries of one head) and each key block at or before it, the K block
