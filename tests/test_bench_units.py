@@ -40,3 +40,13 @@ def test_causal_flops(B, T, H, D, flops):
 def test_job_rate_units():
     # 505,282,560 B in 0.1116 ms is 4.53 TB/s
     assert bench.job_rate(505_282_560, 1, 0.1116) / 1e9 == pytest.approx(4527.6, rel=1e-4)
+
+
+def test_recorded_traffic_is_keyed_to_the_kernel_sources():
+    # a record is used only while the hash of its kernel's source files matches
+    assert bench.recorded_traffic("decode_bwd_kernel", ["rows.cu"]) is None
+    assert bench.recorded_traffic("no_such_kernel", ["decode.cu"]) is None
+    for key, files in (("decode_bwd_kernel", ["decode.cu", "abw_device.cuh"]),
+                       ("causal_kv_tc_kernel", ["causal.cu", "abw_device.cuh", "tcgen05.cuh"])):
+        v = bench.recorded_traffic(key, files)
+        assert v is None or (isinstance(v, int) and v > 0)
