@@ -41,11 +41,11 @@ __all__ = [
     "softmax_backward_sums_to_zero",
     "rope_forward_pair", "rope_backward_pair", "rope_roundtrip_check",
     "rope_angles", "rope_forward", "rope_backward",
-    "rmsnorm_forward", "rmsnorm_backward",
+    "rmsnorm_forward", "rmsnorm_backward", "rmsnorm_backward_gamma",
     "dot_product", "scaled_dot_forward", "scaled_dot_backward_q",
     "scaled_dot_backward_k",
     "attention_forward_single", "attention_backward_single",
-    "attention_head_forward", "attention_head_backward",
+    "attention_head_forward", "attention_head_backward", "attention_head_backward_saved_p",
     "decode_backward", "causal_forward", "causal_backward",
     "chain_layer_backward",
     "numerical_grad", "check_gradient",
@@ -194,6 +194,19 @@ def rmsnorm_backward(x, gamma, dy, eps=1e-6):
     return (dy * gamma - x * c / (n * rms * rms)) / rms
 
 
+def rmsnorm_backward_gamma(x, dy, eps=1e-6):
+    """Gradient of the RMSNorm scale, summed over rows:
+    dgamma_i = sum over rows of dy_i x_i / rms.
+
+    The page states only dx; the forward y_i = gamma_i x_i / rms is linear in
+    gamma, so this is its plain derivative (the norm's other gradient)."""
+    x = _f64(x)
+    dy = _f64(dy)
+    n = x.shape[-1]
+    rms = np.sqrt(np.sum(x * x, axis=-1, keepdims=True) / n + eps)
+    return np.sum((dy * x / rms).reshape(-1, n), axis=0)
+
+
 # ==========================================================================
 # Scaled dot product  (VerifiedBackward, section "Scaled Dot-Product")
 # ==========================================================================
@@ -290,6 +303,18 @@ def attention_head_backward(Q, K, V, dO, scale, causal, q_offset=0):
     dK = scale * (dS.T @ Q)
     dV = P.T @ dO
     return dQ, dK, dV
+
+
+def attention_head_backward_saved_p(P, Q, K, V, dO, scale):
+    """dQ, dK, dV of one head from a saved probability matrix P [Tq][S]
+    (the attention weights the forward kept, masked entries 0) instead of
+    recomputing it -- the form of transformer.js backward(), which reads the
+    cached attention A: dV = A^T dctx, dA = dctx V^T,
+    dS = A (dA - sum_j A dA), dQ = scale dS K, dK = scale dS^T Q."""
+    P, Q, K, V, dO = _f64(P), _f64(Q), _f64(K), _f64(V), _f64(dO)
+    dP = dO @ V.T
+    dS = softmax_backward(P, dP)
+    return scale * (dS @ K), scale * (dS.T @ Q), P.T @ dO
 
 
 # ==========================================================================

@@ -186,6 +186,22 @@ def test_rmsnorm_scale_identity():
     assert abs(np.mean(y * y) - 1.0) < 1e-14
 
 
+@pytest.mark.parametrize("eps", [1e-6, 0.5])
+def test_rmsnorm_gamma_gradient(eps):
+    """<dy, y> is linear in gamma, so its central difference is exact up to
+    rounding: dgamma summed over the rows must match it tightly."""
+    r = rng(22)
+    x, dy = r.normal(size=(5, 12)), r.normal(size=(5, 12))
+    gamma = 1 + 0.1 * r.normal(size=12)
+    num = O.numerical_grad(lambda g: float(np.sum(dy * O.rmsnorm_forward(x, g, eps))), gamma)
+    got = O.rmsnorm_backward_gamma(x, dy, eps)
+    assert O.check_gradient(got, num)
+    np.testing.assert_allclose(got, num, atol=1e-9)
+    # one row at a time sums to the same
+    rows = sum(O.rmsnorm_backward_gamma(x[i:i + 1], dy[i:i + 1], eps) for i in range(5))
+    np.testing.assert_allclose(got, rows, atol=1e-13)
+
+
 # --------------------------------------------------------------------------
 # Scaled dot product and single-query attention
 # --------------------------------------------------------------------------
@@ -209,6 +225,20 @@ def test_contraction_adjoints(causal):
     assert abs(np.sum(dS * (scale * Q @ Kp.T)) - np.sum(dK * Kp)) < 1e-12
     if causal:   # masked pairs carry no gradient
         assert np.all(dS[~(np.arange(S)[None, :] <= np.arange(Tq)[:, None] + off)] == 0.0)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_saved_p_backward_matches_recompute(causal):
+    """Given the exact probabilities, the saved-P backward is the recompute
+    backward."""
+    r = rng(45 + causal)
+    Tq, S, D, scale = 4, 6, 3, 0.6
+    Q, K, V, dO = r.normal(size=(Tq, D)), r.normal(size=(S, D)), r.normal(size=(S, D)), r.normal(size=(Tq, D))
+    off = S - Tq if causal else 0
+    _, _, P = O.attention_head_forward(Q, K, V, scale, causal, off)
+    for a, b in zip(O.attention_head_backward_saved_p(P, Q, K, V, dO, scale),
+                    O.attention_head_backward(Q, K, V, dO, scale, causal, off)):
+        np.testing.assert_allclose(a, b, atol=1e-13)
 
 
 def test_scaled_dot_vjp():
