@@ -1,6 +1,10 @@
-"""Shared test helpers: the error metric and host<->device marshalling."""
+"""Shared test helpers: the error metrics and host<->device marshalling."""
 import numpy as np
 import torch
+
+# (test id, tensor name, max relative error, max per-element relative error)
+# of every comparison made through `checked`; printed at the end of the run.
+PARITY_LOG = []
 
 
 def max_rel_err(got, ref) -> float:
@@ -15,6 +19,32 @@ def max_rel_err(got, ref) -> float:
     if denom == 0.0:
         return float(np.max(np.abs(g - r)))
     return float(np.max(np.abs(g - r)) / denom)
+
+
+def max_elem_rel_err(got, ref) -> float:
+    """max over elements of |got - ref| / (|ref| + 1e-6 max |ref|): the
+    per-element figure, reported beside max_rel_err (not a bound: where a
+    gradient entry is a near-cancelling sum, its own magnitude is far below
+    the rounding of the terms it sums)."""
+    g = np.asarray(got, dtype=np.float64)
+    r = np.asarray(ref, dtype=np.float64)
+    assert g.shape == r.shape, (g.shape, r.shape)
+    if g.size == 0:
+        return 0.0
+    if not np.all(np.isfinite(g)):
+        return float("inf")
+    floor = 1e-6 * np.max(np.abs(r))
+    if floor == 0.0:
+        return float(np.max(np.abs(g - r)))
+    return float(np.max(np.abs(g - r) / (np.abs(r) + floor)))
+
+
+def checked(name, got, ref, tag="") -> float:
+    """max_rel_err of one output, with both error figures logged for the
+    end-of-run parity report."""
+    e = max_rel_err(got, ref)
+    PARITY_LOG.append((tag, name, e, max_elem_rel_err(got, ref)))
+    return e
 
 
 def to_np(t: torch.Tensor) -> np.ndarray:

@@ -9,7 +9,7 @@ import pytest
 import torch
 
 import oracle as O
-from tests.helpers import TOL_BF16, max_rel_err, to_np
+from tests.helpers import TOL_BF16, checked, max_rel_err, to_np
 from transformer_attention_backward_gb300 import saved_forward
 from transformer_attention_backward_gb300 import workloads as W
 
@@ -37,11 +37,12 @@ def compare_units(inp, shape, dq, dk, dv, units):
     rq, rk, rv = O.causal_backward(q, k, v, do, shape.scale, shape.rope_base, shape.pos0, kv_heads=units)
     G = shape.Hq // shape.Hkv
     errs = []
+    tag = f"causal B{shape.B} T{shape.T} Hq{shape.Hq}/{shape.Hkv} x{shape.qk_mult:g}"
     for b, j in units:
         hs = slice(j * G, (j + 1) * G)
-        errs.append(max_rel_err(to_np(dq[b, :, hs]), rq[b, :, hs]))
-        errs.append(max_rel_err(to_np(dk[b, :, j]), rk[b, :, j]))
-        errs.append(max_rel_err(to_np(dv[b, :, j]), rv[b, :, j]))
+        errs.append(checked("dq", to_np(dq[b, :, hs]), rq[b, :, hs], tag))
+        errs.append(checked("dk", to_np(dk[b, :, j]), rk[b, :, j], tag))
+        errs.append(checked("dv", to_np(dv[b, :, j]), rv[b, :, j], tag))
     return errs
 
 

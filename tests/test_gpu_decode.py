@@ -9,7 +9,7 @@ import pytest
 import torch
 
 import oracle as O
-from tests.helpers import TOL_F32, max_rel_err, to_np
+from tests.helpers import TOL_F32, checked, max_rel_err, to_np
 from transformer_attention_backward_gb300 import workloads as W
 
 pytestmark = pytest.mark.gpu
@@ -46,7 +46,8 @@ def run_and_compare(abw, shape, seed, units=None, tol=TOL_F32):
             got[2].append(to_np(dv[b:b + 1, :, j:j + 1]))
         got = [np.concatenate(x) for x in got]
         ref = [np.concatenate(x) for x in ref]
-    errs = [max_rel_err(a, r) for a, r in zip(got, ref)]
+    tag = f"decode B{shape.B} Hq{shape.Hq}/{shape.Hkv} S{shape.S} D{shape.D} pos{shape.q_pos}"
+    errs = [checked(n, a, r, tag) for n, a, r in zip(("dq", "dk", "dv"), got, ref)]
     assert max(errs) <= tol, errs
     return dq, dk, dv, inp
 
@@ -79,6 +80,25 @@ def test_decode_tiny_single_head(abw):
 ])
 def test_decode_shapes(abw, shape):
     run_and_compare(abw, shape, seed=shape.S + shape.D)
+
+
+# Shapes that take the tensor-core path: bf16 cache, D = 128 and 513 <= S <=
+# 1024, so each CTA of the cluster owns one 128-key chunk (the last one
+# possibly ragged).  The score and dP products then run as M=128 x N=16
+# tcgen05 chains whose B operands hold 2G rows (each head's vector split into
+# bf16 high and low parts), so every group size G = 1..8 is a different
+# operand layout.
+@pytest.mark.parametrize("shape", [
+    W.DecodeShape(B=4, Hq=5, Hkv=5, S=1024, D=128, rope_base=500000.0, q_pos=1023),     # G = 1
+    W.DecodeShape(B=4, Hq=10, Hkv=5, S=1024, D=128, rope_base=500000.0, q_pos=1023),    # G = 2
+    W.DecodeShape(B=2, Hq=16, Hkv=2, S=1024, D=128, rope_base=500000.0, q_pos=1023),    # G = 8, N = 16 full
+    W.DecodeShape(B=3, Hq=20, Hkv=5, S=1000, D=128, rope_base=500000.0, q_pos=999),     # ragged last chunk
+    W.DecodeShape(B=3, Hq=20, Hkv=5, S=1024, D=128, rope_base=500000.0, q_pos=-1),      # RoPE off
+    W.DecodeShape(B=2, Hq=12, Hkv=4, S=600, D=128, rope_base=10000.0, q_pos=17),        # G = 3, 5-CTA cluster
+    W.DecodeShape(B=1, Hq=7, Hkv=1, S=513, D=128, rope_base=0.0, q_pos=-1),             # G = 7, 1-key tail
+])
+def test_decode_tensor_core_shapes(abw, shape):
+    run_and_compare(abw, shape, seed=shape.S + shape.Hq)
 
 
 def test_decode_one_key_closed_form(abw):

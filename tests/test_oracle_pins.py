@@ -126,6 +126,26 @@ def test_rope_pair_vjp_and_roundtrip():
     assert abs(y0 - 0.7) < 1e-15 and abs(y1 - 0.3) < 1e-15
 
 
+def test_rope_roundtrip_check_rejects_broken_inverses(monkeypatch):
+    """ropeRoundtripCheck must return False when the backward is not the
+    inverse rotation: planted slips in a copy of the pair backward (wrong
+    sign, identity, a perturbation above the 1e-6 tolerance) each fail, and a
+    perturbation below it still passes."""
+    x0, x1, theta = 0.8, -1.3, 1.1
+    assert O.rope_roundtrip_check(x0, x1, theta)
+    good = O.rope_backward_pair
+    slips = {
+        "wrong sign": lambda a, b, t: O.rope_forward_pair(a, b, t),
+        "identity": lambda a, b, t: (a, b),
+        "perturbed 1e-5": lambda a, b, t: (good(a, b, t)[0] + 1e-5, good(a, b, t)[1]),
+    }
+    for name, slip in slips.items():
+        monkeypatch.setattr(O, "rope_backward_pair", slip)
+        assert not O.rope_roundtrip_check(x0, x1, theta), name
+    monkeypatch.setattr(O, "rope_backward_pair", lambda a, b, t: (good(a, b, t)[0] + 1e-8, good(a, b, t)[1]))
+    assert O.rope_roundtrip_check(x0, x1, theta)
+
+
 @pytest.mark.parametrize("interleaved", [True, False])
 def test_rope_tensor_matches_pairs(interleaved):
     r = rng(12)
