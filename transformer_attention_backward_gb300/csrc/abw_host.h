@@ -11,8 +11,14 @@
 
 namespace abw {
 
-// Error word + wait limit for the current device (lazily resolved once per
-// device).  `err` is null if the symbol address could not be obtained.
+// Unique id of the calling thread's current CUDA context (0 if none).
+// Per-device caches (symbol addresses, raised attribute limits) are keyed on
+// it as well as on the ordinal, so that they are resolved again in a context
+// created after cudaDeviceReset.
+unsigned long long context_id();
+
+// Error word + wait limit for the current device (resolved once per device
+// and context).  `err` is null if the symbol address could not be obtained.
 WaitCtl wait_ctl();
 
 // cuTensorMapEncodeTiled through the runtime's driver entry point (no link

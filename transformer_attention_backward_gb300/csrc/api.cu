@@ -23,6 +23,7 @@ __device__ unsigned int g_abw_err_word;
 constexpr int kMaxDevices = 64;
 std::mutex g_dev_mu;
 unsigned int *g_err_addr[kMaxDevices] = {};
+unsigned long long g_err_ctx[kMaxDevices] = {};   // context the cached address belongs to
 
 abw_status fail(abw_status st, const char *fmt, ...) {
   char buf[512];
@@ -81,13 +82,43 @@ size_t dt_size(abw_dtype d) { return d == ABW_BF16 ? 2 : 4; }
 
 namespace abw {
 
+unsigned long long context_id() {
+  // cuCtxGetCurrent / cuCtxGetId through the runtime's driver entry points
+  // (no link against libcuda).  The id is unique for the life of the
+  // process, so a context created after cudaDeviceReset never matches a
+  // cached entry of the one it replaced, even at the same handle address.
+  using GetCur = CUresult (*)(CUcontext *);
+  using GetId = CUresult (*)(CUcontext, unsigned long long *);
+  static GetCur get_cur = nullptr;
+  static GetId get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_cur = reinterpret_cast<GetCur>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<GetId>(p);
+  });
+  CUcontext c = nullptr;
+  unsigned long long id = 0;
+  if (!get_cur || !get_id || get_cur(&c) != CUDA_SUCCESS || c == nullptr || get_id(c, &id) != CUDA_SUCCESS)
+    return 0;
+  return id;
+}
+
 cudaError_t ensure_dynamic_smem(const void *func, int bytes) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
+  const unsigned long long ctx = context_id();
   struct Entry {
     const void *func;
     int dev, bytes;
+    unsigned long long ctx;
   };
   static std::mutex mu;
   static Entry seen[64];
@@ -95,13 +126,16 @@ cudaError_t ensure_dynamic_smem(const void *func, int bytes) {
   std::lock_guard<std::mutex> lock(mu);
   for (int i = 0; i < nseen; ++i) {
     if (seen[i].func != func || seen[i].dev != dev) continue;
-    if (seen[i].bytes >= bytes) return cudaSuccess;
+    if (ctx != 0 && seen[i].ctx == ctx && seen[i].bytes >= bytes) return cudaSuccess;
     e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-    if (e == cudaSuccess) seen[i].bytes = bytes;
+    if (e == cudaSuccess) {
+      seen[i].bytes = bytes;
+      seen[i].ctx = ctx;
+    }
     return e;
   }
   e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-  if (e == cudaSuccess && nseen < 64) seen[nseen++] = Entry{func, dev, bytes};
+  if (e == cudaSuccess && nseen < 64) seen[nseen++] = Entry{func, dev, bytes, ctx};
   return e;
 }
 
@@ -109,11 +143,13 @@ WaitCtl wait_ctl() {
   WaitCtl w{nullptr, g_wait_limit_ns.load()};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return w;
+  const unsigned long long ctx = context_id();
   std::lock_guard<std::mutex> lk(g_dev_mu);
-  if (g_err_addr[dev] == nullptr) {
+  if (g_err_addr[dev] == nullptr || ctx == 0 || g_err_ctx[dev] != ctx) {
     void *p = nullptr;
     if (cudaGetSymbolAddress(&p, g_abw_err_word) != cudaSuccess) return w;
     g_err_addr[dev] = static_cast<unsigned int *>(p);
+    g_err_ctx[dev] = ctx;
   }
   w.err = g_err_addr[dev];
   return w;

@@ -782,11 +782,13 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratch
 }  // namespace
 
 cudaError_t noalloc_scratch(void **ptr, const char **why) {
-  // Resolved once per device, with that device current.  A symbol's name in
-  // host code is only a host-side stand-in; the device address must come
-  // from the runtime.
+  // Resolved once per device and context, with that device current.  A
+  // symbol's name in host code is only a host-side stand-in; the device
+  // address must come from the runtime.  The context id in the key makes a
+  // context created after cudaDeviceReset resolve the address again.
   static std::mutex mu;
   static void *addr[64] = {};
+  static unsigned long long ctx_of[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -794,8 +796,9 @@ cudaError_t noalloc_scratch(void **ptr, const char **why) {
     *why = "device ordinal out of range";
     return cudaErrorInvalidDevice;
   }
+  const unsigned long long ctx = context_id();
   std::lock_guard<std::mutex> lk(mu);
-  if (addr[dev] == nullptr) {
+  if (addr[dev] == nullptr || ctx == 0 || ctx_of[dev] != ctx) {
     void *p = nullptr;
     e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
     if (e != cudaSuccess) {
@@ -803,6 +806,7 @@ cudaError_t noalloc_scratch(void **ptr, const char **why) {
       return e;
     }
     addr[dev] = p;
+    ctx_of[dev] = ctx;
   }
   *ptr = addr[dev];
   return cudaSuccess;
