@@ -267,6 +267,69 @@ def load_peaks():
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
 
 
+# Nominal GB300 figures (datasheet): HBM3e bandwidth and dense bf16 tensor
+# throughput.  The roofline fractions are taken against the measured peaks;
+# these are reported beside them.
+DATASHEET = {"hbm_gbs": 7900.0, "bf16_tflops": 2250.0}
+
+
+def fractions(achieved, kind_key, peaks, peak_kind):
+    """Roofline fraction against the measured peak and against the datasheet."""
+    return {"frac": round(achieved / peaks[kind_key], 4), "peak_kind": peak_kind,
+            "frac_datasheet": round(achieved / DATASHEET[kind_key], 4), "peak_datasheet": DATASHEET[kind_key]}
+
+
+def kernel_breakdown(fn, reps=2):
+    """Device time per call of every kernel (and memset) `fn` launches, from
+    the profiler's CUDA activity records of `reps` untimed calls: {name:
+    (launches per call, us per call)}.  None if the profiler is unavailable."""
+    import torch
+    try:
+        from torch.profiler import ProfilerActivity, profile
+    except ImportError:
+        return None
+    try:
+        torch.cuda.synchronize()
+        with profile(activities=[ProfilerActivity.CUDA]) as prof:
+            for _ in range(reps):
+                fn()
+            torch.cuda.synchronize()
+        out = {}
+        for e in prof.key_averages():
+            t = getattr(e, "device_time_total", None)
+            if t is None:
+                t = getattr(e, "cuda_time_total", 0.0)
+            if not t:
+                continue
+            name = e.key
+            for short in ("causal_kv_tc_kernel", "causal_dq_tc_kernel", "causal_prep_kernel", "rmsnorm_bwd",
+                          "softmax_bwd", "rope_bwd_kernel", "decode_bwd_kernel", "Memset"):
+                if short in name:
+                    name = short
+                    break
+            n, us = out.get(name, (0, 0.0))
+            out[name] = (n + e.count / reps, us + t / reps)
+        return out
+    except Exception:  # noqa: BLE001 - profiling is optional evidence
+        return None
+
+
+def time_launches(fn, stream, reps, flush=None):
+    """Mean device time (ms) of one call of `fn`, from CUDA events around
+    each call on `stream`; with `flush`, a buffer larger than L2 is written
+    before every call (outside the events)."""
+    import torch
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+    for a, b in evs:
+        if flush is not None:
+            flush.fill_(1.0)
+        a.record(stream)
+        fn()
+        b.record(stream)
+    torch.cuda.synchronize()
+    return statistics.mean(a.elapsed_time(b) for a, b in evs)
+
+
 def source_hash(*names):
     h = hashlib.sha256()
     for n in names:
@@ -362,9 +425,226 @@ def run_chain(abw, saved_forward, W, dev, stream, args, barrier, max_over_ranks,
     ms = max_over_ranks(e0.elapsed_time(e1)) / reps
     flops = L * causal_flops(shape.B, shape.T, shape.Hq, shape.D)
     rms_bytes = L * rmsnorm_bytes(shape.B * shape.T, W.CHAIN_HIDDEN, x_es=2, dx_es=2)
+    # per-kernel device time of one chain (eager launches under the profiler,
+    # outside the timed region), per layer, with each kernel's own rate
+    peaks, kind = load_peaks()
+    bd = kernel_breakdown(lambda: chain_once(stream), reps=1)
+    kernels = None
+    if bd:
+        per_layer = {k: (n / L, us / L) for k, (n, us) in bd.items()}
+        kernels = causal_kernel_figures({k: v for k, v in per_layer.items() if k != "rmsnorm_bwd"}, shape, peaks, kind)
+        if "rmsnorm_bwd" in per_layer:
+            n, us = per_layer["rmsnorm_bwd"]
+            gbs = rmsnorm_bytes(shape.B * shape.T, W.CHAIN_HIDDEN, 2, 2) / (us * 1e-6) / 1e9
+            kernels["rmsnorm_bwd"] = {"launches": round(n, 2), "us": round(us, 2), "gbs": round(gbs, 1),
+                                      "frac": round(gbs / peaks["hbm_gbs"], 4)}
+        kernels["note"] = "per layer; profiler activity records of one eagerly launched chain"
+    abw.device_check(stream)
     return {"workload": "chain_30_layers_b2_t512_hq20_hkv5_d128_n2560", "ms_per_chain": round(ms, 4),
             "us_per_layer": round(1e3 * ms / L, 2), "attn_tflops": round(world * flops / (ms * 1e-3) / 1e12, 2),
-            "launch": mode, "flops_per_chain": flops, "rmsnorm_bytes_per_chain": rms_bytes}
+            "launch": mode, "flops_per_chain": flops, "rmsnorm_bytes_per_chain": rms_bytes,
+            "kernels_per_layer": kernels}
+
+
+def causal_io_bytes(B, T, Hq, Hkv, D):
+    """Algorithmic bytes of one causal call: q, o, dout, k, v (bf16) and lse
+    read once; dq, dk, dv (fp32) written once."""
+    return 2 * (3 * B * T * Hq * D + 2 * B * T * Hkv * D) + 4 * B * Hq * T + 4 * (B * T * Hq * D + 2 * B * T * Hkv * D)
+
+
+def causal_kernel_figures(bd, shape, peaks, kind):
+    """Per-kernel share, time and rate of one causal call from the profiler
+    breakdown: the kv kernel does four of the five products (S, dP, dV, dK),
+    the dq kernel the fifth; the prep kernel reads o and dout and writes the
+    per-row statistics (bytes)."""
+    if not bd:
+        return None
+    B, T, Hq, Hkv, D = shape.B, shape.T, shape.Hq, shape.Hkv, shape.D
+    Tp = (T + 127) // 128 * 128
+    flops = causal_flops(B, T, Hq, D)
+    total = sum(us for _, us in bd.values())
+    out = {}
+    for name, (n, us) in sorted(bd.items(), key=lambda kv: -kv[1][1]):
+        e = {"launches": round(n, 2), "us": round(us, 2), "share": round(us / total, 4) if total else None}
+        if name == "causal_kv_tc_kernel":
+            tf = 0.8 * flops / (us * 1e-6) / 1e12
+            e.update(tflops=round(tf, 1), frac=round(tf / peaks["bf16_tflops"], 4))
+        elif name == "causal_dq_tc_kernel":
+            tf = 0.2 * flops / (us * 1e-6) / 1e12
+            e.update(tflops=round(tf, 1), frac=round(tf / peaks["bf16_tflops"], 4))
+        elif name == "causal_prep_kernel":
+            by = 2 * 2 * B * T * Hq * D + 4 * B * Hq * T + 2 * 4 * B * Hq * Tp + T * (D // 2) * 8
+            gbs = by / (us * 1e-6) / 1e9
+            e.update(gbs=round(gbs, 1), frac=round(gbs / peaks["hbm_gbs"], 4))
+        out[name] = e
+    out["peak_kind"] = kind + " (burst)"
+    return out
+
+
+def run_causal(abw, saved_forward, W, cs, seed, name, dev, stream, args, barrier, max_over_ranks, world, local):
+    """One causal backward call per step (prep, dK/dV and dQ kernels), CUDA
+    events around the K calls, clocks sampled meanwhile; per-kernel times
+    from a separate profiled call."""
+    import torch
+    cin = {k: v.to(dev) for k, v in W.causal_inputs(cs, seed=seed).items()}
+    o, lse = saved_forward.causal_forward(cin["q"], cin["k"], cin["v"], cs.scale)
+    cq = torch.empty(cin["q"].shape, dtype=torch.float32, device=dev)
+    ck = torch.empty(cin["k"].shape, dtype=torch.float32, device=dev)
+    cv = torch.empty_like(ck)
+    wsb = abw.attn_bwd_causal_workspace_bytes(cs.B, cs.T, cs.Hq, cs.D)
+    ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
+
+    def cstep():
+        abw.attn_bwd_causal(cin["q"], cin["k"], cin["v"], o, cin["dout"], lse, cs.scale, cs.rope_base, cs.pos0,
+                            dq=cq, dk=ck, dv=cv, workspace=ws, stream=stream)
+
+    for _ in range(args.warmup):
+        cstep()
+    abw.device_check(stream)
+    barrier()
+    c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    csteps = max(1, args.steps)
+    with ClockSampler(local) as cclocks:
+        cclocks.wait_first()
+        keep_busy(cstep, stream, 0.3)
+        barrier()
+        ch0 = cclocks.mark()
+        c0.record(stream)
+        for _ in range(csteps):
+            cstep()
+        c1.record(stream)
+        torch.cuda.synchronize()
+        ch1 = cclocks.mark()
+    barrier()
+    abw.device_check(stream)
+    cms = max_over_ranks(c0.elapsed_time(c1)) / csteps
+    flops = causal_flops(cs.B, cs.T, cs.Hq, cs.D)
+    ctf = world * flops / (cms * 1e-3) / 1e12
+    peaks, kind = load_peaks()
+    io = causal_io_bytes(cs.B, cs.T, cs.Hq, cs.Hkv, cs.D)
+    bd = kernel_breakdown(cstep)
+    abw.device_check(stream)
+    out = {"workload": name, "value": round(ctf, 3), "unit": "TFLOP/s", "ms_per_call": round(cms, 4),
+           "flops_per_call": flops,
+           "l2": f"no flush: one call reads {io_in_mb(cs)} MB of inputs and writes {io_out_mb(cs)} MB of outputs, "
+                 f"and its dS workspace round trip moves {2 * (wsb >> 20)} MB, over 4x L2",
+           "algorithmic_bytes": io,
+           "roofline": {"bound": "tensor", "achieved": round(ctf / world, 3), "peak": peaks["bf16_tflops"],
+                        "unit": "TFLOP/s", **fractions(ctf / world, "bf16_tflops", peaks, kind + " (burst)"),
+                        "traffic": recorded_traffic("causal_kv_tc_kernel" if cs.T == 2048 else "causal_kv_tc_kernel_t8192",
+                                                    ["causal.cu", "abw_device.cuh", "tcgen05.cuh"]),
+                        "traffic_kernel": "causal_kv_tc_kernel", "scope": "whole call"},
+           "kernels": causal_kernel_figures(bd, cs, peaks, kind),
+           "clocks": cclocks.summary(ch0, ch1)}
+    del cin, o, lse, cq, ck, cv, ws
+    torch.cuda.empty_cache()
+    return out
+
+
+def io_in_mb(cs):
+    return round((2 * (3 * cs.B * cs.T * cs.Hq * cs.D + 2 * cs.B * cs.T * cs.Hkv * cs.D) + 4 * cs.B * cs.Hq * cs.T) / 1e6)
+
+
+def io_out_mb(cs):
+    return round(4 * (cs.B * cs.T * cs.Hq * cs.D + 2 * cs.B * cs.T * cs.Hkv * cs.D) / 1e6)
+
+
+def run_rows(abw, W, dev, stream, args):
+    """The memory-bound row kernels on their own, each timed per launch with
+    CUDA events against the HBM peak: RoPE backward over the causal dq shape,
+    RMSNorm backward at the chain's 1024 x 2560 bf16 rows (L2 flushed before
+    every launch) and at 65536 x 2560 fp32 rows, softmax backward over
+    65536 rows of 1024."""
+    import torch
+    peaks, kind = load_peaks()
+    g = torch.Generator(device=dev)
+    g.manual_seed(W.SEED_BASE + 30)
+    reps = max(3, args.steps)
+    flush = torch.empty(256 << 20, dtype=torch.float32, device=dev)    # 1 GiB, over 8x L2
+    out = {}
+
+    def leg(name, fn, nbytes, cold):
+        for _ in range(3):
+            fn()
+        ms = time_launches(fn, stream, reps, flush if cold else None)
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        out[name] = {"us": round(ms * 1e3, 2), "bytes": nbytes, "gbs": round(gbs, 1),
+                     **fractions(gbs, "hbm_gbs", peaks, kind),
+                     "l2": "flushed before each launch" if cold else "inputs larger than L2"}
+
+    # RoPE backward, dq of the causal T = 2048 workload: [4][2048][20][128] fp32
+    dy = torch.randn(4, 2048, 20, 128, generator=g, device=dev)
+    dx = torch.empty_like(dy)
+    leg("rope_bwd_b4_t2048_h20_d128", lambda: abw.rope_bwd(dy, pos0=0, base=10000.0, dx=dx, stream=stream),
+        2 * dy.numel() * 4, False)
+    del dy, dx
+    # RMSNorm backward at the chain's rows (bf16 x and dx, fp32 dy)
+    for rows_n, xdt, cold in ((1024, torch.bfloat16, True), (65536, torch.float32, False)):
+        x = torch.randn(rows_n, 2560, generator=g, device=dev).to(xdt)
+        gam = 1.0 + 0.1 * torch.randn(2560, generator=g, device=dev)
+        dyr = torch.randn(rows_n, 2560, generator=g, device=dev)
+        dxr = torch.empty(rows_n, 2560, dtype=xdt, device=dev)
+        es = 2 if xdt == torch.bfloat16 else 4
+        leg(f"rmsnorm_bwd_{rows_n}x2560_{'bf16' if es == 2 else 'f32'}",
+            lambda: abw.rmsnorm_bwd(x, gam, dyr, eps=1e-6, dx=dxr, stream=stream),
+            rmsnorm_bytes(rows_n, 2560, es, es), cold)
+        del x, gam, dyr, dxr
+    # softmax backward, 65536 rows of 1024 probabilities
+    sm = torch.softmax(torch.randn(65536, 1024, generator=g, device=dev), -1)
+    dys = torch.randn(65536, 1024, generator=g, device=dev)
+    dxs = torch.empty_like(dys)
+    leg("softmax_bwd_65536x1024", lambda: abw.softmax_bwd(sm, dys, dx=dxs, stream=stream), 3 * sm.numel() * 4, False)
+    del sm, dys, dxs, flush
+    abw.device_check(stream)
+    torch.cuda.empty_cache()
+    return out
+
+
+def run_tiny(abw, W, dev, stream, reps=200):
+    """Latency of each operation at the single-head sizes (attention with
+    D = 8 over 16 keys, softmax of 16, four RoPE pairs, RMSNorm of 8): mean
+    device time per call over back-to-back calls, in microseconds."""
+    import torch
+    import numpy as np
+    t = W.tiny_inputs()
+    q = t["q"].reshape(1, 1, 8).to(dev)
+    k = t["k"].reshape(1, 16, 1, 8).to(dev)
+    v = t["v"].reshape(1, 16, 1, 8).to(dev)
+    do = t["dout"].reshape(1, 1, 8).to(dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    x = t["soft_x"][None].to(dev)
+    s = torch.softmax(x, -1)
+    sdy = t["soft_dy"][None].to(dev)
+    sdx = torch.empty_like(s)
+    rdy = torch.stack([t["rope_x0"], t["rope_x1"]], -1).reshape(1, 4, 1, 2).contiguous().to(dev)
+    th = t["rope_theta"].reshape(4, 1).contiguous().to(dev)
+    rdx = torch.empty_like(rdy)
+    mx = t["rms_x"][None].to(dev)
+    mg = t["rms_gamma"].to(dev)
+    mdy = t["rms_dy"][None].to(dev)
+    mdx = torch.empty_like(mx)
+    ops = {
+        "attn_bwd_decode_d8_s16": lambda: abw.attn_bwd_decode(q, k, v, do, t["scale"], dq=dq, dk=dk, dv=dv,
+                                                              stream=stream),
+        "softmax_bwd_16": lambda: abw.softmax_bwd(s, sdy, dx=sdx, stream=stream),
+        "rope_bwd_4_pairs": lambda: abw.rope_bwd(rdy, theta=th, dx=rdx, stream=stream),
+        "rmsnorm_bwd_8": lambda: abw.rmsnorm_bwd(mx, mg, mdy, eps=t["eps"], dx=mdx, stream=stream),
+    }
+    out = {}
+    for name, fn in ops.items():
+        for _ in range(10):
+            fn()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(reps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        out[name] = round(1e3 * e0.elapsed_time(e1) / reps, 2)
+    abw.device_check(stream)
+    out["unit"] = "us per call (back-to-back launches, events on the stream)"
+    return out
 
 
 def keep_busy(fn, stream, seconds):
@@ -545,58 +825,19 @@ def run_native(args):
     del g, gbuf, obuf, dq, dk, dv, dx, hout
     torch.cuda.empty_cache()
 
-    # ------------------------------------------------------------ causal T = 2048
-    causal = None
+    # ------------------------------------------------------------ causal T = 2048 and T = 8192
+    causal, causal_long = None, None
     if not args.skip_causal:
-        cs = W.CAUSAL_2K
-        cin = {k: v.to(dev) for k, v in W.causal_inputs(cs, seed=W.SEED_BASE + 3).items()}
-        o, lse = saved_forward.causal_forward(cin["q"], cin["k"], cin["v"], cs.scale)
-        cq = torch.empty(cin["q"].shape, dtype=torch.float32, device=dev)
-        ck = torch.empty(cin["k"].shape, dtype=torch.float32, device=dev)
-        cv = torch.empty_like(ck)
-        ws = torch.empty(abw.attn_bwd_causal_workspace_bytes(cs.B, cs.T, cs.Hq, cs.D), dtype=torch.uint8, device=dev)
+        causal = run_causal(abw, saved_forward, W, W.CAUSAL_2K, W.SEED_BASE + 3,
+                            "causal_b4_h20_d128_t2048_bf16_rope1e4", dev, stream, args, barrier, max_over_ranks,
+                            world, local)
+        causal_long = run_causal(abw, saved_forward, W, W.CAUSAL_8K, W.SEED_BASE + 4,
+                                 "causal_b1_h32_d128_t8192_bf16_qkx4", dev, stream, args, barrier, max_over_ranks,
+                                 world, local)
 
-        def cstep():
-            abw.attn_bwd_causal(cin["q"], cin["k"], cin["v"], o, cin["dout"], lse, cs.scale, cs.rope_base, 0,
-                                dq=cq, dk=ck, dv=cv, workspace=ws, stream=stream)
-
-        for _ in range(args.warmup):
-            cstep()
-        abw.device_check(stream)
-        barrier()
-        c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        csteps = max(1, args.steps)
-        with ClockSampler(local) as cclocks:
-            cclocks.wait_first()
-            keep_busy(cstep, stream, 0.3)
-            barrier()
-            ch0 = cclocks.mark()
-            c0.record(stream)
-            for _ in range(csteps):
-                cstep()
-            c1.record(stream)
-            torch.cuda.synchronize()
-            ch1 = cclocks.mark()
-        barrier()
-        abw.device_check(stream)
-        cms = max_over_ranks(c0.elapsed_time(c1)) / csteps
-        flops = causal_flops(cs.B, cs.T, cs.Hq, cs.D)
-        ctf = world * flops / (cms * 1e-3) / 1e12
-        peaks, kind = load_peaks()
-        causal = {"workload": "causal_b4_h20_d128_t2048_bf16_rope1e4", "value": round(ctf, 3), "unit": "TFLOP/s",
-                  "ms_per_call": round(cms, 4), "flops_per_call": flops,
-                  "l2": "no flush: one call moves 590 MB (inputs 105 MB, dS workspace 359 MB, outputs 126 MB), "
-                        "over 4x L2",
-                  "roofline": {"bound": "tensor", "achieved": round(ctf / world, 3),
-                               "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                               "frac": round(ctf / world / peaks["bf16_tflops"], 4),
-                               "traffic": recorded_traffic("causal_kv_tc_kernel",
-                                                           ["causal.cu", "abw_device.cuh", "tcgen05.cuh"]),
-                               "traffic_kernel": "causal_kv_tc_kernel",
-                               "peak_kind": kind + " (burst)", "scope": "whole call"},
-                  "clocks": cclocks.summary(ch0, ch1)}
-        del cin, o, lse, cq, ck, cv, ws
-        torch.cuda.empty_cache()
+    # ------------------------------------------------------------ row kernels
+    rows = None if args.skip_rows else run_rows(abw, W, dev, stream, args)
+    tiny = None if args.skip_rows else run_tiny(abw, W, dev, stream)
 
     # ------------------------------------------------------------ 30-layer chain
     chain = None
@@ -607,9 +848,9 @@ def run_native(args):
     peaks, kind = load_peaks()
     achieved = dec_bytes / (kern_ms * 1e-3) / 1e9
     roofline = {"bound": "hbm", "achieved": round(achieved, 2), "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": round(achieved / peaks["hbm_gbs"], 4),
+                **fractions(achieved, "hbm_gbs", peaks, kind),
                 "traffic": recorded_traffic("decode_bwd_kernel", ["decode.cu", "abw_device.cuh"]),
-                "kernel": "decode_bwd_kernel", "bytes_per_launch": dec_bytes, "peak_kind": kind}
+                "kernel": "decode_bwd_kernel", "bytes_per_launch": dec_bytes}
 
     cpu = None
     if rank == 0 and world == 1 and not args.skip_cpu:
@@ -628,7 +869,7 @@ def run_native(args):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic",
             "config": {"workload": DECODE_WORKLOAD, "global_batch": 64 * world, "seq_len": 1024,
-                       "parallelism": f"replicas{world}", "l2": "inputs larger than L2 (505 MB per step)",
+                       "parallelism": "replicas", "l2": "inputs larger than L2 (505 MB per step)",
                        "launch": launch_mode,
                        "compute": "bf16 K/V; scores and dP on the tensor core with q/dout split into bf16 high+low parts, fp32 accumulation; fp32 elsewhere"},
             "roofline": roofline,
@@ -639,6 +880,9 @@ def run_native(args):
             "gpu_launches": launches,
             "clocks": clocks.summary(h0, h1),
             "causal_t2048": causal,
+            "causal_t8192": causal_long,
+            "rows": rows,
+            "tiny_latency": tiny,
             "chain_30_layers": chain,
         }
         print(json.dumps(line), flush=True)
@@ -656,6 +900,7 @@ def main():
     ap.add_argument("--skip-causal", action="store_true")
     ap.add_argument("--skip-cpu", action="store_true")
     ap.add_argument("--skip-chain", action="store_true")
+    ap.add_argument("--skip-rows", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "native":
         args.warmup = 3
