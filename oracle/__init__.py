@@ -13,8 +13,10 @@ Each function is the plain definition of one step, written from these pages:
     Numerical Gradient Verification) -- the CPU specs of the backward ops;
   * Hesper pull request #1, commit log ("Attention backward GPU kernels",
     "RMSNorm backward in attention chain", the 30-layer reverse iteration,
-    "Tests/WrongBackwardTest.lean") -- the order of the chain and the
-    negative controls;
+    "Tests/WrongBackwardTest.lean", the FFN-backward commit with the
+    ReLU^2 x Mul backward, the LoRA backward at the end of the chain, the
+    FlashAttention commits' online-softmax forward) -- the order of the chain,
+    the negative controls and the steps around the attention backward;
   * DaisyChain-Train ``web/public/transformer.js`` (causal softmax in
     ``forward``, the batched attention block of ``backward``) -- the causal
     mask and the dK = dS^T Q / dV = A^T dctx products.
@@ -48,6 +50,8 @@ __all__ = [
     "attention_head_forward", "attention_head_backward", "attention_head_backward_saved_p",
     "decode_backward", "causal_forward", "causal_backward",
     "chain_layer_backward",
+    "relu2_mul_forward", "relu2_mul_backward",
+    "lora_forward", "lora_backward",
     "numerical_grad", "check_gradient",
 ]
 
@@ -415,6 +419,53 @@ def chain_layer_backward(x, gamma, dhidden, q, k, v, eps, scale, rope_base,
     dout = dx.reshape(B, T, Hq, D)
     dq, dk, dv = causal_backward(q, k, v, dout, scale, rope_base, 0, kv_heads)
     return dx, dq, dk, dv
+
+
+# ==========================================================================
+# FFN gate (Hesper pull request #1, the FFN-backward commit: "ReLU^2 x Mul
+# backward", the gated activation between the FFN's gate/up projections and
+# its down projection)
+# ==========================================================================
+def relu2_mul_forward(gate, up):
+    """hidden = ReLU(gate)^2 * up, element by element."""
+    gate, up = _f64(gate), _f64(up)
+    r = np.maximum(gate, 0.0)
+    return r * r * up
+
+
+def relu2_mul_backward(gate, up, dh):
+    """The page's two formulas, element by element:
+    dGate = dH * up * 2 ReLU(gate),  dUp = dH * ReLU(gate)^2."""
+    gate, up, dh = _f64(gate), _f64(up), _f64(dh)
+    r = np.maximum(gate, 0.0)
+    return dh * up * 2.0 * r, dh * r * r
+
+
+# ==========================================================================
+# LoRA adapter gradients (Hesper pull request #1: "LoRA gradients use
+# per-layer saved normedBuf", the chain that ends "RoPE backward -> dQ ->
+# LoRA backward", and the residual fix: LoRA's input gradient feeds only the
+# adapter's own parameter gradients dA, dB)
+# ==========================================================================
+def lora_forward(x, A, B, scale):
+    """The adapter's added output y = scale * B (A x) per row: x [rows][n_in],
+    A [r][n_in], B [n_out][r]; returns [rows][n_out].  The pages name the
+    adapter (rank 8 on the Q and V projections) but print no formula; this is
+    the standard low-rank update, with `scale` its alpha / r factor."""
+    x, A, B = _f64(x), _f64(A), _f64(B)
+    return scale * ((x @ A.T) @ B.T)
+
+
+def lora_backward(x, A, B, dy, scale):
+    """Parameter gradients of lora_forward, summed over rows:
+    h = x A^T;  dB = scale dy^T h;  dh = scale dy B;  dA = dh^T x.
+    Returns (dA [r][n_in], dB [n_out][r])."""
+    x, A, B, dy = _f64(x), _f64(A), _f64(B), _f64(dy)
+    h = x @ A.T
+    dB = scale * (dy.T @ h)
+    dh = scale * (dy @ B)
+    dA = dh.T @ x
+    return dA, dB
 
 
 # ==========================================================================

@@ -555,3 +555,73 @@ def test_planted_mistakes_fail():
     # RoPE angle with the wrong exponent (-i/D instead of -2i/D) breaks the closed form
     wrong = np.arange(4)[:, None] * np.power(10000.0, -np.arange(2) / 4.0)
     assert not np.allclose(wrong, O.rope_angles(np.arange(4), 4, 10000.0))
+
+
+# --------------------------------------------------------------------------
+# Causal forward (O, lse), FFN gate, LoRA: closed forms, VJPs, planted slips
+# --------------------------------------------------------------------------
+def test_golden_attention_forward(golden):
+    """Two keys, hand-derived: O = 3/2 and lse = ln 4 (the forward's saved
+    statistics that the backward consumes)."""
+    g = golden["attention_two_keys"]
+    O_, lse, P = O.attention_head_forward(np.array([g["q"]]), np.array(g["K"]), np.array(g["V"]), g["scale"],
+                                          causal=False)
+    np.testing.assert_allclose(O_[0], g["O"], rtol=1e-15)
+    np.testing.assert_allclose(lse, g["lse"], rtol=1e-15)
+    # the causal form over a single query at the last position is the same
+    o, l = O.causal_forward(np.array(g["q"])[None, None, None, :].repeat(2, 1),
+                            np.array(g["K"])[None, :, None, :], np.array(g["V"])[None, :, None, :], g["scale"])
+    np.testing.assert_allclose(o[0, 1, 0], g["O"], rtol=1e-15)
+    np.testing.assert_allclose(l[0, 0, 1], g["lse"], rtol=1e-15)
+
+
+def test_golden_relu2_mul(golden):
+    g = golden["relu2_mul"]
+    np.testing.assert_allclose(O.relu2_mul_forward(g["gate"], g["up"]), g["hidden"], rtol=0, atol=0)
+    dg, du = O.relu2_mul_backward(g["gate"], g["up"], g["dh"])
+    np.testing.assert_allclose(dg, g["dgate"], rtol=0, atol=0)
+    np.testing.assert_allclose(du, g["dup"], rtol=0, atol=0)
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_relu2_mul_vjp_and_controls(seed):
+    r = rng(400 + seed)
+    gate, up, dh = r.normal(size=11), r.normal(size=11), r.normal(size=11)
+    dg, du = O.relu2_mul_backward(gate, up, dh)
+    num_g = O.numerical_grad(lambda z: float(np.dot(dh, O.relu2_mul_forward(z, up))), gate)
+    num_u = O.numerical_grad(lambda z: float(np.dot(dh, O.relu2_mul_forward(gate, z))), up)
+    assert O.check_gradient(dg, num_g) and O.check_gradient(du, num_u)
+    relu = np.maximum(gate, 0.0)
+    for bad in (np.zeros_like(dg), dh, -dg, dh * up * relu):          # zero, identity, negated, dropped 2
+        assert not O.check_gradient(bad, num_g)
+    for bad in (np.zeros_like(du), dh, -du, dh * relu):                # ..., ReLU for ReLU^2
+        assert not O.check_gradient(bad, num_u)
+
+
+def test_golden_lora(golden):
+    g = golden["lora_rank1"]
+    np.testing.assert_allclose(O.lora_forward(g["x"], g["A"], g["B"], g["scale"]), g["y"], rtol=0, atol=0)
+    dA, dB = O.lora_backward(g["x"], g["A"], g["B"], g["dy"], g["scale"])
+    np.testing.assert_allclose(dA, g["dA"], rtol=0, atol=0)
+    np.testing.assert_allclose(dB, g["dB"], rtol=0, atol=0)
+
+
+def test_lora_vjp_and_controls():
+    r = rng(410)
+    rows, n_in, rank, n_out, s = 5, 7, 3, 6, 0.75
+    x, A, B, dy = (r.normal(size=(rows, n_in)), r.normal(size=(rank, n_in)), r.normal(size=(n_out, rank)),
+                   r.normal(size=(rows, n_out)))
+    dA, dB = O.lora_backward(x, A, B, dy, s)
+    num_A = O.numerical_grad(lambda z: float(np.sum(dy * O.lora_forward(x, z, B, s))), A)
+    num_B = O.numerical_grad(lambda z: float(np.sum(dy * O.lora_forward(x, A, z, s))), B)
+    assert O.check_gradient(dA, num_A) and O.check_gradient(dB, num_B)
+    h = x @ A.T
+    assert not O.check_gradient(dA / s, num_A)                        # dropped scale
+    assert not O.check_gradient(-dA, num_A)                           # negated
+    assert not O.check_gradient((dy @ B).T @ x * 0.0, num_A)          # zero
+    assert not O.check_gradient(s * (dy.T @ (x @ A.T)) * 0.5, num_B)  # halved
+    assert not O.check_gradient(s * (dy.T @ h[:, ::-1]), num_B)       # wrong rank index order
+    # rows are independent terms of the sums: the whole equals the row sum
+    parts = [O.lora_backward(x[i:i + 1], A, B, dy[i:i + 1], s) for i in range(rows)]
+    np.testing.assert_allclose(sum(p[0] for p in parts), dA, rtol=1e-13, atol=1e-13)
+    np.testing.assert_allclose(sum(p[1] for p in parts), dB, rtol=1e-13, atol=1e-13)
