@@ -87,7 +87,17 @@ struct Layout {
     const int scratch = resident ? 0 : 2 * rs * G * D * 4;    // streaming: row-split dq partials
     const int ns = resident ? 0 : 1;
     kv = o;    o += tiles > scratch ? tiles : scratch;   o = up(o, 16);
-    qs = o;    o += swz ? 2 * gs * 4 * (D / 4 + 4) * 4 : 0;
+    // The tensor-core path (128-key chunk, D = 128) stages its [16 rows]
+    // [128] bf16 B operands at qs: first s / dP's two (8 KB, which may run on
+    // into sbuf / pbuf, written only after those products complete), later
+    // dq's one (4 KB, written while pbuf is read, so within qs alone).
+    int qsz = swz ? 2 * gs * 4 * (D / 4 + 4) * 4 : 0;
+    if (swz && D == 128 && chunk == 2 * kTile) {
+      const int need = 8192 - 2 * gs * chunk * 4;
+      qsz = qsz > need ? qsz : need;
+      qsz = qsz > 4096 ? qsz : 4096;
+    }
+    qs = o;    o += qsz;
     sbuf = o;  o += gs * chunk * 4;
     pbuf = o;  o += gs * chunk * 4;
     etile = o; o += ns * gs * kTile * 4;
