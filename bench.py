@@ -289,11 +289,16 @@ def kernel_breakdown(fn, reps=2):
     except ImportError:
         return None
     try:
-        torch.cuda.synchronize()
-        with profile(activities=[ProfilerActivity.CUDA]) as prof:
-            for _ in range(reps):
-                fn()
+        prof = None
+        for _ in range(2):                      # the first profiled run can come back without device times
             torch.cuda.synchronize()
+            with profile(activities=[ProfilerActivity.CUDA]) as prof:
+                for _ in range(reps):
+                    fn()
+                torch.cuda.synchronize()
+            if any((getattr(e, "device_time_total", None) or getattr(e, "cuda_time_total", 0.0))
+                   for e in prof.key_averages()):
+                break
         out = {}
         for e in prof.key_averages():
             t = getattr(e, "device_time_total", None)
@@ -550,11 +555,13 @@ def io_out_mb(cs):
 
 
 def run_rows(abw, W, dev, stream, args):
-    """The memory-bound row kernels on their own, each timed per launch with
-    CUDA events against the HBM peak: RoPE backward over the causal dq shape,
-    RMSNorm backward at the chain's 1024 x 2560 bf16 rows (L2 flushed before
-    every launch) and at 65536 x 2560 fp32 rows, softmax backward over
-    65536 rows of 1024."""
+    """The memory-bound kernels on their own, each timed per launch with CUDA
+    events against the HBM peak: RoPE backward over the causal dq shape,
+    RMSNorm backward at the chain's 1024 x 2560 bf16 rows and at 65536 x 2560
+    fp32 rows, softmax backward over 65536 rows of 1024, and one chain
+    layer's RMSNorm scale gradient, FFN gate backward and LoRA Q / V adapter
+    gradients.  Working sets below L2 are timed with L2 flushed before every
+    launch."""
     import torch
     peaks, kind = load_peaks()
     g = torch.Generator(device=dev)
@@ -594,7 +601,37 @@ def run_rows(abw, W, dev, stream, args):
     dys = torch.randn(65536, 1024, generator=g, device=dev)
     dxs = torch.empty_like(dys)
     leg("softmax_bwd_65536x1024", lambda: abw.softmax_bwd(sm, dys, dx=dxs, stream=stream), 3 * sm.numel() * 4, False)
-    del sm, dys, dxs, flush
+    del sm, dys, dxs
+    # RMSNorm backward with the scale gradient, one chain layer's rows
+    x = torch.randn(1024, 2560, generator=g, device=dev).to(torch.bfloat16)
+    gam = 1.0 + 0.1 * torch.randn(2560, generator=g, device=dev)
+    dyr = torch.randn(1024, 2560, generator=g, device=dev)
+    dxr = torch.empty(1024, 2560, dtype=torch.bfloat16, device=dev)
+    dgr = torch.empty(2560, device=dev)
+    leg("rmsnorm_bwd_dgamma_1024x2560_bf16",
+        lambda: abw.rmsnorm_bwd_dgamma(x, gam, dyr, eps=1e-6, dx=dxr, dgamma=dgr, stream=stream),
+        rmsnorm_bytes(1024, 2560, 2, 2) + 2560 * 4, True)
+    # ReLU^2 x Mul backward over one layer's FFN activations (1024 tokens x
+    # intermediate width 6912, bf16 gate / up, fp32 gradients)
+    gt = torch.randn(1024, 6912, generator=g, device=dev).to(torch.bfloat16)
+    ut = torch.randn(1024, 6912, generator=g, device=dev).to(torch.bfloat16)
+    dht = torch.randn(1024, 6912, generator=g, device=dev)
+    dgt, dut = torch.empty_like(dht), torch.empty_like(dht)
+    leg("relu2_mul_bwd_1024x6912_bf16", lambda: abw.relu2_mul_bwd(gt, ut, dht, dgate=dgt, dup=dut, stream=stream),
+        gt.numel() * (2 + 2 + 4 + 8), True)
+    del gt, ut, dht, dgt, dut
+    # LoRA adapter gradients of one chain layer: Q (2560 -> 2560) and V
+    # (2560 -> 640), rank 8, 1024 rows of the saved normed input (bf16)
+    for nm, n_out in (("q", 2560), ("v", 640)):
+        A = 0.02 * torch.randn(8, 2560, generator=g, device=dev)
+        Bm = 0.02 * torch.randn(n_out, 8, generator=g, device=dev)
+        dyl = torch.randn(1024, n_out, generator=g, device=dev)
+        dA, dB = torch.empty_like(A), torch.empty_like(Bm)
+        wsl = torch.empty(abw.lora_bwd_workspace_bytes(1024, 8), dtype=torch.uint8, device=dev)
+        leg(f"lora_bwd_{nm}_1024x2560_to_{n_out}_r8",
+            lambda: abw.lora_bwd(x, dyl, A, Bm, 2.0, dA=dA, dB=dB, workspace=wsl, stream=stream),
+            1024 * 2560 * 2 + 1024 * n_out * 4 + 2 * 8 * (2560 + n_out) * 4, True)
+    del x, gam, dyr, dxr, dgr, flush
     abw.device_check(stream)
     torch.cuda.empty_cache()
     return out

@@ -1,10 +1,12 @@
 /*
  * attn_bwd.h -- C ABI of the attention backward chain for NVIDIA GB300 (sm_103a).
  *
- * Five operations, each the backward (vector-Jacobian product) of one step of
- * a transformer attention layer, as specified by the CPU specs of the
+ * The backward (vector-Jacobian product) of each step of a transformer
+ * attention layer, as specified by the CPU specs of the
  * "Hesper.Training.VerifiedBackward" API page and the backward chain of
- * Hesper pull request #1 ("Attention backward GPU kernels"):
+ * Hesper pull request #1 ("Attention backward GPU kernels"), plus the steps
+ * around it that the chain runs (the norm's scale gradient, the FFN's gated
+ * activation, the LoRA adapter gradients):
  *
  *   softmax_bwd      dx = s * (dy - sum(s * dy))                     (section Softmax)
  *   rope_bwd         dx = R(-theta) dy per rotary pair               (section RoPE)
@@ -16,6 +18,9 @@
  *                    probabilities from the saved log-sum-exp; RoPE backward fused on
  *                    dq and dk (DaisyChain-Train transformer.js, backward(): dV = A^T dctx,
  *                    dA = dctx V^T, dS = A (dA - sum A dA), dQ = dS K, dK = dS^T Q)
+ *   rmsnorm_bwd_dgamma  rmsnorm_bwd plus dgamma = sum_rows dy x / rms
+ *   relu2_mul_bwd    dgate = dh up 2 ReLU(gate), dup = dh ReLU(gate)^2  (PR #1, FFN backward)
+ *   lora_bwd         dA, dB of y = s B A x                             (PR #1, LoRA backward)
  *
  * Conventions shared by every entry point
  *   - All pointers are DEVICE pointers (cudaMalloc'd or equivalent), owned by
@@ -126,6 +131,56 @@ abw_status rope_bwd(const float *dy, float *dx, int B, int T, int H, int D,
 abw_status rmsnorm_bwd(const void *x, abw_dtype x_dtype, const float *gamma,
                        const float *dy, void *dx, abw_dtype dx_dtype, int rows, int n,
                        float eps, abw_stream stream);
+
+/*
+ * rmsnorm_bwd_dgamma -- rmsNormBackward (section RMSNorm) together with the
+ * gradient of the norm's scale.  The page states dx only; the forward
+ * y_i = gamma_i x_i / rms is linear in gamma, so its scale gradient is
+ *   dgamma_i = sum over rows of dy_i x_i / rms.
+ *   x, gamma, dy, dx as rmsnorm_bwd; dx may be NULL (then gamma may be NULL
+ *   too, and only dgamma is produced)
+ *   dgamma [n] f32, overwritten (the call zeroes it, then adds every row)
+ * The row sums are fp32; the order in which the rows' terms are added into
+ * dgamma varies from call to call (reductions in L2), so results agree to
+ * fp32 rounding, not bit for bit.
+ */
+abw_status rmsnorm_bwd_dgamma(const void *x, abw_dtype x_dtype, const float *gamma, const float *dy,
+                              void *dx, abw_dtype dx_dtype, float *dgamma, int rows, int n, float eps,
+                              abw_stream stream);
+
+/*
+ * relu2_mul_bwd -- backward of the FFN's gated activation
+ * hidden = ReLU(gate)^2 * up (Hesper pull request #1, the FFN-backward
+ * commit's "ReLU^2 x Mul backward"), element by element:
+ *   dgate = dh * up * 2 ReLU(gate),   dup = dh * ReLU(gate)^2.
+ *   gate, up  [n] act_dtype (f32 or bf16)  saved forward activations
+ *   dh        [n] f32                      upstream gradient of hidden
+ *   dgate, dup [n] f32                     outputs
+ * n >= 0 (any layout: the operation is element-wise).
+ */
+abw_status relu2_mul_bwd(const void *gate, const void *up, abw_dtype act_dtype, const float *dh,
+                         float *dgate, float *dup, long long n, abw_stream stream);
+
+/*
+ * lora_bwd -- parameter gradients of a rank-r LoRA adapter on a projection
+ * (Hesper pull request #1: the backward chain ends "RoPE backward -> dQ ->
+ * LoRA backward", the adapter's input being the layer's saved normed
+ * activations, and its input gradient feeds only dA and dB).  The adapter
+ * adds y = scale * B (A x) per row; with h = x A^T:
+ *   dB = scale dy^T h,   dA = (scale dy B)^T x      (sums over the rows)
+ *   x   [rows][n_in] f32 or bf16 (x_dtype)   saved adapter input
+ *   dy  [rows][n_out] f32                    gradient of the projection's output
+ *                                            (e.g. dq as [tokens][Hq*D])
+ *   A   [r][n_in] f32;   B [n_out][r] f32
+ *   dA  [r][n_in] f32;   dB [n_out][r] f32   overwritten
+ *   workspace  device memory of at least lora_bwd_workspace_bytes(rows, r)
+ * Supported: 1 <= r <= 16; n_in and n_out multiples of 4.  Sums over rows are
+ * fp32, added in an order that varies from call to call.
+ */
+size_t lora_bwd_workspace_bytes(int rows, int r);
+abw_status lora_bwd(const void *x, abw_dtype x_dtype, const float *dy, const float *A, const float *B,
+                    float *dA, float *dB, int rows, int n_in, int n_out, int r, float scale,
+                    void *workspace, size_t workspace_bytes, abw_stream stream);
 
 /*
  * attn_bwd_decode -- one query per sequence against a KV cache (attentionBackwardQ,

@@ -7,8 +7,9 @@ stream to the library.  Every arithmetic step runs in the library's CUDA
 kernels; nothing here computes, and there is no fallback path.
 
 Functions (same names as the C ABI):
-  softmax_bwd, rope_bwd, rmsnorm_bwd, attn_bwd_decode, attn_bwd_causal,
-  attn_bwd_causal_workspace_bytes, device_check
+  softmax_bwd, rope_bwd, rmsnorm_bwd, rmsnorm_bwd_dgamma, relu2_mul_bwd,
+  lora_bwd, attn_bwd_decode, attn_bwd_causal, attn_bwd_causal_workspace_bytes,
+  device_check
 """
 from __future__ import annotations
 
@@ -19,7 +20,8 @@ import torch
 
 from . import _binding as _b
 
-__all__ = ["softmax_bwd", "rope_bwd", "rmsnorm_bwd", "attn_bwd_decode", "attn_bwd_causal",
+__all__ = ["softmax_bwd", "rope_bwd", "rmsnorm_bwd", "rmsnorm_bwd_dgamma", "relu2_mul_bwd", "lora_bwd",
+           "attn_bwd_decode", "attn_bwd_causal",
            "attn_bwd_causal_workspace_bytes", "device_check", "AbwError", "library"]
 
 AbwError = _b.AbwError
@@ -103,6 +105,75 @@ def rmsnorm_bwd(x, gamma, dy, eps=1e-6, dx=None, dx_dtype=torch.float32, stream=
     _b.check(library().rmsnorm_bwd(_p(x), _DT[x.dtype], _p(gamma), _p(dy), _p(dx), _DT[dx.dtype], rows, n,
                                    float(eps), _s(stream)), "rmsnorm_bwd")
     return dx
+
+
+def rmsnorm_bwd_dgamma(x, gamma, dy, eps=1e-6, dx=None, dgamma=None, dx_dtype=torch.float32, want_dx=True,
+                       stream=None):
+    """RMSNorm backward with the scale gradient.  x [rows][n] fp32/bf16,
+    gamma [n] fp32, dy [rows][n] fp32.  Returns (dx or None, dgamma [n] fp32)."""
+    _req(x, "x", (torch.float32, torch.bfloat16))
+    n = x.shape[-1]
+    rows = x.numel() // n
+    _req(dy, "dy", (torch.float32,), x.shape)
+    if want_dx:
+        _req(gamma, "gamma", (torch.float32,), (n,))
+        if dx is None:
+            dx = torch.empty(x.shape, dtype=dx_dtype, device=x.device)
+        _req(dx, "dx", (torch.float32, torch.bfloat16), x.shape)
+    else:
+        dx = None
+    if dgamma is None:
+        dgamma = torch.empty(n, dtype=torch.float32, device=x.device)
+    _req(dgamma, "dgamma", (torch.float32,), (n,))
+    _b.check(library().rmsnorm_bwd_dgamma(_p(x), _DT[x.dtype], _p(gamma) if want_dx else None, _p(dy), _p(dx),
+                                          _DT[dx.dtype] if dx is not None else _b.F32, _p(dgamma), rows, n,
+                                          float(eps), _s(stream)), "rmsnorm_bwd_dgamma")
+    return dx, dgamma
+
+
+def relu2_mul_bwd(gate, up, dh, dgate=None, dup=None, stream=None):
+    """Backward of hidden = ReLU(gate)^2 * up: gate, up fp32/bf16 (same
+    dtype), dh fp32, all the same shape.  Returns (dgate, dup) fp32."""
+    _req(gate, "gate", (torch.float32, torch.bfloat16))
+    _req(up, "up", (gate.dtype,), gate.shape)
+    _req(dh, "dh", (torch.float32,), gate.shape)
+    dgate = torch.empty(gate.shape, dtype=torch.float32, device=gate.device) if dgate is None else dgate
+    dup = torch.empty(gate.shape, dtype=torch.float32, device=gate.device) if dup is None else dup
+    _req(dgate, "dgate", (torch.float32,), gate.shape)
+    _req(dup, "dup", (torch.float32,), gate.shape)
+    _b.check(library().relu2_mul_bwd(_p(gate), _p(up), _DT[gate.dtype], _p(dh), _p(dgate), _p(dup), gate.numel(),
+                                     _s(stream)), "relu2_mul_bwd")
+    return dgate, dup
+
+
+def lora_bwd_workspace_bytes(rows, r) -> int:
+    return int(library().lora_bwd_workspace_bytes(rows, r))
+
+
+def lora_bwd(x, dy, A, B, scale, dA=None, dB=None, workspace=None, stream=None):
+    """LoRA adapter gradients of y = scale * B (A x): x [rows][n_in]
+    fp32/bf16, dy [rows][n_out] fp32, A [r][n_in], B [n_out][r] fp32.
+    Returns (dA, dB) fp32."""
+    _req(x, "x", (torch.float32, torch.bfloat16))
+    _req(A, "A", (torch.float32,))
+    r, n_in = A.shape
+    rows = x.numel() // n_in
+    _req(x, "x", (x.dtype,), (rows, n_in))
+    _req(B, "B", (torch.float32,))
+    n_out = B.shape[0]
+    _req(B, "B", (torch.float32,), (n_out, r))
+    _req(dy, "dy", (torch.float32,), (rows, n_out))
+    dA = torch.empty_like(A) if dA is None else dA
+    dB = torch.empty_like(B) if dB is None else dB
+    _req(dA, "dA", (torch.float32,), A.shape)
+    _req(dB, "dB", (torch.float32,), B.shape)
+    need = lora_bwd_workspace_bytes(rows, r)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=x.device)
+    _req(workspace, "workspace", (torch.uint8,))
+    _b.check(library().lora_bwd(_p(x), _DT[x.dtype], _p(dy), _p(A), _p(B), _p(dA), _p(dB), rows, n_in, n_out, r,
+                                float(scale), _p(workspace), workspace.numel(), _s(stream)), "lora_bwd")
+    return dA, dB
 
 
 def attn_bwd_decode(q, k, v, dout, scale=None, rope_base=0.0, q_pos=-1, dq=None, dk=None, dv=None,

@@ -42,6 +42,16 @@ cudaError_t launch_rope_bwd(const float *dy, float *dx, int B, int T, int H, int
 cudaError_t launch_rmsnorm_bwd(const void *x, int x_bf16, const float *gamma, const float *dy, void *dx,
                                int dx_bf16, int rows, int n, float eps, cudaStream_t st);
 
+// Zeroes dgamma, then adds every row's dy x / rms into it; dx may be null.
+cudaError_t launch_rmsnorm_bwd_dgamma(const void *x, int x_bf16, const float *gamma, const float *dy, void *dx,
+                                      int dx_bf16, float *dgamma, int rows, int n, float eps, cudaStream_t st);
+cudaError_t launch_relu2_mul_bwd(const void *gate, const void *up, int bf16, const float *dh, float *dgate,
+                                 float *dup, long long n, cudaStream_t st);
+size_t lora_workspace_bytes(int rows, int r);
+cudaError_t launch_lora_bwd(const void *x, int x_bf16, const float *dy, const float *A, const float *B, float *dA,
+                            float *dB, int rows, int n_in, int n_out, int r, float scale, void *ws,
+                            cudaStream_t st);
+
 // Returns cudaErrorNotSupported (and sets *why) when a shape has no kernel.
 cudaError_t launch_attn_bwd_decode(const float *q, const void *k, const void *v, const float *dout,
                                    float *dq, float *dk, float *dv, int B, int Hq, int Hkv, int S, int D,

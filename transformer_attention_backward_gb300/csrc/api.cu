@@ -279,6 +279,68 @@ abw_status rmsnorm_bwd(const void *x, abw_dtype x_dtype, const float *gamma, con
                    "rmsnorm_bwd");
 }
 
+abw_status rmsnorm_bwd_dgamma(const void *x, abw_dtype x_dtype, const float *gamma, const float *dy, void *dx,
+                              abw_dtype dx_dtype, float *dgamma, int rows, int n, float eps, abw_stream stream) {
+  if (rows < 0 || n < 1) return fail(ABW_EINVAL, "rmsnorm_bwd_dgamma: rows=%d n=%d", rows, n);
+  if ((x_dtype != ABW_F32 && x_dtype != ABW_BF16) || (dx_dtype != ABW_F32 && dx_dtype != ABW_BF16))
+    return fail(ABW_EINVAL, "rmsnorm_bwd_dgamma: bad dtype");
+  if (!(eps >= 0.0f)) return fail(ABW_EINVAL, "rmsnorm_bwd_dgamma: eps must be >= 0");
+  const size_t rn = static_cast<size_t>(rows) * n;
+  Range in[] = {{"x", x, rn * dt_size(x_dtype)},
+                {"gamma", gamma, dx ? static_cast<size_t>(n) * 4 : 0},
+                {"dy", dy, rn * 4}};
+  Range out[] = {{"dgamma", dgamma, static_cast<size_t>(n) * 4}, {"dx", dx, dx ? rn * dt_size(dx_dtype) : 0}};
+  abw_status st = check_buffers("rmsnorm_bwd_dgamma", in, 3, out, 2);
+  if (st != ABW_OK) return st;
+  return from_cuda(abw::launch_rmsnorm_bwd_dgamma(x, x_dtype == ABW_BF16, gamma, dy, dx, dx_dtype == ABW_BF16,
+                                                  dgamma, rows, n, eps, reinterpret_cast<cudaStream_t>(stream)),
+                   "rmsnorm_bwd_dgamma");
+}
+
+abw_status relu2_mul_bwd(const void *gate, const void *up, abw_dtype act_dtype, const float *dh, float *dgate,
+                         float *dup, long long n, abw_stream stream) {
+  if (n < 0) return fail(ABW_EINVAL, "relu2_mul_bwd: n=%lld", n);
+  if (act_dtype != ABW_F32 && act_dtype != ABW_BF16) return fail(ABW_EINVAL, "relu2_mul_bwd: bad dtype");
+  if (n == 0) return ABW_OK;
+  const size_t nb = static_cast<size_t>(n);
+  Range in[] = {{"gate", gate, nb * dt_size(act_dtype)}, {"up", up, nb * dt_size(act_dtype)}, {"dh", dh, nb * 4}};
+  Range out[] = {{"dgate", dgate, nb * 4}, {"dup", dup, nb * 4}};
+  abw_status st = check_buffers("relu2_mul_bwd", in, 3, out, 2);
+  if (st != ABW_OK) return st;
+  return from_cuda(abw::launch_relu2_mul_bwd(gate, up, act_dtype == ABW_BF16, dh, dgate, dup, n,
+                                             reinterpret_cast<cudaStream_t>(stream)),
+                   "relu2_mul_bwd");
+}
+
+size_t lora_bwd_workspace_bytes(int rows, int r) {
+  if (rows < 0 || r < 1) return 0;
+  return abw::lora_workspace_bytes(rows, r);
+}
+
+abw_status lora_bwd(const void *x, abw_dtype x_dtype, const float *dy, const float *A, const float *B, float *dA,
+                    float *dB, int rows, int n_in, int n_out, int r, float scale, void *workspace,
+                    size_t workspace_bytes, abw_stream stream) {
+  if (rows < 0 || n_in < 1 || n_out < 1) return fail(ABW_EINVAL, "lora_bwd: rows=%d n_in=%d n_out=%d", rows, n_in, n_out);
+  if (x_dtype != ABW_F32 && x_dtype != ABW_BF16) return fail(ABW_EINVAL, "lora_bwd: bad dtype");
+  if (r < 1 || r > 16) return fail(ABW_ENOTSUP, "lora_bwd: rank r=%d unsupported (1 <= r <= 16)", r);
+  if (n_in % 4 != 0 || n_out % 4 != 0)
+    return fail(ABW_ENOTSUP, "lora_bwd: n_in=%d, n_out=%d must be multiples of 4", n_in, n_out);
+  if (!(scale == scale)) return fail(ABW_EINVAL, "lora_bwd: scale is NaN");
+  const size_t need = abw::lora_workspace_bytes(rows, r);
+  if (workspace == nullptr || workspace_bytes < need)
+    return fail(ABW_EWORKSPACE, "lora_bwd: workspace %zu bytes at %p, need %zu", workspace_bytes, workspace, need);
+  const size_t rb = static_cast<size_t>(rows);
+  Range in[] = {{"x", x, rb * n_in * dt_size(x_dtype)}, {"dy", dy, rb * n_out * 4},
+                {"A", A, static_cast<size_t>(r) * n_in * 4}, {"B", B, static_cast<size_t>(n_out) * r * 4}};
+  Range out[] = {{"dA", dA, static_cast<size_t>(r) * n_in * 4}, {"dB", dB, static_cast<size_t>(n_out) * r * 4},
+                 {"workspace", workspace, need}};
+  abw_status st = check_buffers("lora_bwd", in, 4, out, 3);
+  if (st != ABW_OK) return st;
+  return from_cuda(abw::launch_lora_bwd(x, x_dtype == ABW_BF16, dy, A, B, dA, dB, rows, n_in, n_out, r, scale,
+                                        workspace, reinterpret_cast<cudaStream_t>(stream)),
+                   "lora_bwd");
+}
+
 abw_status attn_bwd_decode(const float *q, const void *k, const void *v, const float *dout, float *dq, float *dk,
                            float *dv, int B, int Hq, int Hkv, int S, int D, abw_dtype kv_dtype, float scale,
                            float rope_base, int q_pos, abw_stream stream) {

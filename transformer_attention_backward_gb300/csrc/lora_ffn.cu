@@ -1,0 +1,298 @@
+// The steps of the layer backward around the attention backward, all bound
+// by HBM bandwidth:
+//
+//   relu2_mul_bwd : the FFN's gated activation hidden = ReLU(gate)^2 * up
+//                   (Hesper pull request #1, FFN-backward commit, "ReLU^2 x
+//                   Mul backward"): dGate = dH up 2 ReLU(gate),
+//                   dUp = dH ReLU(gate)^2, element by element.
+//   lora_bwd      : parameter gradients of a rank-r adapter y = s B (A x) on
+//                   a projection (pull request #1: the chain ends "RoPE
+//                   backward -> dQ -> LoRA backward", with the adapter's
+//                   input the layer's saved normed activations):
+//                   h = x A^T, dB = s dy^T h, dh = s dy B, dA = dh^T x.
+//
+// The adapter products have rank r <= 16, so they are skinny: per row of x
+// and dy the work is r dot products, and the whole step is a stream over x
+// and dy.  Two kernels: a row pass forms h and dh (r values per row each,
+// into the caller's workspace) and zeroes dA / dB; a column pass adds each
+// chunk of rows' outer-product sums into dA and dB with vector reductions.
+// x and dy are read twice; the second read comes from L2 for the chain's
+// shapes (1024 rows of 2560).
+#include "abw_host.h"
+
+namespace abw {
+namespace {
+
+// ----------------------------------------------------------------- ReLU^2 x Mul
+__device__ __forceinline__ float4 ld_cs_f4(const float *p) {
+  float4 v;
+  asm volatile("ld.global.cs.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "l"(p));
+  return v;
+}
+
+template <bool BF16>
+__device__ __forceinline__ float4 ld_act4(const void *p, long long i4) {
+  if (BF16) {
+    uint2 u;
+    asm volatile("ld.global.cs.v2.u32 {%0, %1}, [%2];"
+                 : "=r"(u.x), "=r"(u.y)
+                 : "l"(reinterpret_cast<const uint2 *>(p) + i4));
+    return make_float4(bf16_lo(u.x), bf16_hi(u.x), bf16_lo(u.y), bf16_hi(u.y));
+  } else {
+    return ld_cs_f4(reinterpret_cast<const float *>(p) + 4 * i4);
+  }
+}
+
+template <bool BF16>
+__device__ __forceinline__ float ld_act1(const void *p, long long i) {
+  return BF16 ? __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(p)[i]) : reinterpret_cast<const float *>(p)[i];
+}
+
+// grid-stride over groups of four elements; the (n % 4) tail by block 0
+template <bool BF16>
+__global__ void __launch_bounds__(256) relu2_mul_bwd_kernel(const void *__restrict__ gate, const void *__restrict__ up,
+                                                            const float *__restrict__ dh, float *__restrict__ dgate,
+                                                            float *__restrict__ dup, long long n) {
+  const long long n4 = n >> 2;
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4; i += stride) {
+    const float4 g = ld_act4<BF16>(gate, i), u = ld_act4<BF16>(up, i), d = ld_cs_f4(dh + 4 * i);
+    const float rx = fmaxf(g.x, 0.f), ry = fmaxf(g.y, 0.f), rz = fmaxf(g.z, 0.f), rw = fmaxf(g.w, 0.f);
+    st_cs_f4(dgate + 4 * i, make_float4(2.f * d.x * u.x * rx, 2.f * d.y * u.y * ry, 2.f * d.z * u.z * rz,
+                                        2.f * d.w * u.w * rw));
+    st_cs_f4(dup + 4 * i, make_float4(d.x * rx * rx, d.y * ry * ry, d.z * rz * rz, d.w * rw * rw));
+  }
+  if (blockIdx.x == 0) {
+    const long long e = 4 * n4 + threadIdx.x;
+    if (e < n) {
+      const float g = ld_act1<BF16>(gate, e), u = ld_act1<BF16>(up, e), d = dh[e];
+      const float r = fmaxf(g, 0.f);
+      dgate[e] = 2.f * d * u * r;
+      dup[e] = d * r * r;
+    }
+  }
+}
+
+// ----------------------------------------------------------------- LoRA
+constexpr int kLoraRows = 4;     // rows per block of the row pass
+constexpr int kLoraChunk = 32;   // rows per block of the column pass
+
+template <bool XBF16>
+__device__ __forceinline__ float4 ldg_x4(const void *x, size_t i4) {
+  if (XBF16) {
+    const uint2 u = __ldg(reinterpret_cast<const uint2 *>(x) + i4);
+    return make_float4(bf16_lo(u.x), bf16_hi(u.x), bf16_lo(u.y), bf16_hi(u.y));
+  } else {
+    return __ldg(reinterpret_cast<const float4 *>(x) + i4);
+  }
+}
+
+// Row pass: block b takes rows kLoraRows b .. + kLoraRows - 1 and writes
+// h[t][j] = x_t . A_j and dh[t][j] = s dy_t . B[:, j] (j < r) to the
+// workspace; every thread also zeroes its share of dA and dB.
+template <bool XBF16, int RK>
+__global__ void __launch_bounds__(256) lora_rows_kernel(const void *__restrict__ x, const float *__restrict__ dy,
+                                                        const float *__restrict__ A, const float *__restrict__ B,
+                                                        float *__restrict__ h, float *__restrict__ dh,
+                                                        float *__restrict__ dA, float *__restrict__ dB, int rows,
+                                                        int n_in, int n_out, int r, float scale) {
+  __shared__ float red[8][2 * kLoraRows * RK];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  {
+    const long long nz = static_cast<long long>(r) * (n_in + n_out);
+    const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+    for (long long e = static_cast<long long>(blockIdx.x) * blockDim.x + tid; e < nz; e += stride) {
+      if (e < static_cast<long long>(r) * n_in)
+        dA[e] = 0.f;
+      else
+        dB[e - static_cast<long long>(r) * n_in] = 0.f;
+    }
+  }
+  const int t0 = blockIdx.x * kLoraRows;
+  float acc[kLoraRows][RK], acc2[kLoraRows][RK];
+#pragma unroll
+  for (int t = 0; t < kLoraRows; ++t)
+#pragma unroll
+    for (int j = 0; j < RK; ++j) acc[t][j] = acc2[t][j] = 0.f;
+  // h: four input columns per step
+  const int c4 = n_in >> 2;
+  for (int c = tid; c < c4; c += 256) {
+    float4 a[RK];
+#pragma unroll
+    for (int j = 0; j < RK; ++j)
+      a[j] = j < r ? __ldg(reinterpret_cast<const float4 *>(A + static_cast<size_t>(j) * n_in) + c)
+                   : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int t = 0; t < kLoraRows; ++t) {
+      if (t0 + t < rows) {
+        const float4 xv = ldg_x4<XBF16>(x, static_cast<size_t>(t0 + t) * c4 + c);
+#pragma unroll
+        for (int j = 0; j < RK; ++j) acc[t][j] += xv.x * a[j].x + xv.y * a[j].y + xv.z * a[j].z + xv.w * a[j].w;
+      }
+    }
+  }
+  // dh: one output column per step (B row o holds its r rank entries)
+  for (int o = tid; o < n_out; o += 256) {
+    float bo[RK];
+#pragma unroll
+    for (int j = 0; j < RK; ++j) bo[j] = j < r ? __ldg(B + static_cast<size_t>(o) * r + j) : 0.f;
+#pragma unroll
+    for (int t = 0; t < kLoraRows; ++t) {
+      if (t0 + t < rows) {
+        const float d = __ldg(dy + static_cast<size_t>(t0 + t) * n_out + o);
+#pragma unroll
+        for (int j = 0; j < RK; ++j) acc2[t][j] = fmaf(d, bo[j], acc2[t][j]);
+      }
+    }
+  }
+#pragma unroll
+  for (int t = 0; t < kLoraRows; ++t)
+#pragma unroll
+    for (int j = 0; j < RK; ++j) {
+      const float s1 = warp_sum(acc[t][j]), s2 = warp_sum(acc2[t][j]);
+      if (lane == 0) {
+        red[warp][t * RK + j] = s1;
+        red[warp][kLoraRows * RK + t * RK + j] = s2;
+      }
+    }
+  __syncthreads();
+  if (tid < 2 * kLoraRows * RK) {
+    float s = 0.f;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) s += red[w][tid];
+    const int second = tid >= kLoraRows * RK;
+    const int k = second ? tid - kLoraRows * RK : tid;
+    const int t = k / RK, j = k % RK;
+    if (t0 + t < rows && j < r) {
+      if (second)
+        dh[static_cast<size_t>(t0 + t) * r + j] = scale * s;
+      else
+        h[static_cast<size_t>(t0 + t) * r + j] = s;
+    }
+  }
+}
+
+// Column pass: block (tile, chunk) covers 256 groups of four columns (of dA's
+// n_in, then of dB's n_out) over kLoraChunk rows and adds its partial sums
+//   dA[j][i] += sum_t dh[t][j] x[t][i],   dB[o][j] += s sum_t dy[t][o] h[t][j].
+template <bool XBF16, int RK>
+__global__ void __launch_bounds__(256) lora_cols_kernel(const void *__restrict__ x, const float *__restrict__ dy,
+                                                        const float *__restrict__ h, const float *__restrict__ dh,
+                                                        float *__restrict__ dA, float *__restrict__ dB, int rows,
+                                                        int n_in, int n_out, int r, float scale) {
+  __shared__ float hs[kLoraChunk][RK], dhs[kLoraChunk][RK];
+  const int tid = threadIdx.x;
+  const int r0 = blockIdx.y * kLoraChunk;
+  const int nr = min(kLoraChunk, rows - r0);
+  for (int e = tid; e < kLoraChunk * RK; e += 256) {
+    const int t = e / RK, j = e % RK;
+    const bool on = t < nr && j < r;
+    hs[t][j] = on ? h[static_cast<size_t>(r0 + t) * r + j] : 0.f;
+    dhs[t][j] = on ? dh[static_cast<size_t>(r0 + t) * r + j] : 0.f;
+  }
+  __syncthreads();
+  const int in4 = n_in >> 2, out4 = n_out >> 2;
+  const int c = blockIdx.x * 256 + tid;
+  if (c < in4) {
+    float4 acc[RK];
+#pragma unroll
+    for (int j = 0; j < RK; ++j) acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int t = 0; t < nr; ++t) {
+      const float4 xv = ldg_x4<XBF16>(x, static_cast<size_t>(r0 + t) * in4 + c);
+#pragma unroll
+      for (int j = 0; j < RK; ++j) {
+        const float w = dhs[t][j];
+        acc[j].x = fmaf(w, xv.x, acc[j].x);
+        acc[j].y = fmaf(w, xv.y, acc[j].y);
+        acc[j].z = fmaf(w, xv.z, acc[j].z);
+        acc[j].w = fmaf(w, xv.w, acc[j].w);
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < RK; ++j)
+      if (j < r) red_add_f4(dA + static_cast<size_t>(j) * n_in + 4 * c, acc[j]);
+  } else if (c < in4 + out4) {
+    const int o4 = c - in4;
+    float acc[4][RK];
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+#pragma unroll
+      for (int j = 0; j < RK; ++j) acc[e][j] = 0.f;
+    for (int t = 0; t < nr; ++t) {
+      const float4 d = __ldg(reinterpret_cast<const float4 *>(dy + static_cast<size_t>(r0 + t) * n_out) + o4);
+#pragma unroll
+      for (int j = 0; j < RK; ++j) {
+        const float w = hs[t][j];
+        acc[0][j] = fmaf(d.x, w, acc[0][j]);
+        acc[1][j] = fmaf(d.y, w, acc[1][j]);
+        acc[2][j] = fmaf(d.z, w, acc[2][j]);
+        acc[3][j] = fmaf(d.w, w, acc[3][j]);
+      }
+    }
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      float *row = dB + static_cast<size_t>(4 * o4 + e) * r;
+      if ((r & 3) == 0) {
+#pragma unroll
+        for (int j = 0; j < RK; j += 4)
+          if (j < r)
+            red_add_f4(row + j, make_float4(scale * acc[e][j], scale * acc[e][j + 1], scale * acc[e][j + 2],
+                                            scale * acc[e][j + 3]));
+      } else {
+#pragma unroll
+        for (int j = 0; j < RK; ++j)
+          if (j < r) atomicAdd(row + j, scale * acc[e][j]);
+      }
+    }
+  }
+}
+
+template <bool XB, int RK>
+cudaError_t lora_launch(const void *x, const float *dy, const float *A, const float *B, float *dA, float *dB,
+                        float *h, float *dh, int rows, int n_in, int n_out, int r, float scale, cudaStream_t st) {
+  const int rblocks = rows > 0 ? (rows + kLoraRows - 1) / kLoraRows : 1;
+  lora_rows_kernel<XB, RK><<<rblocks, 256, 0, st>>>(x, dy, A, B, h, dh, dA, dB, rows, n_in, n_out, r, scale);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess || rows == 0) return e;
+  const int tiles = ((n_in >> 2) + (n_out >> 2) + 255) / 256;
+  const dim3 grid(tiles, (rows + kLoraChunk - 1) / kLoraChunk);
+  lora_cols_kernel<XB, RK><<<grid, 256, 0, st>>>(x, dy, h, dh, dA, dB, rows, n_in, n_out, r, scale);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_relu2_mul_bwd(const void *gate, const void *up, int bf16, const float *dh, float *dgate,
+                                 float *dup, long long n, cudaStream_t st) {
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  const long long groups = (n + 3) / 4;
+  long long blocks = (groups + 255) / 256;
+  blocks = blocks < 1 ? 1 : blocks;
+  if (blocks > 8LL * sms) blocks = 8LL * sms;   // 2048 threads per SM, each looping
+  if (bf16)
+    relu2_mul_bwd_kernel<true><<<static_cast<unsigned>(blocks), 256, 0, st>>>(gate, up, dh, dgate, dup, n);
+  else
+    relu2_mul_bwd_kernel<false><<<static_cast<unsigned>(blocks), 256, 0, st>>>(gate, up, dh, dgate, dup, n);
+  return cudaGetLastError();
+}
+
+size_t lora_workspace_bytes(int rows, int r) { return static_cast<size_t>(rows) * r * 2 * 4 + 256; }
+
+cudaError_t launch_lora_bwd(const void *x, int x_bf16, const float *dy, const float *A, const float *B, float *dA,
+                            float *dB, int rows, int n_in, int n_out, int r, float scale, void *ws,
+                            cudaStream_t st) {
+  char *p = static_cast<char *>(ws);
+  p += (256 - (reinterpret_cast<uintptr_t>(p) & 255)) & 255;
+  float *h = reinterpret_cast<float *>(p);
+  float *dh = h + static_cast<size_t>(rows) * r;
+  if (r <= 8)
+    return x_bf16 ? lora_launch<true, 8>(x, dy, A, B, dA, dB, h, dh, rows, n_in, n_out, r, scale, st)
+                  : lora_launch<false, 8>(x, dy, A, B, dA, dB, h, dh, rows, n_in, n_out, r, scale, st);
+  return x_bf16 ? lora_launch<true, 16>(x, dy, A, B, dA, dB, h, dh, rows, n_in, n_out, r, scale, st)
+                : lora_launch<false, 16>(x, dy, A, B, dA, dB, h, dh, rows, n_in, n_out, r, scale, st);
+}
+
+}  // namespace abw

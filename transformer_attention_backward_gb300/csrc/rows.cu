@@ -3,6 +3,9 @@
 //
 //   softmax_bwd : softmaxBackward, "Hesper.Training.VerifiedBackward" section Softmax
 //   rope_bwd    : ropeBackward, section RoPE (rotation by -theta)
+//   rmsnorm_bwd_dgamma : the same plus the scale gradient dgamma = sum over
+//                 rows of dy x / rms (the forward y = gamma x / rms is linear
+//                 in gamma; the norm's other gradient)
 //   rmsnorm_bwd : rmsNormBackward, section RMSNorm; the two row reductions the
 //                 Hesper WGSL kernel runs as separate shared-memory phases
 //                 ("RMSNorm backward kernel" fix, Hesper pull request #1) are
@@ -275,6 +278,143 @@ cudaError_t rms_dispatch(const void *x, const float *g, const float *dy, void *d
 }
 
 // ---------------------------------------------------------------------------
+// RMSNorm backward with the scale gradient: dx as above (optional) and
+// dgamma_i = sum over rows of dy_i x_i / rms.  Blocks stride over the rows;
+// each thread keeps its columns' dgamma partial sums in registers across its
+// block's rows and adds them into the zeroed output once, with 16-byte
+// vector reductions.
+// ---------------------------------------------------------------------------
+template <bool XBF16, bool DXBF16, int NV, bool DX>
+__global__ void __launch_bounds__(kRowThreads) rmsnorm_bwd_dgamma_v4(const void *__restrict__ x,
+                                                                     const float *__restrict__ gamma,
+                                                                     const float *__restrict__ dy,
+                                                                     void *__restrict__ dx, float *__restrict__ dgamma,
+                                                                     int rows, int n, float eps) {
+  __shared__ float2 red[kRowThreads / 32 + 1];
+  const int n4 = n >> 2;
+  float4 gv[NV], ga[NV];
+#pragma unroll
+  for (int k = 0; k < NV; ++k) {
+    const int i = threadIdx.x + kRowThreads * k;
+    gv[k] = (DX && i < n4) ? __ldg(reinterpret_cast<const float4 *>(gamma) + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+    ga[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  for (int row = blockIdx.x; row < rows; row += gridDim.x) {
+    const size_t rb = static_cast<size_t>(row) * n4;
+    float4 xv[NV], dv[NV];
+    float ss = 0.f, cs = 0.f;
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+      const int i = threadIdx.x + kRowThreads * k;
+      if (i < n4) {
+        xv[k] = load_x4<XBF16>(x, rb + i);
+        dv[k] = __ldg(reinterpret_cast<const float4 *>(dy) + rb + i);
+        ss += xv[k].x * xv[k].x + xv[k].y * xv[k].y + xv[k].z * xv[k].z + xv[k].w * xv[k].w;
+        if (DX)
+          cs += dv[k].x * gv[k].x * xv[k].x + dv[k].y * gv[k].y * xv[k].y + dv[k].z * gv[k].z * xv[k].z +
+                dv[k].w * gv[k].w * xv[k].w;
+      }
+    }
+    const float2 sums = block_sum2(ss, cs, red);
+    const float ms = sums.x / static_cast<float>(n) + eps;   // rms^2
+    const float inv_rms = rsqrtf(ms);
+    const float coef = sums.y / (static_cast<float>(n) * ms);
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+      const int i = threadIdx.x + kRowThreads * k;
+      if (i < n4) {
+        ga[k].x = fmaf(dv[k].x * xv[k].x, inv_rms, ga[k].x);
+        ga[k].y = fmaf(dv[k].y * xv[k].y, inv_rms, ga[k].y);
+        ga[k].z = fmaf(dv[k].z * xv[k].z, inv_rms, ga[k].z);
+        ga[k].w = fmaf(dv[k].w * xv[k].w, inv_rms, ga[k].w);
+        if (DX) {
+          float4 r;
+          r.x = (dv[k].x * gv[k].x - xv[k].x * coef) * inv_rms;
+          r.y = (dv[k].y * gv[k].y - xv[k].y * coef) * inv_rms;
+          r.z = (dv[k].z * gv[k].z - xv[k].z * coef) * inv_rms;
+          r.w = (dv[k].w * gv[k].w - xv[k].w * coef) * inv_rms;
+          store_dx4<DXBF16>(dx, rb + i, r);
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < NV; ++k) {
+    const int i = threadIdx.x + kRowThreads * k;
+    if (i < n4 && blockIdx.x < rows) red_add_f4(dgamma + 4 * i, ga[k]);
+  }
+}
+
+// Any n: one block per row in turn, per-element reductions into dgamma.
+template <bool XBF16, bool DXBF16>
+__global__ void __launch_bounds__(kRowThreads) rmsnorm_bwd_dgamma_any(const void *__restrict__ x,
+                                                                      const float *__restrict__ gamma,
+                                                                      const float *__restrict__ dy,
+                                                                      void *__restrict__ dx,
+                                                                      float *__restrict__ dgamma, int rows, int n,
+                                                                      float eps) {
+  __shared__ float2 red[kRowThreads / 32 + 1];
+  auto ldx = [&](size_t i) -> float {
+    return XBF16 ? __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(x)[i])
+                 : reinterpret_cast<const float *>(x)[i];
+  };
+  for (int row = blockIdx.x; row < rows; row += gridDim.x) {
+    const size_t rb = static_cast<size_t>(row) * n;
+    float ss = 0.f, cs = 0.f;
+    for (int i = threadIdx.x; i < n; i += kRowThreads) {
+      const float xi = ldx(rb + i);
+      ss += xi * xi;
+      if (dx) cs += dy[rb + i] * gamma[i] * xi;
+    }
+    const float2 sums = block_sum2(ss, cs, red);
+    const float ms = sums.x / static_cast<float>(n) + eps;
+    const float inv_rms = rsqrtf(ms);
+    const float coef = sums.y / (static_cast<float>(n) * ms);
+    for (int i = threadIdx.x; i < n; i += kRowThreads) {
+      const float xi = ldx(rb + i), d = dy[rb + i];
+      atomicAdd(dgamma + i, d * xi * inv_rms);
+      if (dx) {
+        const float r = (d * gamma[i] - xi * coef) * inv_rms;
+        if (DXBF16)
+          reinterpret_cast<__nv_bfloat16 *>(dx)[rb + i] = __float2bfloat16_rn(r);
+        else
+          reinterpret_cast<float *>(dx)[rb + i] = r;
+      }
+    }
+  }
+}
+
+template <bool XB, bool DB, int NV>
+void rms_dg_launch(int grid, const void *x, const float *g, const float *dy, void *dx, float *dgamma, int rows, int n,
+                   float eps, cudaStream_t st) {
+  if (dx)
+    rmsnorm_bwd_dgamma_v4<XB, DB, NV, true><<<grid, kRowThreads, 0, st>>>(x, g, dy, dx, dgamma, rows, n, eps);
+  else
+    rmsnorm_bwd_dgamma_v4<XB, DB, NV, false><<<grid, kRowThreads, 0, st>>>(x, g, dy, dx, dgamma, rows, n, eps);
+}
+
+template <bool XB, bool DB>
+cudaError_t rms_dg_dispatch(const void *x, const float *g, const float *dy, void *dx, float *dgamma, int rows, int n,
+                            float eps, int sms, cudaStream_t st) {
+  const int n4 = n / 4;
+  const int nv = (n4 + kRowThreads - 1) / kRowThreads;
+  const int grid = rows < 4 * sms ? rows : 4 * sms;
+  if (n % 4 != 0 || nv > 8)
+    rmsnorm_bwd_dgamma_any<XB, DB><<<grid, kRowThreads, 0, st>>>(x, g, dy, dx, dgamma, rows, n, eps);
+  else if (nv <= 1)
+    rms_dg_launch<XB, DB, 1>(grid, x, g, dy, dx, dgamma, rows, n, eps, st);
+  else if (nv <= 2)
+    rms_dg_launch<XB, DB, 2>(grid, x, g, dy, dx, dgamma, rows, n, eps, st);
+  else if (nv <= 3)
+    rms_dg_launch<XB, DB, 3>(grid, x, g, dy, dx, dgamma, rows, n, eps, st);
+  else if (nv <= 4)
+    rms_dg_launch<XB, DB, 4>(grid, x, g, dy, dx, dgamma, rows, n, eps, st);
+  else
+    rms_dg_launch<XB, DB, 8>(grid, x, g, dy, dx, dgamma, rows, n, eps, st);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
 // Self test of the bounded wait: a barrier that expects one arrival which
 // never comes.
 // ---------------------------------------------------------------------------
@@ -337,6 +477,20 @@ cudaError_t launch_rmsnorm_bwd(const void *x, int x_bf16, const float *gamma, co
   if (x_bf16) return rms_dispatch<true, false>(x, gamma, dy, dx, rows, n, eps, st);
   if (dx_bf16) return rms_dispatch<false, true>(x, gamma, dy, dx, rows, n, eps, st);
   return rms_dispatch<false, false>(x, gamma, dy, dx, rows, n, eps, st);
+}
+
+cudaError_t launch_rmsnorm_bwd_dgamma(const void *x, int x_bf16, const float *gamma, const float *dy, void *dx,
+                                      int dx_bf16, float *dgamma, int rows, int n, float eps, cudaStream_t st) {
+  cudaError_t e = cudaMemsetAsync(dgamma, 0, static_cast<size_t>(n) * 4, st);
+  if (e != cudaSuccess || rows == 0) return e;
+  int dev = 0, sms = 0;
+  e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  if (x_bf16 && dx_bf16) return rms_dg_dispatch<true, true>(x, gamma, dy, dx, dgamma, rows, n, eps, sms, st);
+  if (x_bf16) return rms_dg_dispatch<true, false>(x, gamma, dy, dx, dgamma, rows, n, eps, sms, st);
+  if (dx_bf16) return rms_dg_dispatch<false, true>(x, gamma, dy, dx, dgamma, rows, n, eps, sms, st);
+  return rms_dg_dispatch<false, false>(x, gamma, dy, dx, dgamma, rows, n, eps, sms, st);
 }
 
 cudaError_t launch_selftest_wait(const WaitCtl &w, cudaStream_t st) {
