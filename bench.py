@@ -357,7 +357,7 @@ def recorded_traffic(kernel_key, src_files):
     return e.get("dram_bytes_per_launch")
 
 
-def run_chain(abw, saved_forward, W, dev, stream, args, barrier, max_over_ranks, world, local):
+def run_chain(abw, W, dev, stream, args, barrier, max_over_ranks, world, local):
     """The 30-layer backward chain (GQA 20/5, B=2, T=512, hidden 2560): per
     layer, in reverse, RMSNorm backward of the saved normed input (bf16 dx is
     attention's dOut), then causal attention backward with RoPE on dq/dk.
@@ -370,7 +370,7 @@ def run_chain(abw, saved_forward, W, dev, stream, args, barrier, max_over_ranks,
     for layer in range(L):
         inp = W.chain_layer_inputs(layer)
         g = {k: v.to(dev) for k, v in inp.items() if torch.is_tensor(v)}
-        o, lse = saved_forward.causal_forward(g["q"], g["k"], g["v"], shape.scale)
+        o, lse = abw.attn_fwd_causal(g["q"], g["k"], g["v"], shape.scale)
         g.update(o=o, lse=lse, eps=inp["eps"],
                  dx=torch.empty(g["x"].shape, dtype=torch.bfloat16, device=dev),
                  dq=torch.empty(g["q"].shape, dtype=torch.float32, device=dev),
@@ -486,13 +486,13 @@ def causal_kernel_figures(bd, shape, peaks, kind):
     return out
 
 
-def run_causal(abw, saved_forward, W, cs, seed, name, dev, stream, args, barrier, max_over_ranks, world, local):
+def run_causal(abw, W, cs, seed, name, dev, stream, args, barrier, max_over_ranks, world, local):
     """One causal backward call per step (prep, dK/dV and dQ kernels), CUDA
     events around the K calls, clocks sampled meanwhile; per-kernel times
     from a separate profiled call."""
     import torch
     cin = {k: v.to(dev) for k, v in W.causal_inputs(cs, seed=seed).items()}
-    o, lse = saved_forward.causal_forward(cin["q"], cin["k"], cin["v"], cs.scale)
+    o, lse = abw.attn_fwd_causal(cin["q"], cin["k"], cin["v"], cs.scale)
     cq = torch.empty(cin["q"].shape, dtype=torch.float32, device=dev)
     ck = torch.empty(cin["k"].shape, dtype=torch.float32, device=dev)
     cv = torch.empty_like(ck)
@@ -529,6 +529,27 @@ def run_causal(abw, saved_forward, W, cs, seed, name, dev, stream, args, barrier
     io = causal_io_bytes(cs.B, cs.T, cs.Hq, cs.Hkv, cs.D)
     bd = kernel_breakdown(cstep)
     abw.device_check(stream)
+    # the forward that produced O and lse, timed the same way (two products
+    # over the causal half: 2 B H T^2 D flops)
+    fo, fl = torch.empty_like(o), torch.empty_like(lse)
+
+    def fstep():
+        abw.attn_fwd_causal(cin["q"], cin["k"], cin["v"], cs.scale, o=fo, lse=fl, stream=stream)
+
+    for _ in range(args.warmup):
+        fstep()
+    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    f0.record(stream)
+    for _ in range(csteps):
+        fstep()
+    f1.record(stream)
+    torch.cuda.synchronize()
+    abw.device_check(stream)
+    fms = max_over_ranks(f0.elapsed_time(f1)) / csteps
+    ftf = 2.0 * cs.B * cs.Hq * cs.T * cs.T * cs.D / (fms * 1e-3) / 1e12
+    forward = {"kernel": "causal_fwd_kernel", "ms_per_call": round(fms, 4), "tflops": round(ftf, 1),
+               **fractions(ftf, "bf16_tflops", peaks, kind + " (burst)")}
+    del fo, fl
     out = {"workload": name, "value": round(ctf, 3), "unit": "TFLOP/s", "ms_per_call": round(cms, 4),
            "flops_per_call": flops,
            "l2": f"no flush: one call reads {io_in_mb(cs)} MB of inputs and writes {io_out_mb(cs)} MB of outputs, "
@@ -540,6 +561,7 @@ def run_causal(abw, saved_forward, W, cs, seed, name, dev, stream, args, barrier
                                                     ["causal.cu", "abw_device.cuh", "tcgen05.cuh"]),
                         "traffic_kernel": "causal_kv_tc_kernel", "scope": "whole call"},
            "kernels": causal_kernel_figures(bd, cs, peaks, kind),
+           "forward": forward,
            "clocks": cclocks.summary(ch0, ch1)}
     del cin, o, lse, cq, ck, cv, ws
     torch.cuda.empty_cache()
@@ -708,7 +730,6 @@ def run_native(args):
     dev = torch.device("cuda", local)
 
     import transformer_attention_backward_gb300 as abw
-    from transformer_attention_backward_gb300 import saved_forward
     from transformer_attention_backward_gb300 import workloads as W
     lib = abw.library()
     stream = torch.cuda.current_stream()
@@ -865,10 +886,10 @@ def run_native(args):
     # ------------------------------------------------------------ causal T = 2048 and T = 8192
     causal, causal_long = None, None
     if not args.skip_causal:
-        causal = run_causal(abw, saved_forward, W, W.CAUSAL_2K, W.SEED_BASE + 3,
+        causal = run_causal(abw, W, W.CAUSAL_2K, W.SEED_BASE + 3,
                             "causal_b4_h20_d128_t2048_bf16_rope1e4", dev, stream, args, barrier, max_over_ranks,
                             world, local)
-        causal_long = run_causal(abw, saved_forward, W, W.CAUSAL_8K, W.SEED_BASE + 4,
+        causal_long = run_causal(abw, W, W.CAUSAL_8K, W.SEED_BASE + 4,
                                  "causal_b1_h32_d128_t8192_bf16_qkx4", dev, stream, args, barrier, max_over_ranks,
                                  world, local)
 
@@ -879,7 +900,7 @@ def run_native(args):
     # ------------------------------------------------------------ 30-layer chain
     chain = None
     if not args.skip_chain:
-        chain = run_chain(abw, saved_forward, W, dev, stream, args, barrier, max_over_ranks, world, local)
+        chain = run_chain(abw, W, dev, stream, args, barrier, max_over_ranks, world, local)
         torch.cuda.empty_cache()
 
     peaks, kind = load_peaks()

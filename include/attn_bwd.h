@@ -18,6 +18,8 @@
  *                    probabilities from the saved log-sum-exp; RoPE backward fused on
  *                    dq and dk (DaisyChain-Train transformer.js, backward(): dV = A^T dctx,
  *                    dA = dctx V^T, dS = A (dA - sum A dA), dQ = dS K, dK = dS^T Q)
+ *   attn_bwd_causal_saved_p  the same from the saved attention weights (PR #1 softmax fix)
+ *   attn_fwd_causal  the forward whose O and log-sum-exp attn_bwd_causal consumes
  *   rmsnorm_bwd_dgamma  rmsnorm_bwd plus dgamma = sum_rows dy x / rms
  *   relu2_mul_bwd    dgate = dh up 2 ReLU(gate), dup = dh ReLU(gate)^2  (PR #1, FFN backward)
  *   lora_bwd         dA, dB of y = s B A x                             (PR #1, LoRA backward)
@@ -203,6 +205,22 @@ abw_status attn_bwd_decode(const float *q, const void *k, const void *v, const f
                            float scale, float rope_base, int q_pos, abw_stream stream);
 
 /*
+ * attn_fwd_causal -- the causal attention forward that produces the
+ * activations attn_bwd_causal consumes: online-softmax attention (Hesper
+ * pull request #1, FlashAttention commits: flashAttentionSpec, equal to the
+ * three-step standardAttention) under the causal mask (keys j <= query i):
+ *   s_ij = scale q_i . k_j,  lse_i = log sum_{j<=i} exp(s_ij),
+ *   o_i = sum_{j<=i} exp(s_ij - lse_i) v_j
+ *   q [B][T][Hq][D] bf16;  k, v [B][T][Hkv][D] bf16 (query head h reads KV
+ *   head h / (Hq / Hkv))
+ *   o [B][T][Hq][D] bf16 (rounded from fp32);  lse [B][Hq][T] f32, natural log
+ * The probabilities enter the o product rounded to bf16; sums are fp32.
+ * Supported: D == 128; T >= 1; Hq % Hkv == 0.
+ */
+abw_status attn_fwd_causal(const void *q, const void *k, const void *v, void *o, float *lse,
+                           int B, int T, int Hq, int Hkv, int D, float scale, abw_stream stream);
+
+/*
  * attn_bwd_causal_workspace_bytes -- workspace size attn_bwd_causal needs for
  * these sizes, with Tp = T rounded up to 128 and nb = Tp / 128: delta and
  * lse * log2(e), each f32 [B][Hq][Tp]; the RoPE table [T][D/2] of
@@ -233,6 +251,28 @@ abw_status attn_bwd_causal(const void *q, const void *k, const void *v, const vo
                            int B, int T, int Hq, int Hkv, int D, float scale,
                            float rope_base, int pos0,
                            void *workspace, size_t workspace_bytes, abw_stream stream);
+
+/*
+ * attn_bwd_causal_saved_p -- attn_bwd_causal reading the attention weights
+ * the forward saved instead of recomputing them from the log-sum-exp: the
+ * form of Hesper pull request #1's softmax-backward fix ("save per-layer
+ * attention weights ... use saved attnBuf": dScores = attn (dAttn -
+ * sum attn dAttn)) and of transformer.js backward(), which reads the cached
+ * attention A.
+ *   p_attn [B][Hq][T][T] bf16  the softmax output, row = query i, column =
+ *          key j; entries with j > i are not read (the causal mask makes
+ *          them 0)
+ *   o      [B][T][Hq][D] bf16  the forward's output, for
+ *          delta_i = sum_j P_ij dP_ij = dout_i . o_i (the identity holds
+ *          because o = P v)
+ *   everything else as attn_bwd_causal (no lse), with the same workspace
+ *   size (attn_bwd_causal_workspace_bytes).
+ */
+abw_status attn_bwd_causal_saved_p(const void *q, const void *k, const void *v, const void *p_attn,
+                                   const void *o, const void *dout, float *dq, float *dk, float *dv,
+                                   int B, int T, int Hq, int Hkv, int D, float scale,
+                                   float rope_base, int pos0, void *workspace, size_t workspace_bytes,
+                                   abw_stream stream);
 
 /*
  * attn_bwd_causal_noalloc -- attn_bwd_causal for callers that cannot allocate

@@ -10,7 +10,6 @@ import torch
 
 import oracle as O
 from tests.helpers import TOL_BF16, checked, max_rel_err, to_np
-from transformer_attention_backward_gb300 import saved_forward
 from transformer_attention_backward_gb300 import workloads as W
 
 pytestmark = pytest.mark.gpu
@@ -25,7 +24,7 @@ def abw():
 
 def gpu_causal(abw, inp, shape):
     g = {k: v.cuda() for k, v in inp.items()}
-    o, lse = saved_forward.causal_forward(g["q"], g["k"], g["v"], shape.scale)
+    o, lse = abw.attn_fwd_causal(g["q"], g["k"], g["v"], shape.scale)
     dq, dk, dv = abw.attn_bwd_causal(g["q"], g["k"], g["v"], o, g["dout"], lse, shape.scale,
                                      shape.rope_base, shape.pos0)
     abw.device_check()
@@ -96,7 +95,7 @@ def test_chain_30_layers_sampled(abw):
         g = {k: v.cuda() for k, v in inp.items() if torch.is_tensor(v)}
         dx = abw.rmsnorm_bwd(g["x"], g["gamma"], dh_g, eps=inp["eps"], dx_dtype=torch.bfloat16)
         dout = dx.view(shape.B, shape.T, shape.Hq, shape.D)
-        o, lse = saved_forward.causal_forward(g["q"], g["k"], g["v"], shape.scale)
+        o, lse = abw.attn_fwd_causal(g["q"], g["k"], g["v"], shape.scale)
         dq, dk, dv = abw.attn_bwd_causal(g["q"], g["k"], g["v"], o, dout, lse, shape.scale, shape.rope_base, 0)
         if layer in check_layers:
             results[layer] = (inp, dx.float().cpu(), dq.cpu(), dk.cpu(), dv.cpu())
@@ -113,3 +112,64 @@ def test_chain_30_layers_sampled(abw):
             errs += [max_rel_err(to_np(dq[b, :, hs]), rq[b, :, hs]), max_rel_err(to_np(dk[b, :, j]), rk[b, :, j]),
                      max_rel_err(to_np(dv[b, :, j]), rv[b, :, j])]
         assert max(errs) <= TOL_BF16, (layer, errs)
+
+
+def saved_p_reference(q, k, v, dout, P, shape, units):
+    """The oracle's backward from a given probability matrix (the form of
+    transformer.js backward()), per (batch, KV head) unit, group-summed, with
+    RoPE backward on dq and dk when the shape has it."""
+    G = shape.Hq // shape.Hkv
+    dq = np.full(q.shape, np.nan)
+    dk = np.full(k.shape, np.nan)
+    dv = np.full(v.shape, np.nan)
+    for b, j in units:
+        dk[b, :, j] = 0.0
+        dv[b, :, j] = 0.0
+        for h in range(j * G, (j + 1) * G):
+            a, c, e = O.attention_head_backward_saved_p(P[b, h], q[b, :, h], k[b, :, j], v[b, :, j], dout[b, :, h],
+                                                        shape.scale)
+            dq[b, :, h] = a
+            dk[b, :, j] += c
+            dv[b, :, j] += e
+    if shape.rope_base > 0:
+        pos = np.broadcast_to(np.arange(shape.T) + shape.pos0, (shape.B, shape.T))
+        th = O.rope_angles(pos, shape.D, shape.rope_base)
+        dq, dk = O.rope_backward(dq, th), O.rope_backward(dk, th)
+    return dq, dk, dv
+
+
+@pytest.mark.parametrize("shape", [
+    W.CausalShape(B=2, T=130, Hq=4, Hkv=2, D=128, rope_base=10000.0),           # ragged tail, GQA
+    W.CausalShape(B=1, T=304, Hq=3, Hkv=1, D=128, rope_base=500000.0, pos0=5),  # G = 3
+    W.CHAIN_LAYER,                                                              # one chain layer, 20/5 heads
+])
+def test_causal_saved_p(abw, shape):
+    """Backward from the saved attention weights (bf16 [B][Hq][T][T], the
+    oracle's softmax of the same inputs rounded to bf16) and the forward's
+    output o (bf16), against the oracle's saved-probability backward."""
+    inp = W.causal_inputs(shape, seed=shape.T + 3 * shape.Hq)
+    q, k, v, do = (to_np(inp[n]) for n in ("q", "k", "v", "dout"))
+    G = shape.Hq // shape.Hkv
+    Pb = np.zeros((shape.B, shape.Hq, shape.T, shape.T))
+    ob = np.zeros(q.shape)
+    for b in range(shape.B):
+        for h in range(shape.Hq):
+            o_, _, P_ = O.attention_head_forward(q[b, :, h], k[b, :, h // G], v[b, :, h // G], shape.scale, True)
+            Pb[b, h] = P_
+            ob[b, :, h] = o_
+    P_bf = torch.from_numpy(Pb).to(torch.bfloat16)
+    o_bf = torch.from_numpy(ob).to(torch.bfloat16)
+    g = {n: inp[n].cuda() for n in ("q", "k", "v", "dout")}
+    dq, dk, dv = abw.attn_bwd_causal_saved_p(g["q"], g["k"], g["v"], P_bf.cuda(), o_bf.cuda(), g["dout"], shape.scale,
+                                             shape.rope_base, shape.pos0)
+    abw.device_check()
+    units = [(b, j) for b in range(shape.B) for j in range(shape.Hkv)][:4]
+    rq, rk, rv = saved_p_reference(q, k, v, do, to_np(P_bf), shape, units)
+    tag = f"saved_p B{shape.B} T{shape.T} Hq{shape.Hq}/{shape.Hkv}"
+    errs = []
+    for b, j in units:
+        hs = slice(j * G, (j + 1) * G)
+        errs.append(checked("dq", to_np(dq[b, :, hs]), rq[b, :, hs], tag))
+        errs.append(checked("dk", to_np(dk[b, :, j]), rk[b, :, j], tag))
+        errs.append(checked("dv", to_np(dv[b, :, j]), rv[b, :, j], tag))
+    assert max(errs) <= TOL_BF16, errs

@@ -15,7 +15,6 @@ import torch
 
 from tests.helpers import TOL_F32, max_rel_err, to_np
 from transformer_attention_backward_gb300 import _binding as B
-from transformer_attention_backward_gb300 import saved_forward
 from transformer_attention_backward_gb300 import workloads as W
 
 pytestmark = pytest.mark.gpu
@@ -27,7 +26,8 @@ def _p(t):
 
 def _run(lib, shape, seed, noalloc):
     g = {k: v.cuda() for k, v in W.causal_inputs(shape, seed=seed).items()}
-    o, lse = saved_forward.causal_forward(g["q"], g["k"], g["v"], shape.scale)
+    import transformer_attention_backward_gb300 as m
+    o, lse = m.attn_fwd_causal(g["q"], g["k"], g["v"], shape.scale)
     dq = torch.empty(g["q"].shape, dtype=torch.float32, device="cuda")
     dk = torch.empty(g["k"].shape, dtype=torch.float32, device="cuda")
     dv = torch.empty_like(dk)

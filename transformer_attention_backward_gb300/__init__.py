@@ -8,8 +8,8 @@ kernels; nothing here computes, and there is no fallback path.
 
 Functions (same names as the C ABI):
   softmax_bwd, rope_bwd, rmsnorm_bwd, rmsnorm_bwd_dgamma, relu2_mul_bwd,
-  lora_bwd, attn_bwd_decode, attn_bwd_causal, attn_bwd_causal_workspace_bytes,
-  device_check
+  lora_bwd, attn_bwd_decode, attn_fwd_causal, attn_bwd_causal,
+  attn_bwd_causal_saved_p, attn_bwd_causal_workspace_bytes, device_check
 """
 from __future__ import annotations
 
@@ -21,7 +21,7 @@ import torch
 from . import _binding as _b
 
 __all__ = ["softmax_bwd", "rope_bwd", "rmsnorm_bwd", "rmsnorm_bwd_dgamma", "relu2_mul_bwd", "lora_bwd",
-           "attn_bwd_decode", "attn_bwd_causal",
+           "attn_bwd_decode", "attn_fwd_causal", "attn_bwd_causal", "attn_bwd_causal_saved_p",
            "attn_bwd_causal_workspace_bytes", "device_check", "AbwError", "library"]
 
 AbwError = _b.AbwError
@@ -201,6 +201,27 @@ def attn_bwd_decode(q, k, v, dout, scale=None, rope_base=0.0, q_pos=-1, dq=None,
     return dq, dk, dv
 
 
+def attn_fwd_causal(q, k, v, scale=None, o=None, lse=None, stream=None):
+    """Causal attention forward: q [B][T][Hq][D], k, v [B][T][Hkv][D] bf16.
+    Returns (o [B][T][Hq][D] bf16, lse [B][Hq][T] fp32), the activations
+    attn_bwd_causal consumes."""
+    bf = (torch.bfloat16,)
+    _req(q, "q", bf)
+    B, T, Hq, D = q.shape
+    _req(k, "k", bf)
+    Hkv = k.shape[2]
+    _req(k, "k", bf, (B, T, Hkv, D))
+    _req(v, "v", bf, (B, T, Hkv, D))
+    scale = 1.0 / math.sqrt(D) if scale is None else scale
+    o = torch.empty_like(q) if o is None else o
+    lse = torch.empty(B, Hq, T, dtype=torch.float32, device=q.device) if lse is None else lse
+    _req(o, "o", bf, q.shape)
+    _req(lse, "lse", (torch.float32,), (B, Hq, T))
+    _b.check(library().attn_fwd_causal(_p(q), _p(k), _p(v), _p(o), _p(lse), B, T, Hq, Hkv, D, float(scale),
+                                       _s(stream)), "attn_fwd_causal")
+    return o, lse
+
+
 def attn_bwd_causal_workspace_bytes(B, T, Hq, D) -> int:
     return int(library().attn_bwd_causal_workspace_bytes(B, T, Hq, D))
 
@@ -234,4 +255,37 @@ def attn_bwd_causal(q, k, v, o, dout, lse, scale=None, rope_base=0.0, pos0=0, dq
                                        B, T, Hq, Hkv, D, float(scale), float(rope_base), int(pos0),
                                        _p(workspace), workspace.numel(), _s(stream)),
              "attn_bwd_causal")
+    return dq, dk, dv
+
+
+def attn_bwd_causal_saved_p(q, k, v, p_attn, o, dout, scale=None, rope_base=0.0, pos0=0, dq=None, dk=None, dv=None,
+                            workspace=None, stream=None):
+    """Causal attention backward from the saved attention weights p_attn
+    [B][Hq][T][T] bf16 (row = query) instead of the log-sum-exp.  q, o, dout
+    [B][T][Hq][D] bf16; k, v [B][T][Hkv][D] bf16.  Returns fp32 (dq, dk, dv)."""
+    bf = (torch.bfloat16,)
+    _req(q, "q", bf)
+    B, T, Hq, D = q.shape
+    _req(k, "k", bf)
+    Hkv = k.shape[2]
+    _req(k, "k", bf, (B, T, Hkv, D))
+    _req(v, "v", bf, (B, T, Hkv, D))
+    _req(p_attn, "p_attn", bf, (B, Hq, T, T))
+    _req(o, "o", bf, q.shape)
+    _req(dout, "dout", bf, q.shape)
+    scale = 1.0 / math.sqrt(D) if scale is None else scale
+    dq = torch.empty(q.shape, dtype=torch.float32, device=q.device) if dq is None else dq
+    dk = torch.empty(k.shape, dtype=torch.float32, device=k.device) if dk is None else dk
+    dv = torch.empty(v.shape, dtype=torch.float32, device=v.device) if dv is None else dv
+    _req(dq, "dq", (torch.float32,), q.shape)
+    _req(dk, "dk", (torch.float32,), k.shape)
+    _req(dv, "dv", (torch.float32,), v.shape)
+    need = attn_bwd_causal_workspace_bytes(B, T, Hq, D)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    _req(workspace, "workspace", (torch.uint8,))
+    _b.check(library().attn_bwd_causal_saved_p(_p(q), _p(k), _p(v), _p(p_attn), _p(o), _p(dout), _p(dq), _p(dk),
+                                               _p(dv), B, T, Hq, Hkv, D, float(scale), float(rope_base), int(pos0),
+                                               _p(workspace), workspace.numel(), _s(stream)),
+             "attn_bwd_causal_saved_p")
     return dq, dk, dv

@@ -35,9 +35,12 @@ SIGNATURES = {
     "relu2_mul_bwd": (_i, [_vp, _vp, _i, _vp, _vp, _vp, ctypes.c_longlong, _vp]),
     "lora_bwd_workspace_bytes": (_sz, [_i, _i]),
     "lora_bwd": (_i, [_vp, _i, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _vp, _sz, _vp]),
+    "attn_fwd_causal": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _vp]),
     "attn_bwd_causal_workspace_bytes": (_sz, [_i, _i, _i, _i]),
     "attn_bwd_causal": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _f, _i,
                              _vp, _sz, _vp]),
+    "attn_bwd_causal_saved_p": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _f, _i,
+                                     _vp, _sz, _vp]),
     "attn_bwd_causal_noalloc": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _f, _i,
                                      _vp]),
 }

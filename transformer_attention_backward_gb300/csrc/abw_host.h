@@ -58,8 +58,14 @@ cudaError_t launch_attn_bwd_decode(const float *q, const void *k, const void *v,
                                    int kv_bf16, float scale, double rope_base, int q_pos,
                                    const WaitCtl &w, cudaStream_t st, const char **why);
 
+cudaError_t launch_attn_fwd_causal(const void *q, const void *k, const void *v, void *o, float *lse, int B, int T,
+                                   int Hq, int Hkv, int D, float scale, const WaitCtl &w, cudaStream_t st,
+                                   const char **why);
+
 size_t causal_workspace_bytes(int B, int T, int Hq, int D);
-cudaError_t launch_attn_bwd_causal(const void *q, const void *k, const void *v, const void *o,
+// pattn: saved probabilities [B][Hq][T][T] bf16 (then lse may be null), or
+// null to recompute them from lse.
+cudaError_t launch_attn_bwd_causal(const void *q, const void *k, const void *v, const void *pattn, const void *o,
                                    const void *dout, const float *lse, float *dq, float *dk, float *dv,
                                    int B, int T, int Hq, int Hkv, int D, float scale, double rope_base,
                                    int pos0, void *ws, size_t ws_bytes, const WaitCtl &w,

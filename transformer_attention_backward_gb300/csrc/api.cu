@@ -369,6 +369,26 @@ abw_status attn_bwd_decode(const float *q, const void *k, const void *v, const f
                    "attn_bwd_decode", why);
 }
 
+abw_status attn_fwd_causal(const void *q, const void *k, const void *v, void *o, float *lse, int B, int T, int Hq,
+                           int Hkv, int D, float scale, abw_stream stream) {
+  if (B < 0 || T < 0 || Hq < 0 || Hkv < 0) return fail(ABW_EINVAL, "attn_fwd_causal: negative size");
+  if (Hkv == 0 || Hq % Hkv != 0) return fail(ABW_EINVAL, "attn_fwd_causal: Hq=%d not a multiple of Hkv=%d", Hq, Hkv);
+  if (D != 128) return fail(ABW_ENOTSUP, "attn_fwd_causal: D=%d unsupported (D == 128)", D);
+  if (!(scale == scale)) return fail(ABW_EINVAL, "attn_fwd_causal: scale is NaN");
+  if (B == 0 || T == 0 || Hq == 0) return ABW_OK;
+  const size_t qn = static_cast<size_t>(B) * T * Hq * D, kn = static_cast<size_t>(B) * T * Hkv * D;
+  Range in[] = {{"q", q, qn * 2}, {"k", k, kn * 2}, {"v", v, kn * 2}};
+  Range out[] = {{"o", o, qn * 2}, {"lse", lse, static_cast<size_t>(B) * Hq * T * 4}};
+  abw_status st = check_buffers("attn_fwd_causal", in, 3, out, 2);
+  if (st != ABW_OK) return st;
+  abw::WaitCtl w = abw::wait_ctl();
+  if (!w.err) return fail(ABW_ECUDA, "attn_fwd_causal: no CUDA device");
+  const char *why = nullptr;
+  return from_cuda(abw::launch_attn_fwd_causal(q, k, v, o, lse, B, T, Hq, Hkv, D, scale, w,
+                                               reinterpret_cast<cudaStream_t>(stream), &why),
+                   "attn_fwd_causal", why);
+}
+
 size_t attn_bwd_causal_workspace_bytes(int B, int T, int Hq, int D) {
   if (B < 0 || T < 0 || Hq < 0 || D < 0) return 0;
   return abw::causal_workspace_bytes(B, T, Hq, D);
@@ -399,10 +419,42 @@ abw_status attn_bwd_causal(const void *q, const void *k, const void *v, const vo
   if (!w.err) return fail(ABW_ECUDA, "attn_bwd_causal: no CUDA device");
   const char *why = nullptr;
   const double rb = rope_base > 0.0f ? static_cast<double>(rope_base) : 0.0;
-  return from_cuda(abw::launch_attn_bwd_causal(q, k, v, o, dout, lse, dq, dk, dv, B, T, Hq, Hkv, D, scale, rb, pos0,
+  return from_cuda(abw::launch_attn_bwd_causal(q, k, v, nullptr, o, dout, lse, dq, dk, dv, B, T, Hq, Hkv, D, scale, rb, pos0,
                                                workspace, workspace_bytes, w,
                                                reinterpret_cast<cudaStream_t>(stream), &why),
                    "attn_bwd_causal", why);
+}
+
+abw_status attn_bwd_causal_saved_p(const void *q, const void *k, const void *v, const void *p_attn, const void *o,
+                                   const void *dout, float *dq, float *dk, float *dv, int B, int T, int Hq, int Hkv,
+                                   int D, float scale, float rope_base, int pos0, void *workspace,
+                                   size_t workspace_bytes, abw_stream stream) {
+  if (B < 0 || T < 0 || Hq < 0 || Hkv < 0) return fail(ABW_EINVAL, "attn_bwd_causal_saved_p: negative size");
+  if (Hkv == 0 || Hq % Hkv != 0)
+    return fail(ABW_EINVAL, "attn_bwd_causal_saved_p: Hq=%d not a multiple of Hkv=%d", Hq, Hkv);
+  if (D != 128) return fail(ABW_ENOTSUP, "attn_bwd_causal_saved_p: D=%d unsupported (D == 128)", D);
+  if (rope_base > 0.0f && pos0 < 0) return fail(ABW_EINVAL, "attn_bwd_causal_saved_p: pos0 must be >= 0");
+  if (!(scale == scale)) return fail(ABW_EINVAL, "attn_bwd_causal_saved_p: scale is NaN");
+  if (B == 0 || T == 0 || Hq == 0) return ABW_OK;
+  const size_t need = abw::causal_workspace_bytes(B, T, Hq, D);
+  if (workspace == nullptr || workspace_bytes < need)
+    return fail(ABW_EWORKSPACE, "attn_bwd_causal_saved_p: workspace %zu bytes at %p, need %zu", workspace_bytes,
+                workspace, need);
+  const size_t qn = static_cast<size_t>(B) * T * Hq * D, kn = static_cast<size_t>(B) * T * Hkv * D;
+  const size_t pn = static_cast<size_t>(B) * Hq * T * T;
+  Range in[] = {{"q", q, qn * 2},    {"k", k, kn * 2},      {"v", v, kn * 2},
+                {"p_attn", p_attn, pn * 2}, {"o", o, qn * 2}, {"dout", dout, qn * 2}};
+  Range out[] = {{"dq", dq, qn * 4}, {"dk", dk, kn * 4}, {"dv", dv, kn * 4}, {"workspace", workspace, need}};
+  abw_status st = check_buffers("attn_bwd_causal_saved_p", in, 6, out, 4);
+  if (st != ABW_OK) return st;
+  abw::WaitCtl w = abw::wait_ctl();
+  if (!w.err) return fail(ABW_ECUDA, "attn_bwd_causal_saved_p: no CUDA device");
+  const char *why = nullptr;
+  const double rb = rope_base > 0.0f ? static_cast<double>(rope_base) : 0.0;
+  return from_cuda(abw::launch_attn_bwd_causal(q, k, v, p_attn, o, dout, nullptr, dq, dk, dv, B, T, Hq, Hkv, D, scale,
+                                               rb, pos0, workspace, workspace_bytes, w,
+                                               reinterpret_cast<cudaStream_t>(stream), &why),
+                   "attn_bwd_causal_saved_p", why);
 }
 
 abw_status attn_bwd_causal_noalloc(const void *q, const void *k, const void *v, const void *o, const void *dout,
@@ -437,7 +489,7 @@ abw_status attn_bwd_causal_noalloc(const void *q, const void *k, const void *v, 
   cudaError_t e = abw::noalloc_scratch(&scratch, &why);
   if (e != cudaSuccess) return from_cuda(e, "attn_bwd_causal_noalloc", why);
   const double rb = rope_base > 0.0f ? static_cast<double>(rope_base) : 0.0;
-  return from_cuda(abw::launch_attn_bwd_causal(q, k, v, o, dout, lse, dq, dk, dv, B, T, Hq, Hkv, D, scale, rb, pos0,
+  return from_cuda(abw::launch_attn_bwd_causal(q, k, v, nullptr, o, dout, lse, dq, dk, dv, B, T, Hq, Hkv, D, scale, rb, pos0,
                                                scratch, abw::kNoAllocScratchBytes, w,
                                                reinterpret_cast<cudaStream_t>(stream), &why),
                    "attn_bwd_causal_noalloc", why);

@@ -12,8 +12,8 @@
 //             128 queries (padding: delta 0, lse +inf so P = 0 there); the
 //             table of scale * (cos, sin) of theta(t, i) with RoPE
 //   2. kv   : tcgen05 kernel, one CTA per (128-key block, KV head, batch):
-//             dK and dV accumulate in TMEM over every query block at or after
-//             the key block; each bf16 dS tile leaves for the workspace
+//             dK and dV accumulate in TMEM over every 128-query block at or
+//             after the key block; each bf16 dS tile leaves for the workspace
 //   3. dq   : persistent tcgen05 kernel over (128-query block, head, batch):
 //             dQ^T = K^T dS^T accumulates in TMEM over the key blocks at or
 //             before the query block; dq is written once, scaled and rotated
@@ -25,26 +25,26 @@
 //
 // kv kernel (sm_103a, 12 warps, one CTA per SM).  Per CTA the K and V block
 // stays in shared memory; the CTA loops over the query heads of its KV group
-// and the 64-query blocks at or after its key block:
-//   MMA1  S^T  = K Q^T          M=128 keys, N=64 queries, K=128 (TMEM)
+// and the 128-query blocks at or after its key block:
+//   MMA1  S^T  = K Q^T          M=128 keys, N=128 queries, K=128 (TMEM)
 //   MMA2  dP^T = V dO^T         same shape
-//   softmax warps: P = exp2(S scale log2e - lse log2e) (causal mask),
-//          dS = P (dP - delta), both rounded to bf16 and written back into
-//          TMEM over the S / dP values just read; dS also goes straight to
-//          the workspace as a 128B-swizzled tile
-//   MMA3  dV  += P^T dO          M=128 keys, N=128, K=64 queries, A in TMEM
+//   softmax warps: P = exp2(S scale log2e - lse log2e) (causal mask on the
+//          diagonal block), written back as bf16 into TMEM over the S values
+//          just read; then dS = P (dP - delta), written over dP and, as a
+//          128B-swizzled tile row, to the workspace
+//   MMA3  dV  += P^T dO          M=128 keys, N=128, K=128 queries, A in TMEM
 //   MMA4  dK  += dS^T Q          same shape
-// Warp roles: 0 TMA producer, 1 MMA issuer, 2 TMEM owner, 4-11 softmax (two
-// groups of four warps, one per 32-key lane quarter, taking even / odd
-// iterations), then the dK (scale + RoPE) and dV epilogues, each group
-// taking half the columns of both.  S/dP are double-buffered in TMEM
-// so the tensor core computes block n+1 while the softmax warps work on
-// block n.  TMEM (512 columns):
-//   [0,64) S0 / P0   [64,128) dP0 / dS0   [128,192) S1 / P1   [192,256) dP1 / dS1
-//   [256,384) dV   [384,512) dK
-// P and dS stay in TMEM (a variant staging dS in shared memory, copied out in
-// bulk and read there by the dK product, measured slower).  Q / dO / lse /
-// delta arrive through a 5-deep TMA ring.
+// S/dP are single-buffered; what keeps the tensor core busy is the order of
+// the products and four separate signals (S ready, dP ready, P ready, dS
+// ready): per block n the issue order is S(n) dP(n) | dV(n) S(n+1) |
+// dK(n) dP(n+1), so P(n) is formed while dP(n) runs and dS(n) while dV(n)
+// and S(n+1) run.  Warp roles: 0 TMA producer, 1 MMA issuer, 2 TMEM owner,
+// 4-11 softmax (warp w: 32-key lane quarter w % 4, query half (w - 4) / 4),
+// then the dK (scale + RoPE) and dV epilogues, each half of the softmax
+// warps taking half the columns of both.  TMEM (512 columns):
+//   [0,128) S / P   [128,256) dP / dS   [256,384) dV   [384,512) dK
+// Q / dO / lse / delta of one query block (64 KB) arrive through a 2-deep
+// TMA ring.
 //
 // dq kernel (persistent, 12 warps, one CTA per SM): for each work item (128
 // queries of one head) and each key block at or before it, the K block
@@ -67,35 +67,50 @@ namespace {
 
 constexpr int kD = 128;
 constexpr int kBK = 128;   // keys per kv CTA, queries per dq CTA
-constexpr int kBQ = 64;    // queries per block (one dS tile)
+constexpr int kBQ = 64;    // queries per dS tile
 constexpr int kThr = 384;  // 12 warps
 constexpr int kTileBytes = kBK * kBQ * 2;   // one bf16 dS^T tile
 constexpr int kHeadGroup = 8;               // kv kernel: (batch, KV head) pairs per scheduling group
 
 // kv kernel shared memory.  It fills all but a few hundred bytes of the 227
 // KB a CTA may have, so there is no slack to align the base by hand: the
-// kernel checks that the dynamic shared memory starts on a 1024-byte boundary
-// (which the 128B-swizzled tiles need) and otherwise reports and returns.
+// kernel checks that the dynamic shared memory starts on a 1024-byte
+// boundary (which the 128B-swizzled tiles need) and otherwise reports and
+// returns.  One query block is 128 queries; its Q and its dO are each
+// [2 D-halves][128 rows][128 B] 128B-swizzled (32 KB).  Q goes through a
+// 3-deep ring (read by S and, last, dK) and dO through a 2-deep one (read by
+// dP and, last, dV, which comes earlier in the block), so each block's
+// copies are issued well before its first product; the block's lse and
+// delta (1 KB) ride with its Q copy into a 2-deep ring of their own, freed
+// by the softmax warps.  Once the last products have completed, the Q and
+// dO rings (160 KB) stage the dK and dV tiles of the epilogue.
+constexpr int kKvBQ = 128;               // queries per kv block (two dS^T tiles)
 constexpr int kOffK = 0;                 // [2 D-halves][128 keys][128 B], 128B-swizzled
 constexpr int kOffV = 32768;
-constexpr int kStages = 5;               // Q / dO / lse / delta ring depth
-constexpr int kOffStage = 65536;
-constexpr int kStageBytes = 32768;       // Q 16 KB, dO 16 KB
-constexpr int kStQ = 0, kStDO = 16384;
-constexpr int kOffLD = kOffStage + kStages * kStageBytes;   // per stage: lse2 [64] f32, delta [64] f32
-constexpr int kOffBar = kOffLD + kStages * 512;
-constexpr int kSmem = kOffBar + 256;
+constexpr int kQStagesKv = 3, kDOStages = 2, kLDStages = 2;
+constexpr int kBlockBytes = 32768;       // one Q or dO block
+constexpr int kOffQ = 65536;
+constexpr int kOffDO = kOffQ + kQStagesKv * kBlockBytes;
+constexpr int kOffStage = kOffQ;         // epilogue staging: dK tiles, then dV tiles
+constexpr int kHalfQ = 16384;            // one 64-dim half of a Q / dO block
+constexpr int kOffLD = kOffDO + kDOStages * kBlockBytes;   // per slot: lse2 [128] f32, delta [128] f32
+constexpr int kOffBar = kOffLD + kLDStages * 1024;
 
 // kv kernel barrier slots (8 bytes each) after kOffBar.
 enum {
-  kBarKV = 0, kBarQFull = 1, kBarQEmpty = kBarQFull + kStages, kBarSFull = kBarQEmpty + kStages,
-  kBarPFull = kBarSFull + 2, kBarDKV = kBarPFull + 2, kBarFinal = kBarDKV + 1, kNumBars = kBarFinal + 1
+  kBarKV = 0, kBarQFull = 1, kBarQEmpty = kBarQFull + kQStagesKv, kBarDOFull = kBarQEmpty + kQStagesKv,
+  kBarDOEmpty = kBarDOFull + kDOStages, kBarLDEmpty = kBarDOEmpty + kDOStages, kBarSFull = kBarLDEmpty + kLDStages,
+  kBarDPFull = kBarSFull + 1, kBarPFull = kBarDPFull + 1, kBarDSFull = kBarPFull + 1, kBarDKV = kBarDSFull + 1,
+  kBarFinal = kBarDKV + 1, kNumBars = kBarFinal + 1
 };
 constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
 constexpr int kOffAbort = kOffTmemSlot + 4;
+constexpr int kSmem = kOffBar + 256;
 static_assert(kOffAbort + 4 <= kSmem && kSmem <= 232448, "kv kernel shared memory");
+static_assert(2 * 65536 <= kOffLD - kOffStage, "epilogue staging fits the rings");
 
-constexpr uint32_t kColS0 = 0, kColDP0 = 64, kColS1 = 128, kColDP1 = 192, kColDV = 256, kColDK = 384;
+// kv kernel TMEM columns: S^T / P^T, dP^T / dS^T (one query block each), dV, dK.
+constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 384;
 
 // dq kernel shared memory: 3 stages of [K block 32 KB | two dS^T tiles 32 KB].
 constexpr int kQStages = 3;
@@ -208,7 +223,7 @@ __global__ void __launch_bounds__(256) causal_prep_kernel(const __nv_bfloat16 *_
       const size_t src = ((static_cast<size_t>(rb[k]) * T + rt[k]) * Hq + rh[k]) * kD;
       a[k] = reinterpret_cast<const uint4 *>(o + src)[sub];
       g[k] = reinterpret_cast<const uint4 *>(dout + src)[sub];
-      l[k] = lse[(static_cast<size_t>(rb[k]) * Hq + rh[k]) * T + rt[k]];
+      l[k] = lse ? lse[(static_cast<size_t>(rb[k]) * Hq + rh[k]) * T + rt[k]] : 0.f;
     } else {
       a[k] = make_uint4(0, 0, 0, 0);
       g[k] = a[k];
@@ -248,6 +263,7 @@ __global__ void __launch_bounds__(256) causal_prep_kernel(const __nv_bfloat16 *_
 struct TcParams {
   CausalWs ws;
   float *dq, *dk, *dv;
+  const __nv_bfloat16 *pattn;   // saved probabilities [B][Hq][T][T] (row = query), or null: recompute from lse
   int B, T, Tp, Hq, Hkv, G, nkb, nqb;
   int hsplit, gs;  // kv kernel: each KV head's G query heads go to hsplit CTAs, gs = G / hsplit each
   long long tph;   // dS^T tiles per head
@@ -302,8 +318,7 @@ __global__ void __launch_bounds__(kThr, 1)
   const int kvh = (hb / p.hsplit) % p.Hkv, b = hb / (p.hsplit * p.Hkv);
   const int h_first = kvh * p.G + split * p.gs;     // query heads h_first .. h_first + gs - 1
   const int k0 = kb * kBK;
-  const int qb0 = k0 / kBQ;
-  const int nq = p.nqb - qb0;            // query blocks per head
+  const int nq = p.nkb - kb;             // 128-query blocks at or after the key block, per head
   const int N = p.gs * nq;               // iterations of this CTA
 
   auto bar = [&](int i) -> uint32_t { return sb + kOffBar + i * 8; };
@@ -321,12 +336,19 @@ __global__ void __launch_bounds__(kThr, 1)
 
   if (tid == 0) {
     mbar_init(bar(kBarKV), 1);
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < kQStagesKv; ++s) {
       mbar_init(bar(kBarQFull + s), 1);
       mbar_init(bar(kBarQEmpty + s), 1);
     }
-    for (int s = 0; s < 2; ++s) mbar_init(bar(kBarSFull + s), 1);
-    for (int s = 0; s < 2; ++s) mbar_init(bar(kBarPFull + s), 128);   // a softmax group has put P and dS in TMEM
+    for (int s = 0; s < kDOStages; ++s) {
+      mbar_init(bar(kBarDOFull + s), 1);
+      mbar_init(bar(kBarDOEmpty + s), 1);
+    }
+    for (int s = 0; s < kLDStages; ++s) mbar_init(bar(kBarLDEmpty + s), 256);   // the softmax is done with it
+    mbar_init(bar(kBarSFull), 1);
+    mbar_init(bar(kBarDPFull), 1);
+    mbar_init(bar(kBarPFull), 256);    // every softmax thread has put its P row into TMEM
+    mbar_init(bar(kBarDSFull), 256);   // ... and its dS row
     mbar_init(bar(kBarDKV), 1);
     mbar_init(bar(kBarFinal), 1);
     *abort_flag = 0;
@@ -350,91 +372,111 @@ __global__ void __launch_bounds__(kThr, 1)
         tma_load_4d(sb + kOffK + hx * 16384, &tmK, hx * 64, kvh, k0, b, bar(kBarKV));
         tma_load_4d(sb + kOffV + hx * 16384, &tmV, hx * 64, kvh, k0, b, bar(kBarKV));
       }
-      int issued = 0;
+      int q_issued = 0, d_issued = 0;
       for (int n = 0; n < N; ++n) {
-        const int s = n % kStages, cyc = n / kStages;
-        if (!wt(bar(kBarQEmpty + s), (cyc & 1) ^ 1)) break;
         const int h = h_first + n / nq;
-        const int q0 = (qb0 + n % nq) * kBQ;
-        const uint32_t st = sb + kOffStage + s * kStageBytes;
-        const uint32_t fb = bar(kBarQFull + s);
-        mbar_arrive_expect_tx(fb, 2 * 16384 + 2 * 256);
-        for (int hx = 0; hx < 2; ++hx) {
-          tma_load_4d(st + kStQ + hx * 8192, &tmQ, hx * 64, h, q0, b, fb);
-          tma_load_4d(st + kStDO + hx * 8192, &tmDO, hx * 64, h, q0, b, fb);
-        }
+        const int q0 = (kb + n % nq) * kKvBQ;
+        const int qs = n % kQStagesKv, ds = n % kDOStages;
+        const int ls = n % kLDStages;
+        if (!wt(bar(kBarQEmpty + qs), ((n / kQStagesKv) & 1) ^ 1)) break;
+        if (!wt(bar(kBarLDEmpty + ls), ((n / kLDStages) & 1) ^ 1)) break;
+        mbar_arrive_expect_tx(bar(kBarQFull + qs), 2 * kHalfQ + 2 * 512);
+        for (int hx = 0; hx < 2; ++hx)
+          tma_load_4d(sb + kOffQ + qs * kBlockBytes + hx * kHalfQ, &tmQ, hx * 64, h, q0, b, bar(kBarQFull + qs));
         const size_t ro = (static_cast<size_t>(b) * p.Hq + h) * p.Tp + q0;
-        bulk_load(sb + kOffLD + s * 512, p.ws.lse2 + ro, 256, fb);
-        bulk_load(sb + kOffLD + s * 512 + 256, p.ws.delta + ro, 256, fb);
-        issued = n + 1;
+        bulk_load(sb + kOffLD + ls * 1024, p.ws.lse2 + ro, 512, bar(kBarQFull + qs));
+        bulk_load(sb + kOffLD + ls * 1024 + 512, p.ws.delta + ro, 512, bar(kBarQFull + qs));
+        q_issued = n + 1;
+        if (!wt(bar(kBarDOEmpty + ds), ((n / kDOStages) & 1) ^ 1)) break;
+        mbar_arrive_expect_tx(bar(kBarDOFull + ds), 2 * kHalfQ);
+        for (int hx = 0; hx < 2; ++hx)
+          tma_load_4d(sb + kOffDO + ds * kBlockBytes + hx * kHalfQ, &tmDO, hx * 64, h, q0, b, bar(kBarDOFull + ds));
+        d_issued = n + 1;
       }
       if (*abort_flag) {
         // let copies already in flight land before the CTA can exit
-        for (int n = (issued > kStages ? issued - kStages : 0); n < issued; ++n)
-          mbar_wait_bounded(bar(kBarQFull + n % kStages), (n / kStages) & 1, 2000000000ull);
+        for (int n = (q_issued > kQStagesKv ? q_issued - kQStagesKv : 0); n < q_issued; ++n)
+          mbar_wait_bounded(bar(kBarQFull + n % kQStagesKv), (n / kQStagesKv) & 1, 2000000000ull);
+        for (int n = (d_issued > kDOStages ? d_issued - kDOStages : 0); n < d_issued; ++n)
+          mbar_wait_bounded(bar(kBarDOFull + n % kDOStages), (n / kDOStages) & 1, 2000000000ull);
         mbar_wait_bounded(bar(kBarKV), 0, 2000000000ull);
       }
     }
   } else if (warp == 1) {
     // ============================ MMA issuer ==============================
     // The whole warp runs this loop in step (so descriptors and addresses stay
-    // warp-uniform); one elected lane issues each MMA and commit.
+    // warp-uniform); one elected lane issues each MMA and commit.  Per query
+    // block n the products go out in the order
+    //   S(n) dP(n) | P(n) ready: dV(n) S(n+1) | dS(n) ready: dK(n) dP(n+1)
+    // so that the softmax warps turn S(n) into P(n) while dP(n) runs, and
+    // dP(n) into dS(n) while dV(n) and S(n+1) run.  S(n+1) overwrites the
+    // P(n) columns dV(n) reads, and dP(n+1) the dS(n) columns dK(n) reads:
+    // tcgen05 MMAs of one thread run in issue order, so each reads its
+    // operand before the next product writes there.
     {
-      constexpr uint32_t id_sdp = tc::idesc_bf16_f32(128, 64, 0, 0);    // S^T, dP^T
+      constexpr uint32_t id_sdp = tc::idesc_bf16_f32(128, 128, 0, 0);   // S^T, dP^T
       constexpr uint32_t id_kv = tc::idesc_bf16_f32(128, 128, 0, 1);    // dV, dK (A from TMEM)
       // Descriptors are built once; moving by a byte offset inside shared
       // memory adds offset / 16 to the address field (all offsets stay below
       // 256 KB, so the 14-bit field never carries).
       const uint64_t dK = tc::sdesc_sw128(sb + kOffK, 16, 1024), dV = tc::sdesc_sw128(sb + kOffV, 16, 1024);
-      const uint64_t dQk = tc::sdesc_sw128(sb + kOffStage + kStQ, 16, 1024);     // Q as K-major B of S^T
-      const uint64_t dOk = tc::sdesc_sw128(sb + kOffStage + kStDO, 16, 1024);    // dO as K-major B of dP^T
-      const uint64_t dQm = tc::sdesc_sw128(sb + kOffStage + kStQ, 8192, 1024);   // Q as MN-major B of dK
-      const uint64_t dOm = tc::sdesc_sw128(sb + kOffStage + kStDO, 8192, 1024);  // dO as MN-major B of dV
+      const uint64_t dQk = tc::sdesc_sw128(sb + kOffQ, 16, 1024);          // Q as K-major B of S^T
+      const uint64_t dOk = tc::sdesc_sw128(sb + kOffDO, 16, 1024);         // dO as K-major B of dP^T
+      const uint64_t dQm = tc::sdesc_sw128(sb + kOffQ, kHalfQ, 1024);      // Q as MN-major B of dK
+      const uint64_t dOm = tc::sdesc_sw128(sb + kOffDO, kHalfQ, 1024);     // dO as MN-major B of dV
       bool ok = wtw(bar(kBarKV), 0);
       tc::fence_after_sync();
-      // S/dP(n) go to TMEM buffer n & 1.  That buffer last held P/dS(n - 2),
-      // which MMA3/4(n - 2) read; those were issued before this (the loop
-      // below waits for P/dS(n - 2) and issues MMA3/4(n - 2) before it issues
-      // S/dP(n)), and tcgen05 MMAs of one thread run in issue order.
-      auto issue_sdp = [&](int n) -> bool {
-        const int s = n & 1;                                      // TMEM buffer
-        const int qs = n % kStages, qc = n / kStages;             // smem stage
-        if (!wtw(bar(kBarQFull + qs), qc & 1)) return false;
+      auto qoff = [](int n) -> uint64_t { return static_cast<uint64_t>((n % kQStagesKv) * kBlockBytes) >> 4; };
+      auto dooff = [](int n) -> uint64_t { return static_cast<uint64_t>((n % kDOStages) * kBlockBytes) >> 4; };
+      // K-step kk (16 of the 128 head dims): half kk / 4, 32 bytes per step inside it
+      auto kstep = [](int kk, int half) -> uint32_t { return static_cast<uint32_t>((kk >> 2) * half + (kk & 3) * 32) >> 4; };
+      // With saved probabilities there is no S product: the S signal then
+      // only says that the P columns are free again (every product issued
+      // so far, dV(n - 1) included, has completed).
+      const bool saved_p = p.pattn != nullptr;
+      auto issue_s = [&](int n) -> bool {
+        if (!wtw(bar(kBarQFull + n % kQStagesKv), (n / kQStagesKv) & 1)) return false;
         tc::fence_after_sync();
-        const uint64_t so = static_cast<uint64_t>(qs * kStageBytes) >> 4;
-        const uint32_t tS = tmem + (s ? kColS1 : kColS0), tP = tmem + (s ? kColDP1 : kColDP0);
+        if (!saved_p) {
+          const uint64_t so = qoff(n);
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t ko = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4, qo = ((kk >> 2) * 8192 + (kk & 3) * 32) >> 4;
-          tc::mma_bf16_w(tS, dK + ko, dQk + so + qo, id_sdp, kk > 0);
+          for (int kk = 0; kk < 8; ++kk)
+            tc::mma_bf16_w(tmem + kColS, dK + kstep(kk, 16384), dQk + so + kstep(kk, kHalfQ), id_sdp, kk > 0);
         }
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t ko = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4, qo = ((kk >> 2) * 8192 + (kk & 3) * 32) >> 4;
-          tc::mma_bf16_w(tP, dV + ko, dOk + so + qo, id_sdp, kk > 0);
-        }
-        tc::commit_w(bar(kBarSFull + s));
+        tc::commit_w(bar(kBarSFull));
         return true;
       };
-      if (ok && N > 0) ok = issue_sdp(0);
-      for (int n = 0; ok && n < N; ++n) {
-        if (n + 1 < N && !issue_sdp(n + 1)) break;
-        if (!wtw(bar(kBarPFull + (n & 1)), (n >> 1) & 1)) break;
+      auto issue_dp = [&](int n) -> bool {
+        if (!wtw(bar(kBarDOFull + n % kDOStages), (n / kDOStages) & 1)) return false;
         tc::fence_after_sync();
-        const int qs = n % kStages;
-        const uint64_t so = static_cast<uint64_t>(qs * kStageBytes) >> 4;
-        // P^T / dS^T sit in TMEM: queries 32 h .. 32 h + 31 (h = 0, 1) in the
-        // 16 columns from 32 h of the S (P) and dP (dS) columns of the buffer
-        const uint32_t tP = tmem + ((n & 1) ? kColS1 : kColS0), tD = tmem + ((n & 1) ? kColDP1 : kColDP0);
+        const uint64_t so = dooff(n);
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk)   // dV += P^T dO
-          tc::mma_bf16_ts_w(tmem + kColDV, tP + (kk >> 1) * 32 + (kk & 1) * 8, dOm + so + ((kk * 2048) >> 4), id_kv,
-                          (n > 0 || kk > 0));
+        for (int kk = 0; kk < 8; ++kk)
+          tc::mma_bf16_w(tmem + kColDP, dV + kstep(kk, 16384), dOk + so + kstep(kk, kHalfQ), id_sdp, kk > 0);
+        tc::commit_w(bar(kBarDPFull));
+        return true;
+      };
+      if (ok && N > 0) ok = issue_s(0) && issue_dp(0);
+      // P^T / dS^T of query chunk c (16 queries) sit in the 8 TMEM columns
+      // 32 (c / 2) + 8 (c % 2) of the S (P) and dP (dS) columns.
+      for (int n = 0; ok && n < N; ++n) {
+        if (!wtw(bar(kBarPFull), n & 1)) break;
+        tc::fence_after_sync();
+        const uint64_t dso = dooff(n), qso = qoff(n);
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk)   // dK += dS^T Q
-          tc::mma_bf16_ts_w(tmem + kColDK, tD + (kk >> 1) * 32 + (kk & 1) * 8, dQm + so + ((kk * 2048) >> 4), id_kv,
-                          (n > 0 || kk > 0));
-        tc::commit_w(bar(kBarQEmpty + qs));
+        for (int kk = 0; kk < 8; ++kk)   // dV += P^T dO
+          tc::mma_bf16_ts_w(tmem + kColDV, tmem + kColS + (kk >> 1) * 32 + (kk & 1) * 8, dOm + dso + ((kk * 2048) >> 4),
+                            id_kv, (n > 0 || kk > 0));
+        tc::commit_w(bar(kBarDOEmpty + n % kDOStages));   // dO(n) has been read for the last time
+        if (n + 1 < N && !issue_s(n + 1)) break;
+        if (!wtw(bar(kBarDSFull), n & 1)) break;
+        tc::fence_after_sync();
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)   // dK += dS^T Q
+          tc::mma_bf16_ts_w(tmem + kColDK, tmem + kColDP + (kk >> 1) * 32 + (kk & 1) * 8, dQm + qso + ((kk * 2048) >> 4),
+                            id_kv, (n > 0 || kk > 0));
+        tc::commit_w(bar(kBarQEmpty + n % kQStagesKv));   // and Q(n)
+        if (n + 1 < N && !issue_dp(n + 1)) break;
       }
       tc::commit_w(bar(kBarDKV));
       tc::commit_w(bar(kBarFinal));
@@ -442,83 +484,125 @@ __global__ void __launch_bounds__(kThr, 1)
     }
   } else if (warp >= 4) {
     // ============================ softmax warps ===========================
-    // Two groups of four warps take alternate iterations (group g: n = g,
-    // g + 2, ...; TMEM buffer g), so one group's TMEM / memory latencies
-    // overlap the other group's arithmetic.  Each warp covers a 32-key lane
-    // quarter and all 64 queries, in two halves of 32.
+    // Warp w covers the 32-key TMEM lane quarter w % 4 and half g of the 128
+    // queries of every block (64 queries: S / dP columns 64 g .. 64 g + 63).
+    // Per block: wait for S, form P (kept in fp32 registers), write it back
+    // as bf16 over the S values just read, arrive; then wait for dP, form
+    // dS = P (dP - delta), write it over dP and to the workspace, arrive.
     const int qd = warp & 3;                            // TMEM lane quarter
-    const int ch = (warp - 4) >> 2;                     // group: iteration parity (then dK / dV epilogue)
+    const int ch = (warp - 4) >> 2;                     // query half (then dK / dV epilogue half)
     const int j = 32 * qd + lane;                       // key row in the block
     const int key = k0 + j;
     const uint32_t lanebase = static_cast<uint32_t>(32 * qd) << 16;
     const float sl2 = p.scale * 1.4426950408889634f;
-    for (int n = ch; n < N; n += 2) {
-      const int cyc = n >> 1;
-      const int q0 = (qb0 + n % nq) * kBQ;
-      if (!wtw(bar(kBarSFull + ch), cyc & 1)) break;
-      tc::fence_after_sync();
-      const int qs = n % kStages;
+    const uint32_t tS = tmem + lanebase + kColS + 64 * ch;
+    const uint32_t tD = tmem + lanebase + kColDP + 64 * ch;
+    for (int n = 0; n < N; ++n) {
       const int h = h_first + n / nq;
-      const int qb = qb0 + n % nq;
-      unsigned char *row = reinterpret_cast<unsigned char *>(
-          p.ws.ds + ((static_cast<size_t>(b) * p.Hq + h) * p.tph + tile_index(kb, qb, p.nqb)) * (kTileBytes / 2)) +
-          j * 128;
-      // only the two query blocks that overlap the key block need the causal
-      // mask; queries past T have lse = +inf, so their P is exactly 0
-      const bool diag = q0 < k0 + kBK;
-      const float *lse2 = reinterpret_cast<const float *>(smem + kOffLD + qs * 512);
-      const float *dl = reinterpret_cast<const float *>(smem + kOffLD + qs * 512 + 256);
-      const uint32_t tS = tmem + lanebase + (ch ? kColS1 : kColS0);
-      const uint32_t tD = tmem + lanebase + (ch ? kColDP1 : kColDP0);
-      // Four chunks of 16 queries, software-pipelined: the TMEM load of chunk
-      // c + 1 is in flight while chunk c is computed, and the P / dS stores to
-      // TMEM complete once, before the arrive.  P / dS of chunk c (16 bf16
-      // pairs = 8 columns each) go to columns 32 (c / 2) + 8 (c % 2) of the
-      // S / dP block: the A-operand layout of MMA3/4, and only over columns
-      // that chunks <= c have already read.
-      uint32_t buf[2][32];
-      tc::ld16x2_async(tS, tD, buf[0]);
+      const int qb = kb + n % nq;                       // 128-query block
+      const int q0 = qb * kKvBQ + 64 * ch;              // this half's first query
+      // lse * log2 e and delta of this half's 64 queries; they arrived with
+      // Q(n), which S(n) waited for (with saved probabilities too)
+      const int ls = n % kLDStages;
+      const float *lse2 = reinterpret_cast<const float *>(smem + kOffLD + ls * 1024) + 64 * ch;
+      const float *dl = reinterpret_cast<const float *>(smem + kOffLD + ls * 1024 + 512) + 64 * ch;
+      // only the diagonal block needs the causal mask; queries past T have
+      // lse = +inf, so their P is exactly 0
+      const bool diag = qb == kb;
+      float P[64];
+      uint32_t pk[32];
+      if (p.pattn) {
+        // ---- P from the saved probabilities: this thread's key column of
+        // the 64 query rows, read before the P columns are free
+        const __nv_bfloat16 *pc = p.pattn + (static_cast<size_t>(b) * p.Hq + h) * p.T * p.T + key;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t (&cur)[32] = buf[c & 1];
-        tc::wait_ld16x2(cur);
-        if (c < 3) tc::ld16x2_async(tS + 16 * (c + 1), tD + 16 * (c + 1), buf[(c + 1) & 1]);
-        uint32_t pk[8], dk[8];
-#pragma unroll
-        for (int e = 0; e < 16; e += 4) {
-          const float4 l4 = *reinterpret_cast<const float4 *>(lse2 + 16 * c + e);
-          const float4 d4 = *reinterpret_cast<const float4 *>(dl + 16 * c + e);
-          float P0 = fast_exp2(fmaf(__uint_as_float(cur[e]), sl2, -l4.x));
-          float P1 = fast_exp2(fmaf(__uint_as_float(cur[e + 1]), sl2, -l4.y));
-          float P2 = fast_exp2(fmaf(__uint_as_float(cur[e + 2]), sl2, -l4.z));
-          float P3 = fast_exp2(fmaf(__uint_as_float(cur[e + 3]), sl2, -l4.w));
-          if (diag) {
-            const int q = q0 + 16 * c + e;
-            P0 = key <= q ? P0 : 0.f;
-            P1 = key <= q + 1 ? P1 : 0.f;
-            P2 = key <= q + 2 ? P2 : 0.f;
-            P3 = key <= q + 3 ? P3 : 0.f;
-          }
-          const float dS0 = P0 * (__uint_as_float(cur[16 + e]) - d4.x);
-          const float dS1 = P1 * (__uint_as_float(cur[16 + e + 1]) - d4.y);
-          const float dS2 = P2 * (__uint_as_float(cur[16 + e + 2]) - d4.z);
-          const float dS3 = P3 * (__uint_as_float(cur[16 + e + 3]) - d4.w);
-          pk[e / 2] = pack_bf16x2(P0, P1);
-          pk[e / 2 + 1] = pack_bf16x2(P2, P3);
-          dk[e / 2] = pack_bf16x2(dS0, dS1);
-          dk[e / 2 + 1] = pack_bf16x2(dS2, dS3);
+        for (int e = 0; e < 64; ++e) {
+          const int q = q0 + e;
+          P[e] = (q < p.T && key <= q) ? __bfloat162float(pc[static_cast<size_t>(q) * p.T]) : 0.f;
         }
-        const int pc = 32 * (c >> 1) + 8 * (c & 1);
-        tc::st8x2_async(tS + pc, pk, tD + pc, dk);
-        // dS^T row j, queries 16 c .. 16 c + 15 (16-byte units 2c, 2c + 1) of
-        // tile (kb, qb), in the 128B-swizzled layout the dq kernel copies
-        // into shared memory unchanged
-        *reinterpret_cast<uint4 *>(row + (((2 * c) ^ (j & 7)) << 4)) = make_uint4(dk[0], dk[1], dk[2], dk[3]);
-        *reinterpret_cast<uint4 *>(row + (((2 * c + 1) ^ (j & 7)) << 4)) = make_uint4(dk[4], dk[5], dk[6], dk[7]);
+        if (!wtw(bar(kBarSFull), n & 1)) break;
+        tc::fence_after_sync();
+#pragma unroll
+        for (int e = 0; e < 64; e += 2) pk[e / 2] = pack_bf16x2(P[e], P[e + 1]);
+      } else {
+      // ---- P = 2^(S scale log2 e - lse log2 e)
+      if (!wtw(bar(kBarSFull), n & 1)) break;
+      tc::fence_after_sync();
+      {
+        float (&lo)[32] = *reinterpret_cast<float (*)[32]>(&P[0]);
+        float (&hi)[32] = *reinterpret_cast<float (*)[32]>(&P[32]);
+        tc::ld32x2_wait(tS, tS + 32, lo, hi);
+      }
+#pragma unroll
+      for (int e = 0; e < 64; e += 4) {
+        const float4 l4 = *reinterpret_cast<const float4 *>(lse2 + e);
+        P[e] = fast_exp2(fmaf(P[e], sl2, -l4.x));
+        P[e + 1] = fast_exp2(fmaf(P[e + 1], sl2, -l4.y));
+        P[e + 2] = fast_exp2(fmaf(P[e + 2], sl2, -l4.z));
+        P[e + 3] = fast_exp2(fmaf(P[e + 3], sl2, -l4.w));
+        if (diag) {
+          const int q = q0 + e;
+          P[e] = key <= q ? P[e] : 0.f;
+          P[e + 1] = key <= q + 1 ? P[e + 1] : 0.f;
+          P[e + 2] = key <= q + 2 ? P[e + 2] : 0.f;
+          P[e + 3] = key <= q + 3 ? P[e + 3] : 0.f;
+        }
+        pk[e / 2] = pack_bf16x2(P[e], P[e + 1]);
+        pk[e / 2 + 1] = pack_bf16x2(P[e + 2], P[e + 3]);
+      }
+      }
+      // chunk c (16 queries = 8 packed columns) goes to column 32 (c / 2) +
+      // 8 (c % 2) of this half: the A-operand layout of the dV product
+      {
+        const uint32_t (&c0)[8] = *reinterpret_cast<const uint32_t (*)[8]>(&pk[0]);
+        const uint32_t (&c1)[8] = *reinterpret_cast<const uint32_t (*)[8]>(&pk[8]);
+        const uint32_t (&c2)[8] = *reinterpret_cast<const uint32_t (*)[8]>(&pk[16]);
+        const uint32_t (&c3)[8] = *reinterpret_cast<const uint32_t (*)[8]>(&pk[24]);
+        tc::st8x2_async(tS, c0, tS + 8, c1);
+        tc::st8x2_async(tS + 32, c2, tS + 40, c3);
       }
       tc::wait_st();
       tc::fence_before_sync();
-      mbar_arrive(bar(kBarPFull + ch));
+      mbar_arrive(bar(kBarPFull));
+      // ---- dS = P (dP - delta), to TMEM (A operand of dK) and to the workspace
+      unsigned char *row = reinterpret_cast<unsigned char *>(
+          p.ws.ds + ((static_cast<size_t>(b) * p.Hq + h) * p.tph + tile_index(kb, 2 * qb + ch, p.nqb)) *
+                        (kTileBytes / 2)) +
+          j * 128;
+      if (!wtw(bar(kBarDPFull), n & 1)) break;
+      tc::fence_after_sync();
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        float d[32];
+        tc::ld32_wait(tD + 32 * half, d);
+        uint32_t dk[16];
+#pragma unroll
+        for (int e = 0; e < 32; e += 4) {
+          const float4 d4 = *reinterpret_cast<const float4 *>(dl + 32 * half + e);
+          const float s0 = P[32 * half + e] * (d[e] - d4.x);
+          const float s1 = P[32 * half + e + 1] * (d[e + 1] - d4.y);
+          const float s2 = P[32 * half + e + 2] * (d[e + 2] - d4.z);
+          const float s3 = P[32 * half + e + 3] * (d[e + 3] - d4.w);
+          dk[e / 2] = pack_bf16x2(s0, s1);
+          dk[e / 2 + 1] = pack_bf16x2(s2, s3);
+        }
+        {
+          const uint32_t (&c0)[8] = *reinterpret_cast<const uint32_t (*)[8]>(&dk[0]);
+          const uint32_t (&c1)[8] = *reinterpret_cast<const uint32_t (*)[8]>(&dk[8]);
+          tc::st8x2_async(tD + 32 * half, c0, tD + 32 * half + 8, c1);
+        }
+        // dS^T row j, queries 32 half .. 32 half + 31 (16-byte units 4 half ..
+        // 4 half + 3) of tile (kb, 2 qb + g), in the 128B-swizzled layout the
+        // dq kernel copies into shared memory unchanged
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          *reinterpret_cast<uint4 *>(row + (((4 * half + u) ^ (j & 7)) << 4)) =
+              make_uint4(dk[4 * u], dk[4 * u + 1], dk[4 * u + 2], dk[4 * u + 3]);
+      }
+      tc::wait_st();
+      tc::fence_before_sync();
+      mbar_arrive(bar(kBarDSFull));
+      mbar_arrive(bar(kBarLDEmpty + ls));
     }
     // ---- dK (scale + RoPE backward) and dV epilogues.  Group g takes the
     // 32-column chunks 2g and 2g + 1 of both.  Every MMA has completed once
@@ -819,10 +903,10 @@ size_t causal_workspace_bytes(int B, int T, int Hq, int D) {
          up256(static_cast<size_t>(B) * Hq * static_cast<size_t>(tiles_per_head(nkb)) * kTileBytes);
 }
 
-cudaError_t launch_attn_bwd_causal(const void *q, const void *k, const void *v, const void *o, const void *dout,
-                                   const float *lse, float *dq, float *dk, float *dv, int B, int T, int Hq, int Hkv,
-                                   int D, float scale, double rope_base, int pos0, void *ws, size_t ws_bytes,
-                                   const WaitCtl &w, cudaStream_t st, const char **why) {
+cudaError_t launch_attn_bwd_causal(const void *q, const void *k, const void *v, const void *pattn, const void *o,
+                                   const void *dout, const float *lse, float *dq, float *dk, float *dv, int B, int T,
+                                   int Hq, int Hkv, int D, float scale, double rope_base, int pos0, void *ws,
+                                   size_t ws_bytes, const WaitCtl &w, cudaStream_t st, const char **why) {
   (void)ws_bytes;
   if (D != kD) {
     *why = "D != 128";
@@ -870,12 +954,13 @@ cudaError_t launch_attn_bwd_causal(const void *q, const void *k, const void *v, 
     if (e != cudaSuccess) return e;
   }
   CUtensorMap tq, tdo, tk, tv, tdk, tdv;
-  if (!make_map(&tq, q, Hq, T, B, kBQ, why) || !make_map(&tdo, dout, Hq, T, B, kBQ, why) ||
+  if (!make_map(&tq, q, Hq, T, B, kKvBQ, why) || !make_map(&tdo, dout, Hq, T, B, kKvBQ, why) ||
       !make_map(&tk, k, Hkv, T, B, kBK, why) || !make_map(&tv, v, Hkv, T, B, kBK, why) ||
       !make_map_f32(&tdk, dk, Hkv, T, B, why) || !make_map_f32(&tdv, dv, Hkv, T, B, why))
     return cudaErrorInvalidValue;
   TcParams p;
   p.ws = cw;
+  p.pattn = static_cast<const __nv_bfloat16 *>(pattn);
   p.dq = dq;
   p.dk = dk;
   p.dv = dv;
