@@ -949,6 +949,28 @@ def run_native(args):
     return 0
 
 
+def run_profile_target(args):
+    """A short, fixed launch sequence for profiler captures (not a
+    measurement; prints nothing but a one-line note): the causal T = 2048
+    forward and backward, `--warmup` calls each."""
+    import torch
+    import transformer_attention_backward_gb300 as abw
+    from transformer_attention_backward_gb300 import workloads as W
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    cs = W.CAUSAL_2K if args.profile == "causal_t2048" else W.CAUSAL_8K
+    cin = {k: v.to(dev) for k, v in W.causal_inputs(cs, seed=W.SEED_BASE + 3).items()}
+    ws = torch.empty(abw.attn_bwd_causal_workspace_bytes(cs.B, cs.T, cs.Hq, cs.D), dtype=torch.uint8, device=dev)
+    for _ in range(args.warmup):
+        o, lse = abw.attn_fwd_causal(cin["q"], cin["k"], cin["v"], cs.scale)
+    for _ in range(args.warmup):
+        abw.attn_bwd_causal(cin["q"], cin["k"], cin["v"], o, cin["dout"], lse, cs.scale, cs.rope_base, 0,
+                            workspace=ws)
+    abw.device_check()
+    print(f"profile target {args.profile}: {args.warmup} forward and {args.warmup} backward calls", flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -959,9 +981,13 @@ def main():
     ap.add_argument("--skip-cpu", action="store_true")
     ap.add_argument("--skip-chain", action="store_true")
     ap.add_argument("--skip-rows", action="store_true")
+    ap.add_argument("--profile", choices=["causal_t2048", "causal_t8192"], default=None,
+                    help="run a short fixed launch sequence for a profiler capture and exit")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "native":
         args.warmup = 3
+    if args.profile:
+        return run_profile_target(args)
     if args.impl == "reference":
         return run_reference(args)
     return run_native(args)

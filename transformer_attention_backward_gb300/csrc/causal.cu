@@ -565,12 +565,12 @@ __global__ void __launch_bounds__(kThr, 1)
       tc::fence_before_sync();
       mbar_arrive(bar(kBarPFull));
       // ---- dS = P (dP - delta), to TMEM (A operand of dK) and to the workspace
-      unsigned char *row = reinterpret_cast<unsigned char *>(
+      unsigned char *tile = reinterpret_cast<unsigned char *>(
           p.ws.ds + ((static_cast<size_t>(b) * p.Hq + h) * p.tph + tile_index(kb, 2 * qb + ch, p.nqb)) *
-                        (kTileBytes / 2)) +
-          j * 128;
+                        (kTileBytes / 2));
       if (!wtw(bar(kBarDPFull), n & 1)) break;
       tc::fence_after_sync();
+      uint4 U[8];   // this key row's dS^T as eight 16-byte units of 8 queries
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
         float d[32];
@@ -591,13 +591,40 @@ __global__ void __launch_bounds__(kThr, 1)
           const uint32_t (&c1)[8] = *reinterpret_cast<const uint32_t (*)[8]>(&dk[8]);
           tc::st8x2_async(tD + 32 * half, c0, tD + 32 * half + 8, c1);
         }
-        // dS^T row j, queries 32 half .. 32 half + 31 (16-byte units 4 half ..
-        // 4 half + 3) of tile (kb, 2 qb + g), in the 128B-swizzled layout the
-        // dq kernel copies into shared memory unchanged
 #pragma unroll
-        for (int u = 0; u < 4; ++u)
-          *reinterpret_cast<uint4 *>(row + (((4 * half + u) ^ (j & 7)) << 4)) =
-              make_uint4(dk[4 * u], dk[4 * u + 1], dk[4 * u + 2], dk[4 * u + 3]);
+        for (int u = 0; u < 4; ++u) U[4 * half + u] = make_uint4(dk[4 * u], dk[4 * u + 1], dk[4 * u + 2], dk[4 * u + 3]);
+      }
+      // The tile row of key j is one 128-byte line, held whole by one lane.
+      // Stored as it is, each warp store would touch 32 lines with 16 bytes
+      // each; an 8 x 8 transpose of the units within each group of 8 lanes
+      // (three xor-shuffle stages) leaves lane l with unit l % 8 of the 8
+      // rows of its group, so each store writes 4 whole lines.
+#pragma unroll
+      for (int bi = 0; bi < 3; ++bi) {
+        const int bm = 4 >> bi;
+        const bool hi = (lane & bm) != 0;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          if (k & bm) continue;
+          const uint4 send = hi ? U[k] : U[k | bm];
+          uint4 recv;
+          recv.x = __shfl_xor_sync(0xffffffffu, send.x, bm);
+          recv.y = __shfl_xor_sync(0xffffffffu, send.y, bm);
+          recv.z = __shfl_xor_sync(0xffffffffu, send.z, bm);
+          recv.w = __shfl_xor_sync(0xffffffffu, send.w, bm);
+          if (hi)
+            U[k] = recv;
+          else
+            U[k | bm] = recv;
+        }
+      }
+      // lane l now holds, in U[k], unit l % 8 (queries 8 (l % 8) ..) of key
+      // row 32 qd + 8 (l / 8) + k, at its 128B-swizzled position in the tile
+      // (the layout the dq kernel copies into shared memory unchanged)
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const int r = 32 * qd + (lane & ~7) + k;
+        *reinterpret_cast<uint4 *>(tile + r * 128 + (((lane & 7) ^ k) << 4)) = U[k];
       }
       tc::wait_st();
       tc::fence_before_sync();
