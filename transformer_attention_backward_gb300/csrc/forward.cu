@@ -11,7 +11,7 @@
 // m + log l the log-sum-exp.
 //
 // Design (sm_103a, tcgen05): one CTA per (128-query block, head, batch),
-// heaviest query blocks first.  Warp 0 loads Q once and K / V blocks of 128
+// heads in groups of 8 with the heaviest query blocks of a group first.  Warp 0 loads Q once and K / V blocks of 128
 // keys through a 3-deep TMA ring; warp 1 issues
 //   S = Q K^T   (M=128 queries, N=128 keys, K=128: TMEM, two buffers)
 //   O += P V    (M=128 queries, N=128 dims, K=128 keys: A = P in TMEM)
@@ -48,6 +48,7 @@ constexpr int kFSmem = kFOffBar + 256 + 1024;   // + alignment slack
 static_assert(kFOffTmem + 8 <= kFOffBar + 256 && kFSmem <= 232448, "forward kernel shared memory");
 constexpr uint32_t kFColO = 0, kFColS0 = 128, kFColS1 = 256;
 constexpr float kRescale = 8.f;       // lazy-rescale threshold (base-2 units)
+constexpr int kFHeadGroup = 8;        // (batch, head) pairs per scheduling group
 
 struct FwdParams {
   __nv_bfloat16 *o;
@@ -87,11 +88,17 @@ __global__ void __launch_bounds__(kFThr, 1)
   const uint32_t sb = smem_u32(smem);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
-  // item: (query block m, head h, batch b), heaviest (largest m) first
-  const int per_m = p.Hq * p.B;
-  const int m = p.nqb - 1 - static_cast<int>(blockIdx.x) / per_m;
-  const int rem = static_cast<int>(blockIdx.x) % per_m;
-  const int h = rem % p.Hq, b = rem / p.Hq;
+  // item: (query block m, head h, batch b).  The (batch, head) pairs go in
+  // groups of kFHeadGroup; within a group the heavy (late) query blocks come
+  // first.  The CTAs that run at one time then cover few heads, whose K and
+  // V (every query block of a head re-reads them) stay in L2.
+  const int nh = p.Hq * p.B;
+  const int grp = static_cast<int>(blockIdx.x) / (kFHeadGroup * p.nqb);
+  const int gsz = min(kFHeadGroup, nh - grp * kFHeadGroup);
+  const int in_grp = static_cast<int>(blockIdx.x) - grp * kFHeadGroup * p.nqb;
+  const int m = p.nqb - 1 - in_grp / gsz;
+  const int hb = grp * kFHeadGroup + in_grp % gsz;   // b * Hq + h
+  const int h = hb % p.Hq, b = hb / p.Hq;
   const int kvh = h / p.G;
   const int q0 = m * kFB;
   const int N = m + 1;                    // key blocks 0 .. m

@@ -75,7 +75,8 @@ __global__ void __launch_bounds__(256) relu2_mul_bwd_kernel(const void *__restri
 
 // ----------------------------------------------------------------- LoRA
 constexpr int kLoraRows = 4;     // rows per block of the row pass
-constexpr int kLoraChunk = 32;   // rows per block of the column pass
+constexpr int kLoraChunk = 32;   // rows per block of the column pass (a power of two)
+constexpr int kLoraBatch = 8;    // rows whose loads are in flight together
 
 template <bool XBF16>
 __device__ __forceinline__ float4 ldg_x4(const void *x, size_t i4) {
@@ -122,28 +123,29 @@ __global__ void __launch_bounds__(256) lora_rows_kernel(const void *__restrict__
     for (int j = 0; j < RK; ++j)
       a[j] = j < r ? __ldg(reinterpret_cast<const float4 *>(A + static_cast<size_t>(j) * n_in) + c)
                    : make_float4(0.f, 0.f, 0.f, 0.f);
+    float4 xv[kLoraRows];
 #pragma unroll
-    for (int t = 0; t < kLoraRows; ++t) {
-      if (t0 + t < rows) {
-        const float4 xv = ldg_x4<XBF16>(x, static_cast<size_t>(t0 + t) * c4 + c);
+    for (int t = 0; t < kLoraRows; ++t)
+      xv[t] = t0 + t < rows ? ldg_x4<XBF16>(x, static_cast<size_t>(t0 + t) * c4 + c) : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-        for (int j = 0; j < RK; ++j) acc[t][j] += xv.x * a[j].x + xv.y * a[j].y + xv.z * a[j].z + xv.w * a[j].w;
-      }
-    }
+    for (int t = 0; t < kLoraRows; ++t)
+#pragma unroll
+      for (int j = 0; j < RK; ++j)
+        acc[t][j] += xv[t].x * a[j].x + xv[t].y * a[j].y + xv[t].z * a[j].z + xv[t].w * a[j].w;
   }
-  // dh: one output column per step (B row o holds its r rank entries)
+  // dh: one output column per step (B row o holds its r rank entries); the
+  // loads of a step are issued before its products
+#pragma unroll 2
   for (int o = tid; o < n_out; o += 256) {
-    float bo[RK];
+    float bo[RK], d[kLoraRows];
 #pragma unroll
     for (int j = 0; j < RK; ++j) bo[j] = j < r ? __ldg(B + static_cast<size_t>(o) * r + j) : 0.f;
 #pragma unroll
-    for (int t = 0; t < kLoraRows; ++t) {
-      if (t0 + t < rows) {
-        const float d = __ldg(dy + static_cast<size_t>(t0 + t) * n_out + o);
+    for (int t = 0; t < kLoraRows; ++t) d[t] = t0 + t < rows ? __ldg(dy + static_cast<size_t>(t0 + t) * n_out + o) : 0.f;
 #pragma unroll
-        for (int j = 0; j < RK; ++j) acc2[t][j] = fmaf(d, bo[j], acc2[t][j]);
-      }
-    }
+    for (int t = 0; t < kLoraRows; ++t)
+#pragma unroll
+      for (int j = 0; j < RK; ++j) acc2[t][j] = fmaf(d[t], bo[j], acc2[t][j]);
   }
 #pragma unroll
   for (int t = 0; t < kLoraRows; ++t)
@@ -193,20 +195,29 @@ __global__ void __launch_bounds__(256) lora_cols_kernel(const void *__restrict__
   __syncthreads();
   const int in4 = n_in >> 2, out4 = n_out >> 2;
   const int c = blockIdx.x * 256 + tid;
+  // Rows go in batches of kLoraBatch whose loads are all issued before the
+  // first use, so the batch waits for one memory latency rather than one per
+  // row.
   if (c < in4) {
     float4 acc[RK];
 #pragma unroll
     for (int j = 0; j < RK; ++j) acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int t = 0; t < nr; ++t) {
-      const float4 xv = ldg_x4<XBF16>(x, static_cast<size_t>(r0 + t) * in4 + c);
+    for (int t0 = 0; t0 < nr; t0 += kLoraBatch) {
+      float4 xv[kLoraBatch];
 #pragma unroll
-      for (int j = 0; j < RK; ++j) {
-        const float w = dhs[t][j];
-        acc[j].x = fmaf(w, xv.x, acc[j].x);
-        acc[j].y = fmaf(w, xv.y, acc[j].y);
-        acc[j].z = fmaf(w, xv.z, acc[j].z);
-        acc[j].w = fmaf(w, xv.w, acc[j].w);
-      }
+      for (int u = 0; u < kLoraBatch; ++u)
+        xv[u] = t0 + u < nr ? ldg_x4<XBF16>(x, static_cast<size_t>(r0 + t0 + u) * in4 + c)
+                            : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int u = 0; u < kLoraBatch; ++u)
+#pragma unroll
+        for (int j = 0; j < RK; ++j) {
+          const float w = dhs[(t0 + u) & (kLoraChunk - 1)][j];   // rows past nr have xv = 0
+          acc[j].x = fmaf(w, xv[u].x, acc[j].x);
+          acc[j].y = fmaf(w, xv[u].y, acc[j].y);
+          acc[j].z = fmaf(w, xv[u].z, acc[j].z);
+          acc[j].w = fmaf(w, xv[u].w, acc[j].w);
+        }
     }
 #pragma unroll
     for (int j = 0; j < RK; ++j)
@@ -218,16 +229,23 @@ __global__ void __launch_bounds__(256) lora_cols_kernel(const void *__restrict__
     for (int e = 0; e < 4; ++e)
 #pragma unroll
       for (int j = 0; j < RK; ++j) acc[e][j] = 0.f;
-    for (int t = 0; t < nr; ++t) {
-      const float4 d = __ldg(reinterpret_cast<const float4 *>(dy + static_cast<size_t>(r0 + t) * n_out) + o4);
+    for (int t0 = 0; t0 < nr; t0 += kLoraBatch) {
+      float4 dv[kLoraBatch];
 #pragma unroll
-      for (int j = 0; j < RK; ++j) {
-        const float w = hs[t][j];
-        acc[0][j] = fmaf(d.x, w, acc[0][j]);
-        acc[1][j] = fmaf(d.y, w, acc[1][j]);
-        acc[2][j] = fmaf(d.z, w, acc[2][j]);
-        acc[3][j] = fmaf(d.w, w, acc[3][j]);
-      }
+      for (int u = 0; u < kLoraBatch; ++u)
+        dv[u] = t0 + u < nr
+                    ? __ldg(reinterpret_cast<const float4 *>(dy + static_cast<size_t>(r0 + t0 + u) * n_out) + o4)
+                    : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int u = 0; u < kLoraBatch; ++u)
+#pragma unroll
+        for (int j = 0; j < RK; ++j) {
+          const float w = hs[(t0 + u) & (kLoraChunk - 1)][j];
+          acc[0][j] = fmaf(dv[u].x, w, acc[0][j]);
+          acc[1][j] = fmaf(dv[u].y, w, acc[1][j]);
+          acc[2][j] = fmaf(dv[u].z, w, acc[2][j]);
+          acc[3][j] = fmaf(dv[u].w, w, acc[3][j]);
+        }
     }
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
