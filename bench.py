@@ -322,12 +322,17 @@ def kernel_breakdown(fn, reps=2):
 def time_launches(fn, stream, reps, flush=None):
     """Mean device time (ms) of one call of `fn`, from CUDA events around
     each call on `stream`; with `flush`, a buffer larger than L2 is written
-    before every call (outside the events)."""
+    and read back before every call (outside the events)."""
     import torch
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+    flush_sink = torch.empty((), device=flush.device) if flush is not None else None
     for a, b in evs:
         if flush is not None:
+            # write a buffer larger than L2, then read it back: the write
+            # evicts everything, the read turns the dirty lines it left into
+            # clean ones, so the timed call pays no write-back of the flush
             flush.fill_(1.0)
+            flush_sink.copy_(flush.sum())
         a.record(stream)
         fn()
         b.record(stream)
@@ -599,7 +604,7 @@ def run_rows(abw, W, dev, stream, args):
         gbs = nbytes / (ms * 1e-3) / 1e9
         out[name] = {"us": round(ms * 1e3, 2), "bytes": nbytes, "gbs": round(gbs, 1),
                      **fractions(gbs, "hbm_gbs", peaks, kind),
-                     "l2": "flushed before each launch" if cold else "inputs larger than L2"}
+                     "l2": "flushed before each launch (1 GiB written, then read)" if cold else "inputs larger than L2"}
 
     # RoPE backward, dq of the causal T = 2048 workload: [4][2048][20][128] fp32
     dy = torch.randn(4, 2048, 20, 128, generator=g, device=dev)

@@ -39,8 +39,8 @@
  *     a message for the last non-OK status of the calling thread.
  *   - Nothing crosses the ABI as a C++ exception, and nothing aborts.
  *   - Calls neither synchronise nor allocate: the work they enqueue on
- *     `stream` is kernel launches (and, for GQA-split causal shapes,
- *     memsets).  The first call of an operation on a device also resolves
+ *     `stream` is kernel launches (and, for rmsnorm_bwd_dgamma, a memset of
+ *     its output).  The first call of an operation on a device also resolves
  *     per-device state and raises the kernels' shared-memory limits.  So the
  *     calls can be captured into CUDA graphs; make one call of each operation
  *     on the device before capturing.

@@ -173,6 +173,8 @@ struct PrepRope {
   double inv_freq[kD / 2];   // base^(-2i/D), formed on the host in double
   float scale;
   int use_rope, pos0;
+  float *zero_dk, *zero_dv;  // zeroed when zero_n4 > 0 (float4 count of each)
+  long long zero_n4;
 };
 
 __global__ void __launch_bounds__(256) causal_prep_kernel(const __nv_bfloat16 *__restrict__ o,
@@ -181,6 +183,16 @@ __global__ void __launch_bounds__(256) causal_prep_kernel(const __nv_bfloat16 *_
                                                           float *__restrict__ lse2, float2 *__restrict__ rope, int B,
                                                           int T, int Tp, int Hq, const __grid_constant__ PrepRope rp) {
   const long long gid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  // with the kv kernel's head groups split over CTAs, dK and dV receive
+  // partial sums by reduction: zero them first (16 bytes per thread, strided
+  // over the grid)
+  if (rp.zero_n4 > 0) {
+    const long long nthr = static_cast<long long>(gridDim.x) * blockDim.x;
+    for (long long e = gid; e < rp.zero_n4; e += nthr) {
+      reinterpret_cast<float4 *>(rp.zero_dk)[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+      reinterpret_cast<float4 *>(rp.zero_dv)[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+  }
   const int sub = threadIdx.x & 15;
   // padding entries
   const long long npad = static_cast<long long>(B) * Hq * (Tp - T);
@@ -959,6 +971,9 @@ cudaError_t launch_attn_bwd_causal(const void *q, const void *k, const void *v, 
   CausalWs cw = carve(ws, B, T, Hq, D);
   const int rope = rope_base > 0.0;
   PrepRope rp;
+  rp.zero_dk = dk;
+  rp.zero_dv = dv;
+  rp.zero_n4 = hsplit > 1 ? static_cast<long long>(B) * T * Hkv * kD / 4 : 0;
   for (int i = 0; i < kD / 2; ++i) rp.inv_freq[i] = rope ? pow(rope_base, -2.0 * i / kD) : 0.0;
   rp.scale = scale;
   rp.use_rope = rope;
@@ -974,12 +989,6 @@ cudaError_t launch_attn_bwd_causal(const void *q, const void *k, const void *v, 
   }
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  if (hsplit > 1) {
-    const size_t kvn = static_cast<size_t>(B) * T * Hkv * kD * 4;
-    e = cudaMemsetAsync(dk, 0, kvn, st);
-    if (e == cudaSuccess) e = cudaMemsetAsync(dv, 0, kvn, st);
-    if (e != cudaSuccess) return e;
-  }
   CUtensorMap tq, tdo, tk, tv, tdk, tdv;
   if (!make_map(&tq, q, Hq, T, B, kKvBQ, why) || !make_map(&tdo, dout, Hq, T, B, kKvBQ, why) ||
       !make_map(&tk, k, Hkv, T, B, kBK, why) || !make_map(&tv, v, Hkv, T, B, kBK, why) ||
