@@ -956,13 +956,49 @@ def run_native(args):
 
 def run_profile_target(args):
     """A short, fixed launch sequence for profiler captures (not a
-    measurement; prints nothing but a one-line note): the causal T = 2048
-    forward and backward, `--warmup` calls each."""
+    measurement; prints nothing but a one-line note), `--warmup` calls of
+    each operation: the causal T = 2048 (or 8192) forward and backward; the
+    decode step (decode backward + RMSNorm backward); or one call of each
+    memory-bound kernel at the bench's sizes (RMSNorm 16384 x 2560 in place
+    of 65536, to keep the capture small)."""
     import torch
     import transformer_attention_backward_gb300 as abw
     from transformer_attention_backward_gb300 import workloads as W
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
+    if args.profile == "decode":
+        shape = W.DECODE_GQA
+        g = {k: v.to(dev) for k, v in W.decode_inputs(shape, seed=W.SEED_BASE + 2).items()}
+        rn = {k: (v.to(dev) if torch.is_tensor(v) else v)
+              for k, v in W.rmsnorm_inputs(*W.RMSNORM_DECODE, seed=W.SEED_BASE + 20).items()}
+        for _ in range(args.warmup):
+            abw.attn_bwd_decode(g["q"], g["k"], g["v"], g["dout"], shape.scale, shape.rope_base, shape.q_pos)
+            abw.rmsnorm_bwd(rn["x"], rn["gamma"], rn["dy"], eps=rn["eps"])
+        abw.device_check()
+        print(f"profile target decode: {args.warmup} steps", flush=True)
+        return 0
+    if args.profile == "rows":
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(W.SEED_BASE + 30)
+        r = lambda *sh: torch.randn(*sh, generator=gen, device=dev)
+        dy = r(4, 2048, 20, 128)
+        x16, xf = r(1024, 2560).to(torch.bfloat16), r(16384, 2560)
+        gam = 1.0 + 0.1 * r(2560)
+        d16, df = r(1024, 2560), r(16384, 2560)
+        sm, dys = torch.softmax(r(65536, 1024), -1), r(65536, 1024)
+        gt, ut, dht = r(1024, 6912).to(torch.bfloat16), r(1024, 6912).to(torch.bfloat16), r(1024, 6912)
+        A, Bq, dyq = 0.02 * r(8, 2560), 0.02 * r(2560, 8), r(1024, 2560)
+        for _ in range(args.warmup):
+            abw.rope_bwd(dy, pos0=0, base=10000.0)
+            abw.rmsnorm_bwd(x16, gam, d16, eps=1e-6, dx_dtype=torch.bfloat16)
+            abw.rmsnorm_bwd(xf, gam, df, eps=1e-6)
+            abw.softmax_bwd(sm, dys)
+            abw.rmsnorm_bwd_dgamma(x16, gam, d16, eps=1e-6, dx_dtype=torch.bfloat16)
+            abw.relu2_mul_bwd(gt, ut, dht)
+            abw.lora_bwd(x16, dyq, A, Bq, 2.0)
+        abw.device_check()
+        print(f"profile target rows: {args.warmup} rounds", flush=True)
+        return 0
     cs = W.CAUSAL_2K if args.profile == "causal_t2048" else W.CAUSAL_8K
     cin = {k: v.to(dev) for k, v in W.causal_inputs(cs, seed=W.SEED_BASE + 3).items()}
     ws = torch.empty(abw.attn_bwd_causal_workspace_bytes(cs.B, cs.T, cs.Hq, cs.D), dtype=torch.uint8, device=dev)
@@ -986,7 +1022,7 @@ def main():
     ap.add_argument("--skip-cpu", action="store_true")
     ap.add_argument("--skip-chain", action="store_true")
     ap.add_argument("--skip-rows", action="store_true")
-    ap.add_argument("--profile", choices=["causal_t2048", "causal_t8192"], default=None,
+    ap.add_argument("--profile", choices=["causal_t2048", "causal_t8192", "decode", "rows"], default=None,
                     help="run a short fixed launch sequence for a profiler capture and exit")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "native":
