@@ -79,8 +79,10 @@ constexpr int kHeadGroup = 8;               // kv kernel: (batch, KV head) pairs
 // returns.  One query block is 128 queries; its Q and its dO are each
 // [2 D-halves][128 rows][128 B] 128B-swizzled (32 KB).  Q goes through a
 // 3-deep ring (read by S and, last, dK) and dO through a 2-deep one (read by
-// dP and, last, dV, which comes earlier in the block), so each block's
-// copies are issued well before its first product; the block's lse and
+// dP and, last, dV, which comes earlier in the block; after dV the slot
+// stages the block's dS^T rows for their bulk copy to the workspace before
+// it is refilled), so each block's copies are issued well before its first
+// product; the block's lse and
 // delta (1 KB) ride with its Q copy into a 2-deep ring of their own, freed
 // by the softmax warps.  Once the last products have completed, the Q and
 // dO rings (160 KB) stage the dK and dV tiles of the epilogue.
@@ -100,7 +102,8 @@ constexpr int kOffBar = kOffLD + kLDStages * 1024;
 enum {
   kBarKV = 0, kBarV = 1, kBarQFull = 2, kBarQEmpty = kBarQFull + kQStagesKv, kBarDOFull = kBarQEmpty + kQStagesKv,
   kBarDOEmpty = kBarDOFull + kDOStages, kBarLDEmpty = kBarDOEmpty + kDOStages, kBarSFull = kBarLDEmpty + kLDStages,
-  kBarDPFull = kBarSFull + 1, kBarPFull = kBarDPFull + 1, kBarDSFull = kBarPFull + 1, kBarDKV = kBarDSFull + 1,
+  kBarDPFull = kBarSFull + 1, kBarPFull = kBarDPFull + 1, kBarDSFull = kBarPFull + 1, kBarDVDone = kBarDSFull + 1,
+  kBarStaged = kBarDVDone + 1, kBarRope = kBarStaged + 1, kBarDKV = kBarRope + 1,
   kBarFinal = kBarDKV + 1, kNumBars = kBarFinal + 1
 };
 constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
@@ -130,6 +133,14 @@ struct CausalWs {
 };
 
 size_t up256(size_t x) { return (x + 255) / 256 * 256; }
+
+// Position of RoPE pair i of position t in the table: rows of 64 pairs
+// (512 B), the 16-byte units (two pairs) of a row XOR-swizzled by t % 8, so
+// that a warp reading one unit of 32 consecutive rows out of shared memory
+// touches every bank the same number of times.
+__host__ __device__ __forceinline__ int rope_slot(int t, int i) {
+  return t * (kD / 2) + ((((i >> 1) ^ (t & 7)) << 1) | (i & 1));
+}
 
 // Queries and keys padded to whole 128-blocks: every key block then sees an
 // even number of 64-query blocks, and the dq kernel's two tiles always exist.
@@ -267,7 +278,7 @@ __global__ void __launch_bounds__(256) causal_prep_kernel(const __nv_bfloat16 *_
       const float th = static_cast<float>(fma(-twopi, rint(ang * inv_twopi), ang));
       float sn, c;
       __sincosf(th, &sn, &c);   // |th| <= pi: absolute error ~1e-6, far below the bf16 inputs' rounding
-      rope[e] = make_float2(rp.scale * c, rp.scale * sn);
+      rope[rope_slot(t, i)] = make_float2(rp.scale * c, rp.scale * sn);
     }
   }
 }
@@ -355,13 +366,16 @@ __global__ void __launch_bounds__(kThr, 1)
     }
     for (int s = 0; s < kDOStages; ++s) {
       mbar_init(bar(kBarDOFull + s), 1);
-      mbar_init(bar(kBarDOEmpty + s), 1);
+      mbar_init(bar(kBarDOEmpty + s), 1);   // the block's dS copy has read the slot
     }
     for (int s = 0; s < kLDStages; ++s) mbar_init(bar(kBarLDEmpty + s), 256);   // the softmax is done with it
     mbar_init(bar(kBarSFull), 1);
     mbar_init(bar(kBarDPFull), 1);
     mbar_init(bar(kBarPFull), 256);    // every softmax thread has put its P row into TMEM
     mbar_init(bar(kBarDSFull), 256);   // ... and its dS row
+    mbar_init(bar(kBarDVDone), 1);     // dV(n) has read dO(n) for the last time
+    mbar_init(bar(kBarStaged), 256);   // every softmax thread has staged its dS row
+    mbar_init(bar(kBarRope), 1);       // the key block's RoPE rows landed
     mbar_init(bar(kBarDKV), 1);
     mbar_init(bar(kBarFinal), 1);
     *abort_flag = 0;
@@ -486,7 +500,7 @@ __global__ void __launch_bounds__(kThr, 1)
         for (int kk = 0; kk < 8; ++kk)   // dV += P^T dO
           tc::mma_bf16_ts_w(tmem + kColDV, tmem + kColS + (kk >> 1) * 32 + (kk & 1) * 8, dOm + dso + ((kk * 2048) >> 4),
                             id_kv, (n > 0 || kk > 0));
-        tc::commit_w(bar(kBarDOEmpty + n % kDOStages));   // dO(n) has been read for the last time
+        tc::commit_w(bar(kBarDVDone));   // dO(n) has been read for the last time
         if (n + 1 < N && !issue_s(n + 1)) break;
         if (!wtw(bar(kBarDSFull), n & 1)) break;
         tc::fence_after_sync();
@@ -501,6 +515,26 @@ __global__ void __launch_bounds__(kThr, 1)
       tc::commit_w(bar(kBarFinal));
       mbar_wait_bounded(bar(kBarFinal), 0, 2000000000ull);   // every MMA has completed
     }
+  } else if (warp == 3) {
+    // ============================ dS copy warp ============================
+    // Block n's two dS^T tiles are adjacent in the workspace; one 32 KB bulk
+    // copy takes them from the dO(n) slot.  Waiting for the copy to read the
+    // slot (it queues behind the ring's loads) happens here, not in the
+    // softmax warps.
+    if (lane == 0) {
+      for (int n = 0; n < N; ++n) {
+        if (!wt(bar(kBarStaged), n & 1)) break;
+        const int h = h_first + n / nq, qb = kb + n % nq;
+        __nv_bfloat16 *dst =
+            p.ws.ds + ((static_cast<size_t>(b) * p.Hq + h) * p.tph + tile_index(kb, 2 * qb, p.nqb)) * (kTileBytes / 2);
+        bulk_store(dst, sb + kOffDO + (n % kDOStages) * kBlockBytes, 2 * kTileBytes);
+        bulk_commit_group();
+        bulk_wait_group_read0();
+        mbar_arrive(bar(kBarDOEmpty + n % kDOStages));
+      }
+      bulk_wait_group0();
+    }
+    named_barrier(3, 288);
   } else if (warp >= 4) {
     // ============================ softmax warps ===========================
     // Warp w covers the 32-key TMEM lane quarter w % 4 and half g of the 128
@@ -516,6 +550,7 @@ __global__ void __launch_bounds__(kThr, 1)
     const float sl2 = p.scale * 1.4426950408889634f;
     const uint32_t tS = tmem + lanebase + kColS + 64 * ch;
     const uint32_t tD = tmem + lanebase + kColDP + 64 * ch;
+    bool rope_issued = false;
     for (int n = 0; n < N; ++n) {
       const int h = h_first + n / nq;
       const int qb = kb + n % nq;                       // 128-query block
@@ -584,11 +619,21 @@ __global__ void __launch_bounds__(kThr, 1)
       tc::fence_before_sync();
       mbar_arrive(bar(kBarPFull));
       // ---- dS = P (dP - delta), to TMEM (A operand of dK) and to the workspace
-      unsigned char *tile = reinterpret_cast<unsigned char *>(
-          p.ws.ds + ((static_cast<size_t>(b) * p.Hq + h) * p.tph + tile_index(kb, 2 * qb + ch, p.nqb)) *
-                        (kTileBytes / 2));
       if (!wtw(bar(kBarDPFull), n & 1)) break;
       tc::fence_after_sync();
+      if (n == N - 1 && p.rope && warp == 4 && lane == 0) {
+        // dP(N - 1) has completed, so have dK(N - 2) and dK(N - 3): the two
+        // Q slots other than Q(N - 1)'s are free.  They take this key
+        // block's RoPE rows for the dK epilogue (keys 0-63, then 64-127).
+        const int rows = min(kBK, p.T - k0);
+        mbar_arrive_expect_tx(bar(kBarRope), rows * 512);
+        bulk_load(sb + kOffQ + (N % kQStagesKv) * kBlockBytes, p.ws.rope + k0 * (kD / 2), min(rows, 64) * 512,
+                  bar(kBarRope));
+        if (rows > 64)
+          bulk_load(sb + kOffQ + ((N + 1) % kQStagesKv) * kBlockBytes, p.ws.rope + (k0 + 64) * (kD / 2),
+                    (rows - 64) * 512, bar(kBarRope));
+        rope_issued = true;
+      }
       uint4 U[8];   // this key row's dS^T as eight 16-byte units of 8 queries
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
@@ -613,60 +658,54 @@ __global__ void __launch_bounds__(kThr, 1)
 #pragma unroll
         for (int u = 0; u < 4; ++u) U[4 * half + u] = make_uint4(dk[4 * u], dk[4 * u + 1], dk[4 * u + 2], dk[4 * u + 3]);
       }
-      // The tile row of key j is one 128-byte line, held whole by one lane.
-      // Stored as it is, each warp store would touch 32 lines with 16 bytes
-      // each; an 8 x 8 transpose of the units within each group of 8 lanes
-      // (three xor-shuffle stages) leaves lane l with unit l % 8 of the 8
-      // rows of its group, so each store writes 4 whole lines.
-#pragma unroll
-      for (int bi = 0; bi < 3; ++bi) {
-        const int bm = 4 >> bi;
-        const bool hi = (lane & bm) != 0;
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          if (k & bm) continue;
-          const uint4 send = hi ? U[k] : U[k | bm];
-          uint4 recv;
-          recv.x = __shfl_xor_sync(0xffffffffu, send.x, bm);
-          recv.y = __shfl_xor_sync(0xffffffffu, send.y, bm);
-          recv.z = __shfl_xor_sync(0xffffffffu, send.z, bm);
-          recv.w = __shfl_xor_sync(0xffffffffu, send.w, bm);
-          if (hi)
-            U[k] = recv;
-          else
-            U[k | bm] = recv;
-        }
-      }
-      // lane l now holds, in U[k], unit l % 8 (queries 8 (l % 8) ..) of key
-      // row 32 qd + 8 (l / 8) + k, at its 128B-swizzled position in the tile
-      // (the layout the dq kernel copies into shared memory unchanged)
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const int r = 32 * qd + (lane & ~7) + k;
-        *reinterpret_cast<uint4 *>(tile + r * 128 + (((lane & 7) ^ k) << 4)) = U[k];
-      }
+      // dS is in TMEM and this block's lse / delta have been read: the dK
+      // product (and after it dP(n + 1)) may start while the workspace copy
+      // below is still being written
       tc::wait_st();
       tc::fence_before_sync();
       mbar_arrive(bar(kBarDSFull));
       mbar_arrive(bar(kBarLDEmpty + ls));
+      // Once dV(n) has read dO(n) for the last time, its ring slot stages
+      // the block's two dS^T tiles (32 KB in the tiles' own 128B-swizzled
+      // layout: unit u of row r at 16 (u ^ (r % 8))); the copy warp moves
+      // them to the workspace and hands the slot back to the producer.
+      if (!wtw(bar(kBarDVDone), n & 1)) break;
+      tc::fence_after_sync();
+      {
+        const uint32_t stg = kOffDO + (n % kDOStages) * kBlockBytes + ch * 16384 + qd * 4096 + lane * 128;
+#pragma unroll
+        for (int u = 0; u < 8; ++u) *reinterpret_cast<uint4 *>(smem + stg + ((u ^ (lane & 7)) << 4)) = U[u];
+        fence_proxy_async_smem();
+        mbar_arrive(bar(kBarStaged));
+      }
     }
+    // The last dS copies have read the rings before the epilogue reuses them
+    // (the second group's dV tiles cover the first dO slot).
+    named_barrier(3, 288);
     // ---- dK (scale + RoPE backward) and dV epilogues.  Group g takes the
     // 32-column chunks 2g and 2g + 1 of both.  Every MMA has completed once
     // DKV fires, and the producer has nothing left to load, so the Q / dO
     // stages are free: dK and dV are staged there as 128B-swizzled [128 rows]
     // [32] fp32 tiles and one lane per group stores its four with TMA (rows
-    // past T are not written).  The RoPE table entries are fetched before the
-    // wait.  The group agrees on the outcome of the wait: its named barriers
-    // must be reached by all four warps or by none.
+    // past T are not written).  Each thread first takes its key's RoPE
+    // entries from the two Q slots they were copied to; all 256 threads agree
+    // on the outcome of the waits and have read the table before any tile is
+    // staged over it.
     float4 cs[2][8];
+    bool ok = wtw(bar(kBarDKV), 0);
+    if (p.rope) ok = ok && wtw(bar(kBarRope), 0);
+    {
+      const unsigned char *row =
+          smem + kOffQ + ((j < 64 ? N : N + 1) % kQStagesKv) * kBlockBytes + (j & 63) * 512;
 #pragma unroll
-    for (int cc = 0; cc < 2; ++cc)
+      for (int cc = 0; cc < 2; ++cc)
 #pragma unroll
-      for (int i = 0; i < 8; ++i)
-        cs[cc][i] = (p.rope && key < p.T)
-                        ? *reinterpret_cast<const float4 *>(p.ws.rope + key * (kD / 2) + 16 * (2 * ch + cc) + 2 * i)
-                        : make_float4(p.scale, 0.f, p.scale, 0.f);
-    if (named_barrier_and(1 + ch, 128, wtw(bar(kBarDKV), 0))) {
+        for (int i = 0; i < 8; ++i)
+          cs[cc][i] = (ok && p.rope && key < p.T)
+                          ? *reinterpret_cast<const float4 *>(row + ((8 * (2 * ch + cc) + (i ^ (j & 7))) << 4))
+                          : make_float4(p.scale, 0.f, p.scale, 0.f);
+    }
+    if (named_barrier_and(4, 256, ok)) {
       tc::fence_after_sync();
       const uint32_t stage = sb + kOffStage;
       unsigned char *stage_p = smem + kOffStage;
@@ -707,6 +746,8 @@ __global__ void __launch_bounds__(kThr, 1)
         bulk_wait_group_read0();   // shared memory may be released; the writes complete on their own
       }
     }
+    // a RoPE copy still in flight (after a timeout) lands before the CTA exits
+    if (rope_issued) mbar_wait_bounded(bar(kBarRope), 0, 2000000000ull);
   }
   tc::fence_before_sync();
   __syncthreads();
@@ -875,7 +916,7 @@ __global__ void __launch_bounds__(kThr, 1)
         for (int c = 0; c < 32; ++c) {
           const int q = qbase + c;
           cs[c] = !p.rope ? make_float2(p.scale, 0.f)
-                  : q < p.T ? p.ws.rope[q * (kD / 2) + (d >> 1)] : make_float2(0.f, 0.f);
+                  : q < p.T ? p.ws.rope[rope_slot(q, d >> 1)] : make_float2(0.f, 0.f);
         }
         float *dst = p.dq + ((static_cast<size_t>(w.b) * p.T + qbase) * p.Hq + w.h) * kD + d;
 #pragma unroll
