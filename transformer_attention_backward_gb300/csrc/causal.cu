@@ -82,10 +82,11 @@ constexpr int kHeadGroup = 8;               // kv kernel: (batch, KV head) pairs
 // dP and, last, dV, which comes earlier in the block; after dV the slot
 // stages the block's dS^T rows for their bulk copy to the workspace before
 // it is refilled), so each block's copies are issued well before its first
-// product; the block's lse and
-// delta (1 KB) ride with its Q copy into a 2-deep ring of their own, freed
-// by the softmax warps.  Once the last products have completed, the Q and
-// dO rings (160 KB) stage the dK and dV tiles of the epilogue.
+// product; the block's lse and delta (1 KB) ride with its Q copy into a
+// 2-deep ring of their own, freed by the softmax warps.  At the end the K / V
+// region stages the dV tiles (after the last dV), two Q slots the key
+// block's RoPE rows (after the last dP) and the dO ring the dK tiles (after
+// the last dK).
 constexpr int kKvBQ = 128;               // queries per kv block (two dS^T tiles)
 constexpr int kOffK = 0;                 // [2 D-halves][128 keys][128 B], 128B-swizzled
 constexpr int kOffV = 32768;
@@ -93,7 +94,6 @@ constexpr int kQStagesKv = 3, kDOStages = 2, kLDStages = 2;
 constexpr int kBlockBytes = 32768;       // one Q or dO block
 constexpr int kOffQ = 65536;
 constexpr int kOffDO = kOffQ + kQStagesKv * kBlockBytes;
-constexpr int kOffStage = kOffQ;         // epilogue staging: dK tiles, then dV tiles
 constexpr int kHalfQ = 16384;            // one 64-dim half of a Q / dO block
 constexpr int kOffLD = kOffDO + kDOStages * kBlockBytes;   // per slot: lse2 [128] f32, delta [128] f32
 constexpr int kOffBar = kOffLD + kLDStages * 1024;
@@ -103,14 +103,13 @@ enum {
   kBarKV = 0, kBarV = 1, kBarQFull = 2, kBarQEmpty = kBarQFull + kQStagesKv, kBarDOFull = kBarQEmpty + kQStagesKv,
   kBarDOEmpty = kBarDOFull + kDOStages, kBarLDEmpty = kBarDOEmpty + kDOStages, kBarSFull = kBarLDEmpty + kLDStages,
   kBarDPFull = kBarSFull + 1, kBarPFull = kBarDPFull + 1, kBarDSFull = kBarPFull + 1, kBarDVDone = kBarDSFull + 1,
-  kBarStaged = kBarDVDone + 1, kBarRope = kBarStaged + 1, kBarDKV = kBarRope + 1,
+  kBarStaged = kBarDVDone + 1, kBarRope = kBarStaged + 1, kBarDVFinal = kBarRope + 1, kBarDKV = kBarDVFinal + 1,
   kBarFinal = kBarDKV + 1, kNumBars = kBarFinal + 1
 };
 constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
 constexpr int kOffAbort = kOffTmemSlot + 4;
 constexpr int kSmem = kOffBar + 256;
 static_assert(kOffAbort + 4 <= kSmem && kSmem <= 232448, "kv kernel shared memory");
-static_assert(2 * 65536 <= kOffLD - kOffStage, "epilogue staging fits the rings");
 
 // kv kernel TMEM columns: S^T / P^T, dP^T / dS^T (one query block each), dV, dK.
 constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 384;
@@ -376,6 +375,7 @@ __global__ void __launch_bounds__(kThr, 1)
     mbar_init(bar(kBarDVDone), 1);     // dV(n) has read dO(n) for the last time
     mbar_init(bar(kBarStaged), 256);   // every softmax thread has staged its dS row
     mbar_init(bar(kBarRope), 1);       // the key block's RoPE rows landed
+    mbar_init(bar(kBarDVFinal), 1);    // the last dV product has completed
     mbar_init(bar(kBarDKV), 1);
     mbar_init(bar(kBarFinal), 1);
     *abort_flag = 0;
@@ -501,6 +501,7 @@ __global__ void __launch_bounds__(kThr, 1)
           tc::mma_bf16_ts_w(tmem + kColDV, tmem + kColS + (kk >> 1) * 32 + (kk & 1) * 8, dOm + dso + ((kk * 2048) >> 4),
                             id_kv, (n > 0 || kk > 0));
         tc::commit_w(bar(kBarDVDone));   // dO(n) has been read for the last time
+        if (n == N - 1) tc::commit_w(bar(kBarDVFinal));
         if (n + 1 < N && !issue_s(n + 1)) break;
         if (!wtw(bar(kBarDSFull), n & 1)) break;
         tc::fence_after_sync();
@@ -512,8 +513,7 @@ __global__ void __launch_bounds__(kThr, 1)
         if (n + 1 < N && !issue_dp(n + 1)) break;
       }
       tc::commit_w(bar(kBarDKV));
-      tc::commit_w(bar(kBarFinal));
-      mbar_wait_bounded(bar(kBarFinal), 0, 2000000000ull);   // every MMA has completed
+      tc::commit_w(bar(kBarFinal));   // waited for after the epilogue
     }
   } else if (warp == 3) {
     // ============================ dS copy warp ============================
@@ -534,7 +534,7 @@ __global__ void __launch_bounds__(kThr, 1)
       }
       bulk_wait_group0();
     }
-    named_barrier(3, 288);
+    __syncwarp();
   } else if (warp >= 4) {
     // ============================ softmax warps ===========================
     // Warp w covers the 32-key TMEM lane quarter w % 4 and half g of the 128
@@ -679,75 +679,89 @@ __global__ void __launch_bounds__(kThr, 1)
         mbar_arrive(bar(kBarStaged));
       }
     }
-    // The last dS copies have read the rings before the epilogue reuses them
-    // (the second group's dV tiles cover the first dO slot).
-    named_barrier(3, 288);
-    // ---- dK (scale + RoPE backward) and dV epilogues.  Group g takes the
-    // 32-column chunks 2g and 2g + 1 of both.  Every MMA has completed once
-    // DKV fires, and the producer has nothing left to load, so the Q / dO
-    // stages are free: dK and dV are staged there as 128B-swizzled [128 rows]
-    // [32] fp32 tiles and one lane per group stores its four with TMA (rows
-    // past T are not written).  Each thread first takes its key's RoPE
-    // entries from the two Q slots they were copied to; all 256 threads agree
-    // on the outcome of the waits and have read the table before any tile is
-    // staged over it.
-    float4 cs[2][8];
-    bool ok = wtw(bar(kBarDKV), 0);
-    if (p.rope) ok = ok && wtw(bar(kBarRope), 0);
-    {
-      const unsigned char *row =
-          smem + kOffQ + ((j < 64 ? N : N + 1) % kQStagesKv) * kBlockBytes + (j & 63) * 512;
-#pragma unroll
-      for (int cc = 0; cc < 2; ++cc)
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-          cs[cc][i] = (ok && p.rope && key < p.T)
-                          ? *reinterpret_cast<const float4 *>(row + ((8 * (2 * ch + cc) + (i ^ (j & 7))) << 4))
-                          : make_float4(p.scale, 0.f, p.scale, 0.f);
-    }
-    if (named_barrier_and(4, 256, ok)) {
-      tc::fence_after_sync();
-      const uint32_t stage = sb + kOffStage;
-      unsigned char *stage_p = smem + kOffStage;
-#pragma unroll
-      for (int cc = 0; cc < 2; ++cc) {
-        const int c = 2 * ch + cc;
-        float v[32], u[32];
-        tc::ld32x2_wait(tmem + lanebase + kColDK + 32 * c, tmem + lanebase + kColDV + 32 * c, v, u);
-        unsigned char *krow = stage_p + c * 16384 + j * 128;
-        unsigned char *vrow = stage_p + 65536 + c * 16384 + j * 128;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const float *x = v + 4 * i;   // pairs (4i, 4i+1), (4i+2, 4i+3); the table holds scale * (cos, sin)
-          const float4 t = cs[cc][i];
-          const int o = (i ^ (j & 7)) << 4;
-          *reinterpret_cast<float4 *>(krow + o) =
-              make_float4(x[0] * t.x + x[1] * t.y, -x[0] * t.y + x[1] * t.x, x[2] * t.z + x[3] * t.w,
-                          -x[2] * t.w + x[3] * t.z);
-          *reinterpret_cast<float4 *>(vrow + o) = make_float4(u[4 * i], u[4 * i + 1], u[4 * i + 2], u[4 * i + 3]);
-        }
-      }
-      fence_proxy_async_smem();
-      named_barrier(1 + ch, 128);
-      if (qd == 0 && lane == 0) {
-        // with the head group split over CTAs, each adds its partial sums
-        // into the zeroed outputs
-        for (int cc = 0; cc < 2; ++cc) {
-          const int c = 2 * ch + cc;
-          if (p.hsplit > 1) {
-            tma_reduce_add_4d(&tmdK, stage + c * 16384, 32 * c, kvh, k0, b);
-            tma_reduce_add_4d(&tmdV, stage + 65536 + c * 16384, 32 * c, kvh, k0, b);
-          } else {
-            tma_store_4d(&tmdK, stage + c * 16384, 32 * c, kvh, k0, b);
-            tma_store_4d(&tmdV, stage + 65536 + c * 16384, 32 * c, kvh, k0, b);
-          }
-        }
-        bulk_commit_group();
-        bulk_wait_group_read0();   // shared memory may be released; the writes complete on their own
-      }
-    }
     // a RoPE copy still in flight (after a timeout) lands before the CTA exits
     if (rope_issued) mbar_wait_bounded(bar(kBarRope), 0, 2000000000ull);
+  }
+  if (warp < 4) {
+    // ===================== dK / dV epilogue (warps 0-3) ====================
+    // Warp w, done with its own role, takes TMEM lane quarter w: 32 key rows,
+    // all 128 columns of dV, then of dK, staged as four 128B-swizzled
+    // [128 rows][32] fp32 tiles and written by TMA tensor stores (rows past T
+    // are not written; with the head group split over CTAs the partial sums
+    // are added into the zeroed outputs).  dV goes out as soon as the last dV
+    // product has completed, while the softmax warps still work on the last
+    // block; its tiles take the K / V region, which no product reads after
+    // the last S and dP.  dK follows the last dK product; its tiles take the
+    // dO ring, whose last workspace copy warp 3 has seen read before it got
+    // here, and its RoPE rows come from the two Q slots the softmax warps
+    // filled.  The four warps agree on each outcome at their named barrier.
+    const int jr = 32 * warp + lane;
+    const int keyr = k0 + jr;
+    const uint32_t lb = static_cast<uint32_t>(32 * warp) << 16;
+    bool ok = wtw(bar(kBarDVFinal), 0);
+    if (ok) {
+      tc::fence_after_sync();
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        float u[32];
+        tc::ld32_wait(tmem + lb + kColDV + 32 * c, u);
+        unsigned char *vrow = smem + kOffK + c * 16384 + jr * 128;
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          *reinterpret_cast<float4 *>(vrow + ((i ^ (jr & 7)) << 4)) =
+              make_float4(u[4 * i], u[4 * i + 1], u[4 * i + 2], u[4 * i + 3]);
+      }
+    }
+    fence_proxy_async_smem();
+    ok = named_barrier_and(5, 128, ok);
+    if (ok && warp == 0 && lane == 0) {
+      for (int c = 0; c < 4; ++c) {
+        if (p.hsplit > 1)
+          tma_reduce_add_4d(&tmdV, sb + kOffK + c * 16384, 32 * c, kvh, k0, b);
+        else
+          tma_store_4d(&tmdV, sb + kOffK + c * 16384, 32 * c, kvh, k0, b);
+      }
+      bulk_commit_group();
+    }
+    bool okk = ok && wtw(bar(kBarDKV), 0);
+    if (p.rope) okk = okk && wtw(bar(kBarRope), 0);
+    if (okk) {
+      tc::fence_after_sync();
+      const unsigned char *rrow =
+          smem + kOffQ + ((jr < 64 ? N : N + 1) % kQStagesKv) * kBlockBytes + (jr & 63) * 512;
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        float v[32];
+        tc::ld32_wait(tmem + lb + kColDK + 32 * c, v);
+        unsigned char *krow = smem + kOffDO + c * 16384 + jr * 128;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          // pairs (4i, 4i+1), (4i+2, 4i+3); the table holds scale * (cos, sin)
+          const float4 t = (p.rope && keyr < p.T)
+                               ? *reinterpret_cast<const float4 *>(rrow + ((8 * c + (i ^ (jr & 7))) << 4))
+                               : make_float4(p.scale, 0.f, p.scale, 0.f);
+          const float *x = v + 4 * i;
+          *reinterpret_cast<float4 *>(krow + ((i ^ (jr & 7)) << 4)) =
+              make_float4(x[0] * t.x + x[1] * t.y, -x[0] * t.y + x[1] * t.x, x[2] * t.z + x[3] * t.w,
+                          -x[2] * t.w + x[3] * t.z);
+        }
+      }
+    }
+    fence_proxy_async_smem();
+    okk = named_barrier_and(5, 128, okk);
+    if (warp == 0 && lane == 0) {
+      if (okk) {
+        for (int c = 0; c < 4; ++c) {
+          if (p.hsplit > 1)
+            tma_reduce_add_4d(&tmdK, sb + kOffDO + c * 16384, 32 * c, kvh, k0, b);
+          else
+            tma_store_4d(&tmdK, sb + kOffDO + c * 16384, 32 * c, kvh, k0, b);
+        }
+        bulk_commit_group();
+      }
+      bulk_wait_group_read0();   // shared memory may be released; the writes complete on their own
+    }
+    if (warp == 1) mbar_wait_bounded(bar(kBarFinal), 0, 2000000000ull);   // every MMA has completed
   }
   tc::fence_before_sync();
   __syncthreads();
