@@ -534,7 +534,8 @@ __global__ void __launch_bounds__(kThr, 1)
       }
       bulk_wait_group0();
     }
-    __syncwarp();
+    // the softmax warps stage dK in the dO ring once the last copy has read it
+    named_barrier(3, 288);
   } else if (warp >= 4) {
     // ============================ softmax warps ===========================
     // Warp w covers the 32-key TMEM lane quarter w % 4 and half g of the 128
@@ -679,42 +680,34 @@ __global__ void __launch_bounds__(kThr, 1)
         mbar_arrive(bar(kBarStaged));
       }
     }
-    // a RoPE copy still in flight (after a timeout) lands before the CTA exits
-    if (rope_issued) mbar_wait_bounded(bar(kBarRope), 0, 2000000000ull);
-  }
-  if (warp < 4) {
-    // ===================== dK / dV epilogue (warps 0-3) ====================
-    // Warp w, done with its own role, takes TMEM lane quarter w: 32 key rows,
-    // all 128 columns of dV, then of dK, staged as four 128B-swizzled
+    // ---- dK (scale + RoPE backward) and dV epilogues.  Group ch takes the
+    // 32-column chunks 2 ch and 2 ch + 1 of both, staged as 128B-swizzled
     // [128 rows][32] fp32 tiles and written by TMA tensor stores (rows past T
     // are not written; with the head group split over CTAs the partial sums
-    // are added into the zeroed outputs).  dV goes out as soon as the last dV
-    // product has completed, while the softmax warps still work on the last
-    // block; its tiles take the K / V region, which no product reads after
-    // the last S and dP.  dK follows the last dK product; its tiles take the
-    // dO ring, whose last workspace copy warp 3 has seen read before it got
-    // here, and its RoPE rows come from the two Q slots the softmax warps
-    // filled.  The four warps agree on each outcome at their named barrier.
-    const int jr = 32 * warp + lane;
-    const int keyr = k0 + jr;
-    const uint32_t lb = static_cast<uint32_t>(32 * warp) << 16;
-    bool ok = wtw(bar(kBarDVFinal), 0);
-    if (ok) {
+    // are added into the zeroed outputs).  dV first, as soon as the last dV
+    // product has completed, into the K / V region (no product reads it
+    // after the last S and dP); then dK after the last dK product, into the
+    // dO ring once the copy warp has seen its last workspace copy read, with
+    // the RoPE rows from the two Q slots filled above.  All 256 threads agree
+    // on each outcome at their named barriers.
+    bool eok = wtw(bar(kBarDVFinal), 0);
+    if (eok) {
       tc::fence_after_sync();
-#pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
+#pragma unroll
+      for (int cc = 0; cc < 2; ++cc) {
+        const int c = 2 * ch + cc;
         float u[32];
-        tc::ld32_wait(tmem + lb + kColDV + 32 * c, u);
-        unsigned char *vrow = smem + kOffK + c * 16384 + jr * 128;
+        tc::ld32_wait(tmem + lanebase + kColDV + 32 * c, u);
+        unsigned char *vrow = smem + kOffK + c * 16384 + j * 128;
 #pragma unroll
         for (int i = 0; i < 8; ++i)
-          *reinterpret_cast<float4 *>(vrow + ((i ^ (jr & 7)) << 4)) =
+          *reinterpret_cast<float4 *>(vrow + ((i ^ (j & 7)) << 4)) =
               make_float4(u[4 * i], u[4 * i + 1], u[4 * i + 2], u[4 * i + 3]);
       }
     }
     fence_proxy_async_smem();
-    ok = named_barrier_and(5, 128, ok);
-    if (ok && warp == 0 && lane == 0) {
+    eok = named_barrier_and(4, 256, eok);
+    if (eok && warp == 4 && lane == 0) {
       for (int c = 0; c < 4; ++c) {
         if (p.hsplit > 1)
           tma_reduce_add_4d(&tmdV, sb + kOffK + c * 16384, 32 * c, kvh, k0, b);
@@ -723,34 +716,36 @@ __global__ void __launch_bounds__(kThr, 1)
       }
       bulk_commit_group();
     }
-    bool okk = ok && wtw(bar(kBarDKV), 0);
-    if (p.rope) okk = okk && wtw(bar(kBarRope), 0);
-    if (okk) {
+    bool kok = eok && wtw(bar(kBarDKV), 0);
+    if (p.rope) kok = kok && wtw(bar(kBarRope), 0);
+    named_barrier(3, 288);
+    if (kok) {
       tc::fence_after_sync();
       const unsigned char *rrow =
-          smem + kOffQ + ((jr < 64 ? N : N + 1) % kQStagesKv) * kBlockBytes + (jr & 63) * 512;
-#pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
+          smem + kOffQ + ((j < 64 ? N : N + 1) % kQStagesKv) * kBlockBytes + (j & 63) * 512;
+#pragma unroll
+      for (int cc = 0; cc < 2; ++cc) {
+        const int c = 2 * ch + cc;
         float v[32];
-        tc::ld32_wait(tmem + lb + kColDK + 32 * c, v);
-        unsigned char *krow = smem + kOffDO + c * 16384 + jr * 128;
+        tc::ld32_wait(tmem + lanebase + kColDK + 32 * c, v);
+        unsigned char *krow = smem + kOffDO + c * 16384 + j * 128;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           // pairs (4i, 4i+1), (4i+2, 4i+3); the table holds scale * (cos, sin)
-          const float4 t = (p.rope && keyr < p.T)
-                               ? *reinterpret_cast<const float4 *>(rrow + ((8 * c + (i ^ (jr & 7))) << 4))
+          const float4 t = (p.rope && key < p.T)
+                               ? *reinterpret_cast<const float4 *>(rrow + ((8 * c + (i ^ (j & 7))) << 4))
                                : make_float4(p.scale, 0.f, p.scale, 0.f);
           const float *x = v + 4 * i;
-          *reinterpret_cast<float4 *>(krow + ((i ^ (jr & 7)) << 4)) =
+          *reinterpret_cast<float4 *>(krow + ((i ^ (j & 7)) << 4)) =
               make_float4(x[0] * t.x + x[1] * t.y, -x[0] * t.y + x[1] * t.x, x[2] * t.z + x[3] * t.w,
                           -x[2] * t.w + x[3] * t.z);
         }
       }
     }
     fence_proxy_async_smem();
-    okk = named_barrier_and(5, 128, okk);
-    if (warp == 0 && lane == 0) {
-      if (okk) {
+    kok = named_barrier_and(4, 256, kok);
+    if (warp == 4 && lane == 0) {
+      if (kok) {
         for (int c = 0; c < 4; ++c) {
           if (p.hsplit > 1)
             tma_reduce_add_4d(&tmdK, sb + kOffDO + c * 16384, 32 * c, kvh, k0, b);
@@ -761,8 +756,10 @@ __global__ void __launch_bounds__(kThr, 1)
       }
       bulk_wait_group_read0();   // shared memory may be released; the writes complete on their own
     }
-    if (warp == 1) mbar_wait_bounded(bar(kBarFinal), 0, 2000000000ull);   // every MMA has completed
+    // a RoPE copy still in flight (after a timeout) lands before the CTA exits
+    if (rope_issued) mbar_wait_bounded(bar(kBarRope), 0, 2000000000ull);
   }
+  if (warp == 1) mbar_wait_bounded(bar(kBarFinal), 0, 2000000000ull);   // every MMA has completed
   tc::fence_before_sync();
   __syncthreads();
   if (warp == 2) {
