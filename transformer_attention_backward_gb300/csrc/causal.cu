@@ -380,6 +380,26 @@ __global__ void __launch_bounds__(kThr, 1)
     mbar_init(bar(kBarFinal), 1);
     *abort_flag = 0;
     fence_barrier_init();
+    // This thread is the producer: K, Q(0) with its lse / delta, then V and
+    // dO(0) go out before the TMEM allocation and the block barrier.  The
+    // first S product waits for 64 KB rather than for every block's 128 KB.
+    prefetch_tensormap(&tmK);
+    prefetch_tensormap(&tmQ);
+    mbar_arrive_expect_tx(bar(kBarKV), 2 * 16384);
+    for (int hx = 0; hx < 2; ++hx) tma_load_4d(sb + kOffK + hx * 16384, &tmK, hx * 64, kvh, k0, b, bar(kBarKV));
+    mbar_arrive_expect_tx(bar(kBarQFull), 2 * kHalfQ + 2 * 512);
+    for (int hx = 0; hx < 2; ++hx)
+      tma_load_4d(sb + kOffQ + hx * kHalfQ, &tmQ, hx * 64, h_first, kb * kKvBQ, b, bar(kBarQFull));
+    const size_t ro = (static_cast<size_t>(b) * p.Hq + h_first) * p.Tp + kb * kKvBQ;
+    bulk_load(sb + kOffLD, p.ws.lse2 + ro, 512, bar(kBarQFull));
+    bulk_load(sb + kOffLD + 512, p.ws.delta + ro, 512, bar(kBarQFull));
+    prefetch_tensormap(&tmV);
+    mbar_arrive_expect_tx(bar(kBarV), 2 * 16384);
+    for (int hx = 0; hx < 2; ++hx) tma_load_4d(sb + kOffV + hx * 16384, &tmV, hx * 64, kvh, k0, b, bar(kBarV));
+    prefetch_tensormap(&tmDO);
+    mbar_arrive_expect_tx(bar(kBarDOFull), 2 * kHalfQ);
+    for (int hx = 0; hx < 2; ++hx)
+      tma_load_4d(sb + kOffDO + hx * kHalfQ, &tmDO, hx * 64, h_first, kb * kKvBQ, b, bar(kBarDOFull));
   }
   if (warp == 2) tc::tmem_alloc(sb + kOffTmemSlot, 512);
   tc::fence_before_sync();
@@ -390,40 +410,32 @@ __global__ void __launch_bounds__(kThr, 1)
   if (warp == 0) {
     // ============================ TMA producer ============================
     if (lane == 0) {
-      prefetch_tensormap(&tmQ);
-      prefetch_tensormap(&tmDO);
-      prefetch_tensormap(&tmK);
-      prefetch_tensormap(&tmV);
-      // K first, then Q(0), then V and dO(0): the first S product waits for
-      // 64 KB rather than for every block's 128 KB
-      mbar_arrive_expect_tx(bar(kBarKV), 2 * 16384);
-      for (int hx = 0; hx < 2; ++hx) tma_load_4d(sb + kOffK + hx * 16384, &tmK, hx * 64, kvh, k0, b, bar(kBarKV));
-      bool v_issued = false;
-      int q_issued = 0, d_issued = 0;
+      // K, Q(0), V and dO(0) are already on their way (issued with the barriers)
+      const bool v_issued = true;
+      int q_issued = 1, d_issued = 1;
       for (int n = 0; n < N; ++n) {
         const int h = h_first + n / nq;
         const int q0 = (kb + n % nq) * kKvBQ;
         const int qs = n % kQStagesKv, ds = n % kDOStages;
         const int ls = n % kLDStages;
-        if (!wt(bar(kBarQEmpty + qs), ((n / kQStagesKv) & 1) ^ 1)) break;
-        if (!wt(bar(kBarLDEmpty + ls), ((n / kLDStages) & 1) ^ 1)) break;
-        mbar_arrive_expect_tx(bar(kBarQFull + qs), 2 * kHalfQ + 2 * 512);
-        for (int hx = 0; hx < 2; ++hx)
-          tma_load_4d(sb + kOffQ + qs * kBlockBytes + hx * kHalfQ, &tmQ, hx * 64, h, q0, b, bar(kBarQFull + qs));
-        const size_t ro = (static_cast<size_t>(b) * p.Hq + h) * p.Tp + q0;
-        bulk_load(sb + kOffLD + ls * 1024, p.ws.lse2 + ro, 512, bar(kBarQFull + qs));
-        bulk_load(sb + kOffLD + ls * 1024 + 512, p.ws.delta + ro, 512, bar(kBarQFull + qs));
-        q_issued = n + 1;
-        if (!v_issued) {
-          mbar_arrive_expect_tx(bar(kBarV), 2 * 16384);
-          for (int hx = 0; hx < 2; ++hx) tma_load_4d(sb + kOffV + hx * 16384, &tmV, hx * 64, kvh, k0, b, bar(kBarV));
-          v_issued = true;
+        if (n > 0) {
+          if (!wt(bar(kBarQEmpty + qs), ((n / kQStagesKv) & 1) ^ 1)) break;
+          if (!wt(bar(kBarLDEmpty + ls), ((n / kLDStages) & 1) ^ 1)) break;
+          mbar_arrive_expect_tx(bar(kBarQFull + qs), 2 * kHalfQ + 2 * 512);
+          for (int hx = 0; hx < 2; ++hx)
+            tma_load_4d(sb + kOffQ + qs * kBlockBytes + hx * kHalfQ, &tmQ, hx * 64, h, q0, b, bar(kBarQFull + qs));
+          const size_t ro = (static_cast<size_t>(b) * p.Hq + h) * p.Tp + q0;
+          bulk_load(sb + kOffLD + ls * 1024, p.ws.lse2 + ro, 512, bar(kBarQFull + qs));
+          bulk_load(sb + kOffLD + ls * 1024 + 512, p.ws.delta + ro, 512, bar(kBarQFull + qs));
+          q_issued = n + 1;
         }
-        if (!wt(bar(kBarDOEmpty + ds), ((n / kDOStages) & 1) ^ 1)) break;
-        mbar_arrive_expect_tx(bar(kBarDOFull + ds), 2 * kHalfQ);
-        for (int hx = 0; hx < 2; ++hx)
-          tma_load_4d(sb + kOffDO + ds * kBlockBytes + hx * kHalfQ, &tmDO, hx * 64, h, q0, b, bar(kBarDOFull + ds));
-        d_issued = n + 1;
+        if (n > 0) {
+          if (!wt(bar(kBarDOEmpty + ds), ((n / kDOStages) & 1) ^ 1)) break;
+          mbar_arrive_expect_tx(bar(kBarDOFull + ds), 2 * kHalfQ);
+          for (int hx = 0; hx < 2; ++hx)
+            tma_load_4d(sb + kOffDO + ds * kBlockBytes + hx * kHalfQ, &tmDO, hx * 64, h, q0, b, bar(kBarDOFull + ds));
+          d_issued = n + 1;
+        }
       }
       if (*abort_flag) {
         // let copies already in flight land before the CTA can exit
