@@ -320,6 +320,10 @@ __global__ void __launch_bounds__(kThr, 1)
   extern __shared__ __align__(1024) unsigned char smem[];
   const uint32_t sb = smem_u32(smem);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // The dq kernel (launched as this grid's programmatic dependent) may take
+  // the SMs this grid's last CTAs leave idle; it waits for this grid's
+  // completion before it reads any dS tile.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (sb & 1023) {
     if (tid == 0) atomicOr(p.wait.err, kErrSmemAlign);
     return;
@@ -848,6 +852,9 @@ __global__ void __launch_bounds__(kThr, 1)
     if (lane == 0) {
       prefetch_tensormap(&tmK);
       const uint64_t keep = l2_evict_last(), stream = l2_evict_first();
+      // the dS tiles come from the kv kernel: wait for that grid to have
+      // completed (a no-op when this grid was launched after it completed)
+      asm volatile("griddepcontrol.wait;" ::: "memory");
       int g = 0;   // steps issued so far (ring position)
       bool ok = true;
       for (int r = 0, it = nth(0); ok && it < items; it = nth(++r)) {
@@ -1096,7 +1103,20 @@ cudaError_t launch_attn_bwd_causal(const void *q, const void *k, const void *v, 
   e = ensure_dynamic_smem(reinterpret_cast<const void *>(causal_dq_tc_kernel), kQSmem);
   if (e != cudaSuccess) return e;
   const long long dq_grid = std::min<long long>(dq_ctas, sms);
-  causal_dq_tc_kernel<<<static_cast<unsigned>(dq_grid), kThr, kQSmem, st>>>(tk, p);
+  // launched as the kv grid's programmatic dependent: its CTAs start on SMs
+  // the kv grid's tail leaves idle and set up while the last kv CTAs finish
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(dq_grid));
+  cfg.blockDim = dim3(kThr);
+  cfg.dynamicSmemBytes = kQSmem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, causal_dq_tc_kernel, tk, p);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
