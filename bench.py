@@ -488,6 +488,8 @@ def causal_kernel_figures(bd, shape, peaks, kind):
             e.update(gbs=round(gbs, 1), frac=round(gbs / peaks["hbm_gbs"], 4))
         out[name] = e
     out["peak_kind"] = kind + " (burst)"
+    out["note"] = ("the dq kernel is the kv kernel's programmatic dependent: it starts on SMs the kv tail leaves "
+                   "idle and waits there for the kv grid, so its device time overlaps the kv kernel's end")
     return out
 
 
