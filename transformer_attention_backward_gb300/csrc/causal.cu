@@ -925,6 +925,17 @@ __global__ void __launch_bounds__(kThr, 1)
     const uint32_t lanebase = static_cast<uint32_t>(32 * qd) << 16;
     const bool odd = d & 1;
     const size_t qstride = static_cast<size_t>(p.Hq) * kD;
+    // RoPE: the table holds scale * e^{i (pos0 + t) theta} for pair d / 2;
+    // consecutive positions differ by the rotation e^{i theta}, taken once
+    // from the first two rows.  A chunk reads the table at every 8th query
+    // and rotates in between (7 complex products add ~1e-5 relative error),
+    // so the epilogue waits for 4 table reads instead of 32.
+    float2 stp = make_float2(1.f, 0.f);
+    if (p.rope && p.T >= 2) {
+      const float2 t0 = p.ws.rope[rope_slot(0, d >> 1)], t1 = p.ws.rope[rope_slot(1, d >> 1)];
+      const float is2 = 1.f / (p.scale * p.scale);
+      stp = make_float2((t1.x * t0.x + t1.y * t0.y) * is2, (t1.y * t0.x - t1.x * t0.y) * is2);
+    }
     int j = 0;
     for (int r = 0, it = nth(0); it < items; it = nth(++r), ++j) {
       const Item w = item(it);
@@ -938,15 +949,24 @@ __global__ void __launch_bounds__(kThr, 1)
 #pragma unroll
       for (int cc = 0; cc < 2; ++cc) {
         const int qbase = w.m * kBK + 64 * ch + 32 * cc;
-        // pair (2i, 2i+1) rotated by -theta; the table holds scale * (cos,
-        // sin).  All 32 loads come before the first store: a load after a
-        // store to possibly the same memory would wait for it.
+        // pair (2i, 2i+1) rotated by -theta; the factors are scale * (cos,
+        // sin).  The table reads come before the first store: a load after
+        // a store to possibly the same memory would wait for it.
         float2 cs[32];
+        if (!p.rope) {
 #pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          const int q = qbase + c;
-          cs[c] = !p.rope ? make_float2(p.scale, 0.f)
-                  : q < p.T ? p.ws.rope[rope_slot(q, d >> 1)] : make_float2(0.f, 0.f);
+          for (int c = 0; c < 32; ++c) cs[c] = make_float2(p.scale, 0.f);
+        } else {
+#pragma unroll
+          for (int g8 = 0; g8 < 4; ++g8) {
+            const int q = qbase + 8 * g8;
+            cs[8 * g8] = q < p.T ? p.ws.rope[rope_slot(q, d >> 1)] : make_float2(0.f, 0.f);
+          }
+#pragma unroll
+          for (int g8 = 0; g8 < 4; ++g8)
+#pragma unroll
+            for (int c = 8 * g8 + 1; c < 8 * g8 + 8; ++c)
+              cs[c] = make_float2(cs[c - 1].x * stp.x - cs[c - 1].y * stp.y, cs[c - 1].x * stp.y + cs[c - 1].y * stp.x);
         }
         float *dst = p.dq + ((static_cast<size_t>(w.b) * p.T + qbase) * p.Hq + w.h) * kD + d;
 #pragma unroll
