@@ -166,7 +166,7 @@ CausalWs carve(void *ws, int B, int T, int Hq, int D) {
 
 // delta and lse*log2(e) per (b, h, t < Tp) and, with RoPE, the table
 // scale * (cos, sin) of theta = (pos0 + t) * base^(-2i/D).  A half-warp takes
-// kPrepRows rows of o and dout, consecutive in (b, h, t) order (16 bytes per
+// kPrepRows rows of o and dout, consecutive in (b, t, h) order (16 bytes per
 // lane and tensor, all loads issued before the first reduction); table
 // entries are strided over the grid's threads; padding entries t in [T, Tp) get delta 0 and lse +inf,
 // one per thread.  The RoPE angle is formed and reduced modulo 2 pi in
@@ -212,16 +212,16 @@ __global__ void __launch_bounds__(256) causal_prep_kernel(const __nv_bfloat16 *_
     delta[bh * Tp + t] = 0.f;
     lse2[bh * Tp + t] = INFINITY;
   }
-  // Rows are taken in (b, h, t) order: a half-warp's rows are consecutive
-  // positions of one head, so the delta / lse accesses are contiguous; each
-  // row of o and dout is still one 256-byte segment.
+  // Rows are taken in memory order (b, t, h): a block's rows of o and dout
+  // are one contiguous stretch (DRAM pages are read whole), and only the
+  // small delta / lse accesses are strided.
   const long long nrows = static_cast<long long>(B) * T * Hq;
   const long long r0 = (gid >> 4) * kPrepRows;
-  int tt = static_cast<int>(r0 % T), hh, bb;
+  int hh = static_cast<int>(r0 % Hq), tt, bb;
   {
-    const long long bh = r0 / T;
-    hh = static_cast<int>(bh % Hq);
-    bb = static_cast<int>(bh / Hq);
+    const long long bt = r0 / Hq;
+    tt = static_cast<int>(bt % T);
+    bb = static_cast<int>(bt / T);
   }
   int rh[kPrepRows], rt[kPrepRows], rb[kPrepRows];
 #pragma unroll
@@ -229,10 +229,10 @@ __global__ void __launch_bounds__(256) causal_prep_kernel(const __nv_bfloat16 *_
     rh[k] = hh;
     rt[k] = tt;
     rb[k] = bb;
-    if (++tt == T) {
-      tt = 0;
-      if (++hh == Hq) {
-        hh = 0;
+    if (++hh == Hq) {
+      hh = 0;
+      if (++tt == T) {
+        tt = 0;
         ++bb;
       }
     }
