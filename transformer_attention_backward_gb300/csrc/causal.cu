@@ -604,23 +604,30 @@ __global__ void __launch_bounds__(kThr, 1)
         float (&hi)[32] = *reinterpret_cast<float (*)[32]>(&P[32]);
         tc::ld32x2_wait(tS, tS + 32, lo, hi);
       }
+      // two copies of the loop, so that the common, unmasked one is straight-line code
+      auto p_loop = [&](const bool masked) {
 #pragma unroll
-      for (int e = 0; e < 64; e += 4) {
-        const float4 l4 = *reinterpret_cast<const float4 *>(lse2 + e);
-        P[e] = fast_exp2(fmaf(P[e], sl2, -l4.x));
-        P[e + 1] = fast_exp2(fmaf(P[e + 1], sl2, -l4.y));
-        P[e + 2] = fast_exp2(fmaf(P[e + 2], sl2, -l4.z));
-        P[e + 3] = fast_exp2(fmaf(P[e + 3], sl2, -l4.w));
-        if (diag) {
-          const int q = q0 + e;
-          P[e] = key <= q ? P[e] : 0.f;
-          P[e + 1] = key <= q + 1 ? P[e + 1] : 0.f;
-          P[e + 2] = key <= q + 2 ? P[e + 2] : 0.f;
-          P[e + 3] = key <= q + 3 ? P[e + 3] : 0.f;
+        for (int e = 0; e < 64; e += 4) {
+          const float4 l4 = *reinterpret_cast<const float4 *>(lse2 + e);
+          P[e] = fast_exp2(fmaf(P[e], sl2, -l4.x));
+          P[e + 1] = fast_exp2(fmaf(P[e + 1], sl2, -l4.y));
+          P[e + 2] = fast_exp2(fmaf(P[e + 2], sl2, -l4.z));
+          P[e + 3] = fast_exp2(fmaf(P[e + 3], sl2, -l4.w));
+          if (masked) {
+            const int q = q0 + e;
+            P[e] = key <= q ? P[e] : 0.f;
+            P[e + 1] = key <= q + 1 ? P[e + 1] : 0.f;
+            P[e + 2] = key <= q + 2 ? P[e + 2] : 0.f;
+            P[e + 3] = key <= q + 3 ? P[e + 3] : 0.f;
+          }
+          pk[e / 2] = pack_bf16x2(P[e], P[e + 1]);
+          pk[e / 2 + 1] = pack_bf16x2(P[e + 2], P[e + 3]);
         }
-        pk[e / 2] = pack_bf16x2(P[e], P[e + 1]);
-        pk[e / 2 + 1] = pack_bf16x2(P[e + 2], P[e + 3]);
-      }
+      };
+      if (diag)
+        p_loop(true);
+      else
+        p_loop(false);
       }
       // chunk c (16 queries = 8 packed columns) goes to column 32 (c / 2) +
       // 8 (c % 2) of this half: the A-operand layout of the dV product
