@@ -568,6 +568,7 @@ __global__ void __launch_bounds__(kThr, 1)
     const uint32_t tS = tmem + lanebase + kColS + 64 * ch;
     const uint32_t tD = tmem + lanebase + kColDP + 64 * ch;
     bool rope_issued = false;
+    int blocks_done = 0;
     for (int n = 0; n < N; ++n) {
       const int h = h_first + n / nq;
       const int qb = kb + n % nq;                       // 128-query block
@@ -645,19 +646,6 @@ __global__ void __launch_bounds__(kThr, 1)
       // ---- dS = P (dP - delta), to TMEM (A operand of dK) and to the workspace
       if (!wtw(bar(kBarDPFull), n & 1)) break;
       tc::fence_after_sync();
-      if (n == N - 1 && p.rope && warp == 4 && lane == 0) {
-        // dP(N - 1) has completed, so have dK(N - 2) and dK(N - 3): the two
-        // Q slots other than Q(N - 1)'s are free.  They take this key
-        // block's RoPE rows for the dK epilogue (keys 0-63, then 64-127).
-        const int rows = min(kBK, p.T - k0);
-        mbar_arrive_expect_tx(bar(kBarRope), rows * 512);
-        bulk_load(sb + kOffQ + (N % kQStagesKv) * kBlockBytes, p.ws.rope + k0 * (kD / 2), min(rows, 64) * 512,
-                  bar(kBarRope));
-        if (rows > 64)
-          bulk_load(sb + kOffQ + ((N + 1) % kQStagesKv) * kBlockBytes, p.ws.rope + (k0 + 64) * (kD / 2),
-                    (rows - 64) * 512, bar(kBarRope));
-        rope_issued = true;
-      }
       uint4 U[8];   // this key row's dS^T as eight 16-byte units of 8 queries
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
@@ -702,6 +690,20 @@ __global__ void __launch_bounds__(kThr, 1)
         fence_proxy_async_smem();
         mbar_arrive(bar(kBarStaged));
       }
+      blocks_done = n + 1;
+    }
+    if (blocks_done == N && p.rope && warp == 4 && lane == 0) {
+      // dP(N - 1) has completed, so have dK(N - 2) and dK(N - 3): the two Q
+      // slots other than Q(N - 1)'s are free.  They take this key block's
+      // RoPE rows for the dK epilogue (keys 0-63, then 64-127).
+      const int rows = min(kBK, p.T - k0);
+      mbar_arrive_expect_tx(bar(kBarRope), rows * 512);
+      bulk_load(sb + kOffQ + (N % kQStagesKv) * kBlockBytes, p.ws.rope + k0 * (kD / 2), min(rows, 64) * 512,
+                bar(kBarRope));
+      if (rows > 64)
+        bulk_load(sb + kOffQ + ((N + 1) % kQStagesKv) * kBlockBytes, p.ws.rope + (k0 + 64) * (kD / 2),
+                  (rows - 64) * 512, bar(kBarRope));
+      rope_issued = true;
     }
     // ---- dK (scale + RoPE backward) and dV epilogues.  Group ch takes the
     // 32-column chunks 2 ch and 2 ch + 1 of both, staged as 128B-swizzled
