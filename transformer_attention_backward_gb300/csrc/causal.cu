@@ -312,6 +312,10 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t *>(&v);
 }
 
+// kSavedP: P comes from the saved probabilities (no S product) instead of
+// being recomputed from lse; one instantiation per form keeps the softmax
+// loop free of the test.
+template <bool kSavedP>
 __global__ void __launch_bounds__(kThr, 1)
     causal_kv_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmDO,
                         const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
@@ -482,11 +486,11 @@ __global__ void __launch_bounds__(kThr, 1)
       // With saved probabilities there is no S product: the S signal then
       // only says that the P columns are free again (every product issued
       // so far, dV(n - 1) included, has completed).
-      const bool saved_p = p.pattn != nullptr;
+      constexpr bool saved_p = kSavedP;
       auto issue_s = [&](int n) -> bool {
         if (!wtw(bar(kBarQFull + n % kQStagesKv), (n / kQStagesKv) & 1)) return false;
         tc::fence_after_sync();
-        if (!saved_p) {
+        if constexpr (!saved_p) {
           const uint64_t so = qoff(n);
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
@@ -583,7 +587,7 @@ __global__ void __launch_bounds__(kThr, 1)
       const bool diag = qb == kb;
       float P[64];
       uint32_t pk[32];
-      if (p.pattn) {
+      if constexpr (kSavedP) {
         // ---- P from the saved probabilities: this thread's key column of
         // the 64 query rows, read before the P columns are free
         const __nv_bfloat16 *pc = p.pattn + (static_cast<size_t>(b) * p.Hq + h) * p.T * p.T + key;
@@ -1124,9 +1128,10 @@ cudaError_t launch_attn_bwd_causal(const void *q, const void *k, const void *v, 
   p.scale = scale;
   p.rope = rope;
   p.wait = w;
-  e = ensure_dynamic_smem(reinterpret_cast<const void *>(causal_kv_tc_kernel), kSmem);
+  auto kv_kernel = pattn ? causal_kv_tc_kernel<true> : causal_kv_tc_kernel<false>;
+  e = ensure_dynamic_smem(reinterpret_cast<const void *>(kv_kernel), kSmem);
   if (e != cudaSuccess) return e;
-  causal_kv_tc_kernel<<<static_cast<unsigned>(kv_ctas), kThr, kSmem, st>>>(tq, tdo, tk, tv, tdk, tdv, p);
+  kv_kernel<<<static_cast<unsigned>(kv_ctas), kThr, kSmem, st>>>(tq, tdo, tk, tv, tdk, tdv, p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   e = ensure_dynamic_smem(reinterpret_cast<const void *>(causal_dq_tc_kernel), kQSmem);
