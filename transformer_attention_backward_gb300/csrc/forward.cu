@@ -220,12 +220,21 @@ __global__ void __launch_bounds__(kFThr, 1)
       const uint32_t tS = tmem + lanebase + ((n & 1) ? kFColS1 : kFColS0);
       float s[128];
       ld128_wait(tS, s);
-      const bool diag = n == m;
+      // only the diagonal block is masked; a separate copy of the loop keeps
+      // the common one free of the test
       float mb = -INFINITY;
+      if (n == m) {
 #pragma unroll
-      for (int c = 0; c < 128; ++c) {
-        s[c] = (diag && n * kFB + c > q) ? -INFINITY : s[c] * sl2;
-        mb = fmaxf(mb, s[c]);
+        for (int c = 0; c < 128; ++c) {
+          s[c] = n * kFB + c > q ? -INFINITY : s[c] * sl2;
+          mb = fmaxf(mb, s[c]);
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < 128; ++c) {
+          s[c] *= sl2;
+          mb = fmaxf(mb, s[c]);
+        }
       }
       // lazy rescale: only when some row of the warp moves its max by > 8.
       // Every phase of the O barrier (one per PV product) is waited for, in
