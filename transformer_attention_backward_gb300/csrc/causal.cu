@@ -982,12 +982,19 @@ __global__ void __launch_bounds__(kThr, 1)
               cs[c] = make_float2(cs[c - 1].x * stp.x - cs[c - 1].y * stp.y, cs[c - 1].x * stp.y + cs[c - 1].y * stp.x);
         }
         float *dst = p.dq + ((static_cast<size_t>(w.b) * p.T + qbase) * p.Hq + w.h) * kD + d;
+        // the bound is tested once per chunk: only the last chunk can pass T
+        auto store = [&](const bool bounded) {
 #pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          const float x = v[cc][c];
-          const float partner = __shfl_xor_sync(0xffffffffu, x, 1);
-          if (qbase + c < p.T) dst[c * qstride] = x * cs[c].x + (odd ? -partner : partner) * cs[c].y;
-        }
+          for (int c = 0; c < 32; ++c) {
+            const float x = v[cc][c];
+            const float partner = __shfl_xor_sync(0xffffffffu, x, 1);
+            if (!bounded || qbase + c < p.T) dst[c * qstride] = x * cs[c].x + (odd ? -partner : partner) * cs[c].y;
+          }
+        };
+        if (qbase + 32 <= p.T)
+          store(false);
+        else
+          store(true);
       }
     }
   }
