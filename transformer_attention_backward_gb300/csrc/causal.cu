@@ -43,8 +43,8 @@
 // then the dK (scale + RoPE) and dV epilogues, each half of the softmax
 // warps taking half the columns of both.  TMEM (512 columns):
 //   [0,128) S / P   [128,256) dP / dS   [256,384) dV   [384,512) dK
-// Q / dO / lse / delta of one query block (64 KB) arrive through a 2-deep
-// TMA ring.
+// Q (with lse) and dO (with delta) of one query block arrive through a
+// 3-deep and a 2-deep TMA ring.
 //
 // dq kernel (persistent, 12 warps, one CTA per SM): for each work item (128
 // queries of one head) and each key block at or before it, the K block
@@ -82,26 +82,29 @@ constexpr int kHeadGroup = 8;               // kv kernel: (batch, KV head) pairs
 // dP and, last, dV, which comes earlier in the block; after dV the slot
 // stages the block's dS^T rows for their bulk copy to the workspace before
 // it is refilled), so each block's copies are issued well before its first
-// product; the block's lse and delta (1 KB) ride with its Q copy into a
-// 2-deep ring of their own, freed by the softmax warps.  At the end the K / V
+// product.  The block's lse (512 B) rides with its Q copy into a ring of the
+// Q ring's depth and its delta (512 B) with its dO copy into one of the dO
+// ring's depth: the softmax warps are done with both before the slot they
+// ride with is released, so no copy waits for the softmax.  At the end the K / V
 // region stages the dV tiles (after the last dV), two Q slots the key
 // block's RoPE rows (after the last dP) and the dO ring the dK tiles (after
 // the last dK).
 constexpr int kKvBQ = 128;               // queries per kv block (two dS^T tiles)
 constexpr int kOffK = 0;                 // [2 D-halves][128 keys][128 B], 128B-swizzled
 constexpr int kOffV = 32768;
-constexpr int kQStagesKv = 3, kDOStages = 2, kLDStages = 2;
+constexpr int kQStagesKv = 3, kDOStages = 2;
 constexpr int kBlockBytes = 32768;       // one Q or dO block
 constexpr int kOffQ = 65536;
 constexpr int kOffDO = kOffQ + kQStagesKv * kBlockBytes;
 constexpr int kHalfQ = 16384;            // one 64-dim half of a Q / dO block
-constexpr int kOffLD = kOffDO + kDOStages * kBlockBytes;   // per slot: lse2 [128] f32, delta [128] f32
-constexpr int kOffBar = kOffLD + kLDStages * 1024;
+constexpr int kOffLse = kOffDO + kDOStages * kBlockBytes;      // per Q slot: lse2 [128] f32
+constexpr int kOffDelta = kOffLse + kQStagesKv * 512;          // per dO slot: delta [128] f32
+constexpr int kOffBar = kOffDelta + kDOStages * 512;
 
 // kv kernel barrier slots (8 bytes each) after kOffBar.
 enum {
   kBarKV = 0, kBarV = 1, kBarQFull = 2, kBarQEmpty = kBarQFull + kQStagesKv, kBarDOFull = kBarQEmpty + kQStagesKv,
-  kBarDOEmpty = kBarDOFull + kDOStages, kBarLDEmpty = kBarDOEmpty + kDOStages, kBarSFull = kBarLDEmpty + kLDStages,
+  kBarDOEmpty = kBarDOFull + kDOStages, kBarSFull = kBarDOEmpty + kDOStages,
   kBarDPFull = kBarSFull + 1, kBarPFull = kBarDPFull + 1, kBarDSFull = kBarPFull + 1, kBarDVDone = kBarDSFull + 1,
   kBarStaged = kBarDVDone + 1, kBarRope = kBarStaged + 1, kBarDVFinal = kBarRope + 1, kBarDKV = kBarDVFinal + 1,
   kBarFinal = kBarDKV + 1, kNumBars = kBarFinal + 1
@@ -375,7 +378,6 @@ __global__ void __launch_bounds__(kThr, 1)
       mbar_init(bar(kBarDOFull + s), 1);
       mbar_init(bar(kBarDOEmpty + s), 1);   // the block's dS copy has read the slot
     }
-    for (int s = 0; s < kLDStages; ++s) mbar_init(bar(kBarLDEmpty + s), 256);   // the softmax is done with it
     mbar_init(bar(kBarSFull), 1);
     mbar_init(bar(kBarDPFull), 1);
     mbar_init(bar(kBarPFull), 256);    // every softmax thread has put its P row into TMEM
@@ -388,26 +390,26 @@ __global__ void __launch_bounds__(kThr, 1)
     mbar_init(bar(kBarFinal), 1);
     *abort_flag = 0;
     fence_barrier_init();
-    // This thread is the producer: K, Q(0) with its lse / delta, then V and
-    // dO(0) go out before the TMEM allocation and the block barrier.  The
+    // This thread is the producer: K, Q(0) with its lse, then V and dO(0)
+    // with its delta go out before the TMEM allocation and the block barrier.  The
     // first S product waits for 64 KB rather than for every block's 128 KB.
     prefetch_tensormap(&tmK);
     prefetch_tensormap(&tmQ);
     mbar_arrive_expect_tx(bar(kBarKV), 2 * 16384);
     for (int hx = 0; hx < 2; ++hx) tma_load_4d(sb + kOffK + hx * 16384, &tmK, hx * 64, kvh, k0, b, bar(kBarKV));
-    mbar_arrive_expect_tx(bar(kBarQFull), 2 * kHalfQ + 2 * 512);
+    mbar_arrive_expect_tx(bar(kBarQFull), 2 * kHalfQ + 512);
     for (int hx = 0; hx < 2; ++hx)
       tma_load_4d(sb + kOffQ + hx * kHalfQ, &tmQ, hx * 64, h_first, kb * kKvBQ, b, bar(kBarQFull));
     const size_t ro = (static_cast<size_t>(b) * p.Hq + h_first) * p.Tp + kb * kKvBQ;
-    bulk_load(sb + kOffLD, p.ws.lse2 + ro, 512, bar(kBarQFull));
-    bulk_load(sb + kOffLD + 512, p.ws.delta + ro, 512, bar(kBarQFull));
+    bulk_load(sb + kOffLse, p.ws.lse2 + ro, 512, bar(kBarQFull));
     prefetch_tensormap(&tmV);
     mbar_arrive_expect_tx(bar(kBarV), 2 * 16384);
     for (int hx = 0; hx < 2; ++hx) tma_load_4d(sb + kOffV + hx * 16384, &tmV, hx * 64, kvh, k0, b, bar(kBarV));
     prefetch_tensormap(&tmDO);
-    mbar_arrive_expect_tx(bar(kBarDOFull), 2 * kHalfQ);
+    mbar_arrive_expect_tx(bar(kBarDOFull), 2 * kHalfQ + 512);
     for (int hx = 0; hx < 2; ++hx)
       tma_load_4d(sb + kOffDO + hx * kHalfQ, &tmDO, hx * 64, h_first, kb * kKvBQ, b, bar(kBarDOFull));
+    bulk_load(sb + kOffDelta, p.ws.delta + ro, 512, bar(kBarDOFull));
   }
   if (warp == 2) tc::tmem_alloc(sb + kOffTmemSlot, 512);
   tc::fence_before_sync();
@@ -425,23 +427,21 @@ __global__ void __launch_bounds__(kThr, 1)
         const int h = h_first + n / nq;
         const int q0 = (kb + n % nq) * kKvBQ;
         const int qs = n % kQStagesKv, ds = n % kDOStages;
-        const int ls = n % kLDStages;
+        const size_t ro = (static_cast<size_t>(b) * p.Hq + h) * p.Tp + q0;
         if (n > 0) {
           if (!wt(bar(kBarQEmpty + qs), ((n / kQStagesKv) & 1) ^ 1)) break;
-          if (!wt(bar(kBarLDEmpty + ls), ((n / kLDStages) & 1) ^ 1)) break;
-          mbar_arrive_expect_tx(bar(kBarQFull + qs), 2 * kHalfQ + 2 * 512);
+          mbar_arrive_expect_tx(bar(kBarQFull + qs), 2 * kHalfQ + 512);
           for (int hx = 0; hx < 2; ++hx)
             tma_load_4d(sb + kOffQ + qs * kBlockBytes + hx * kHalfQ, &tmQ, hx * 64, h, q0, b, bar(kBarQFull + qs));
-          const size_t ro = (static_cast<size_t>(b) * p.Hq + h) * p.Tp + q0;
-          bulk_load(sb + kOffLD + ls * 1024, p.ws.lse2 + ro, 512, bar(kBarQFull + qs));
-          bulk_load(sb + kOffLD + ls * 1024 + 512, p.ws.delta + ro, 512, bar(kBarQFull + qs));
+          bulk_load(sb + kOffLse + qs * 512, p.ws.lse2 + ro, 512, bar(kBarQFull + qs));
           q_issued = n + 1;
         }
         if (n > 0) {
           if (!wt(bar(kBarDOEmpty + ds), ((n / kDOStages) & 1) ^ 1)) break;
-          mbar_arrive_expect_tx(bar(kBarDOFull + ds), 2 * kHalfQ);
+          mbar_arrive_expect_tx(bar(kBarDOFull + ds), 2 * kHalfQ + 512);
           for (int hx = 0; hx < 2; ++hx)
             tma_load_4d(sb + kOffDO + ds * kBlockBytes + hx * kHalfQ, &tmDO, hx * 64, h, q0, b, bar(kBarDOFull + ds));
+          bulk_load(sb + kOffDelta + ds * 512, p.ws.delta + ro, 512, bar(kBarDOFull + ds));
           d_issued = n + 1;
         }
       }
@@ -577,11 +577,11 @@ __global__ void __launch_bounds__(kThr, 1)
       const int h = h_first + n / nq;
       const int qb = kb + n % nq;                       // 128-query block
       const int q0 = qb * kKvBQ + 64 * ch;              // this half's first query
-      // lse * log2 e and delta of this half's 64 queries; they arrived with
-      // Q(n), which S(n) waited for (with saved probabilities too)
-      const int ls = n % kLDStages;
-      const float *lse2 = reinterpret_cast<const float *>(smem + kOffLD + ls * 1024) + 64 * ch;
-      const float *dl = reinterpret_cast<const float *>(smem + kOffLD + ls * 1024 + 512) + 64 * ch;
+      // lse * log2 e and delta of this half's 64 queries: lse arrived with
+      // Q(n), which S(n) waited for (with saved probabilities too), delta
+      // with dO(n), which dP(n) waited for
+      const float *lse2 = reinterpret_cast<const float *>(smem + kOffLse + (n % kQStagesKv) * 512) + 64 * ch;
+      const float *dl = reinterpret_cast<const float *>(smem + kOffDelta + (n % kDOStages) * 512) + 64 * ch;
       // only the diagonal block needs the causal mask; queries past T have
       // lse = +inf, so their P is exactly 0
       const bool diag = qb == kb;
@@ -674,13 +674,11 @@ __global__ void __launch_bounds__(kThr, 1)
 #pragma unroll
         for (int u = 0; u < 4; ++u) U[4 * half + u] = make_uint4(dk[4 * u], dk[4 * u + 1], dk[4 * u + 2], dk[4 * u + 3]);
       }
-      // dS is in TMEM and this block's lse / delta have been read: the dK
-      // product (and after it dP(n + 1)) may start while the workspace copy
-      // below is still being written
+      // dS is in TMEM: the dK product (and after it dP(n + 1)) may start
+      // while the workspace copy below is still being written
       tc::wait_st();
       tc::fence_before_sync();
       mbar_arrive(bar(kBarDSFull));
-      mbar_arrive(bar(kBarLDEmpty + ls));
       // Once dV(n) has read dO(n) for the last time, its ring slot stages
       // the block's two dS^T tiles (32 KB in the tiles' own 128B-swizzled
       // layout: unit u of row r at 16 (u ^ (r % 8))); the copy warp moves
