@@ -97,6 +97,8 @@ def test_relu2_mul_bwd_golden(abw):
     (1024, 2560, 640, 8, torch.bfloat16),     # V adapter (5 KV heads x 128)
     (3, 16, 8, 5, torch.float32),             # rank not a multiple of 4
     (77, 256, 132, 16, torch.float32),        # largest rank, ragged row chunk
+    (130, 4100, 1028, 8, torch.bfloat16),     # column parts of unequal width, ragged row tiles
+    (33, 8, 4, 3, torch.float32),             # fewer 4-column groups than column parts
     (1, 4, 4, 1, torch.float32),
 ])
 def test_lora_bwd(abw, rows, n_in, n_out, r, xdt):
