@@ -106,7 +106,7 @@ enum {
   kBarKV = 0, kBarV = 1, kBarQFull = 2, kBarQEmpty = kBarQFull + kQStagesKv, kBarDOFull = kBarQEmpty + kQStagesKv,
   kBarDOEmpty = kBarDOFull + kDOStages, kBarSFull = kBarDOEmpty + kDOStages,
   kBarDPFull = kBarSFull + 1, kBarPFull = kBarDPFull + 1, kBarDSFull = kBarPFull + 1, kBarDVDone = kBarDSFull + 1,
-  kBarStaged = kBarDVDone + 1, kBarRope = kBarStaged + 1, kBarDVFinal = kBarRope + 1, kBarDKV = kBarDVFinal + 1,
+  kBarStaged = kBarDVDone + 1, kBarRope = kBarStaged + 2, kBarDVFinal = kBarRope + 1, kBarDKV = kBarDVFinal + 1,
   kBarFinal = kBarDKV + 1, kNumBars = kBarFinal + 1
 };
 constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
@@ -383,7 +383,8 @@ __global__ void __launch_bounds__(kThr, 1)
     mbar_init(bar(kBarPFull), 256);    // every softmax thread has put its P row into TMEM
     mbar_init(bar(kBarDSFull), 256);   // ... and its dS row
     mbar_init(bar(kBarDVDone), 1);     // dV(n) has read dO(n) for the last time
-    mbar_init(bar(kBarStaged), 256);   // every softmax thread has staged its dS row
+    for (int s = 0; s < 2; ++s)
+      mbar_init(bar(kBarStaged + s), 128);   // every thread of query half s has staged its dS row
     mbar_init(bar(kBarRope), 1);       // the key block's RoPE rows landed
     mbar_init(bar(kBarDVFinal), 1);    // the last dV product has completed
     mbar_init(bar(kBarDKV), 1);
@@ -543,12 +544,18 @@ __global__ void __launch_bounds__(kThr, 1)
     // softmax warps.
     if (lane == 0) {
       for (int n = 0; n < N; ++n) {
-        if (!wt(bar(kBarStaged), n & 1)) break;
         const int h = h_first + n / nq, qb = kb + n % nq;
         __nv_bfloat16 *dst =
             p.ws.ds + ((static_cast<size_t>(b) * p.Hq + h) * p.tph + tile_index(kb, 2 * qb, p.nqb)) * (kTileBytes / 2);
-        bulk_store(dst, sb + kOffDO + (n % kDOStages) * kBlockBytes, 2 * kTileBytes);
+        // each query half's tile goes out as soon as its four warps staged it
+        bool staged = true;
+        for (int hf = 0; hf < 2 && staged; ++hf) {
+          staged = wt(bar(kBarStaged + hf), n & 1);
+          if (staged) bulk_store(dst + hf * (kTileBytes / 2), sb + kOffDO + (n % kDOStages) * kBlockBytes + hf * kTileBytes,
+                                 kTileBytes);
+        }
         bulk_commit_group();
+        if (!staged) break;
         bulk_wait_group_read0();
         mbar_arrive(bar(kBarDOEmpty + n % kDOStages));
       }
@@ -690,7 +697,7 @@ __global__ void __launch_bounds__(kThr, 1)
 #pragma unroll
         for (int u = 0; u < 8; ++u) *reinterpret_cast<uint4 *>(smem + stg + ((u ^ (lane & 7)) << 4)) = U[u];
         fence_proxy_async_smem();
-        mbar_arrive(bar(kBarStaged));
+        mbar_arrive(bar(kBarStaged + ch));
       }
       blocks_done = n + 1;
     }
