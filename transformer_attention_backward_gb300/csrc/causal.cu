@@ -538,10 +538,10 @@ __global__ void __launch_bounds__(kThr, 1)
     }
   } else if (warp == 3) {
     // ============================ dS copy warp ============================
-    // Block n's two dS^T tiles are adjacent in the workspace; one 32 KB bulk
-    // copy takes them from the dO(n) slot.  Waiting for the copy to read the
-    // slot (it queues behind the ring's loads) happens here, not in the
-    // softmax warps.
+    // Block n's two dS^T tiles (one per query half, adjacent in the
+    // workspace) are copied from the dO(n) slot by two 16 KB bulk copies.
+    // Waiting for the copies to read the slot (they queue behind the ring's
+    // loads) happens here, not in the softmax warps.
     if (lane == 0) {
       for (int n = 0; n < N; ++n) {
         const int h = h_first + n / nq, qb = kb + n % nq;
