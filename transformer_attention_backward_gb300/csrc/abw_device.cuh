@@ -33,6 +33,29 @@ __device__ __forceinline__ unsigned long long globaltimer_ns() {
   return t;
 }
 
+// Time spent in a bounded wait.  The global timer can be re-synchronised
+// while a kernel runs, so it may step backwards or leap ahead between two
+// readings; the wait sums the steps between successive readings and drops
+// any step that is negative or longer than kWaitStepMaxNs (one polling round
+// takes microseconds).  As a second bound, independent of the timer, the
+// wait gives up after limit_ns / 128 polling rounds: a round of 32 barrier
+// probes takes well over 128 ns, so this cap is never reached before the
+// timed limit while the timer advances.
+constexpr unsigned long long kWaitStepMaxNs = 50000000ull;   // 50 ms
+struct WaitClock {
+  unsigned long long prev, waited, rounds, limit;
+  __device__ __forceinline__ explicit WaitClock(unsigned long long limit_ns)
+      : prev(globaltimer_ns()), waited(0), rounds(0), limit(limit_ns) {}
+  // one polling round has passed; true once the wait has lasted limit_ns
+  __device__ __forceinline__ bool expired() {
+    const unsigned long long now = globaltimer_ns();
+    const unsigned long long step = now - prev;   // huge when the timer stepped back
+    if (step < kWaitStepMaxNs) waited += step;
+    prev = now;
+    return waited > limit || ++rounds > (limit >> 7);
+  }
+};
+
 // ---------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
@@ -85,12 +108,12 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t par
 __device__ __forceinline__ bool mbar_wait_cluster_bounded(uint32_t bar, uint32_t parity,
                                                           unsigned long long limit_ns) {
   if (mbar_try_wait_cluster(bar, parity)) return true;
-  const unsigned long long t0 = globaltimer_ns();
+  WaitClock wc(limit_ns);
   while (true) {
 #pragma unroll 1
     for (int i = 0; i < 32; ++i)
       if (mbar_try_wait_cluster(bar, parity)) return true;
-    if (globaltimer_ns() - t0 > limit_ns) return false;
+    if (wc.expired()) return false;
   }
 }
 
@@ -107,12 +130,12 @@ __device__ __forceinline__ void mbar_arrive_remote(uint32_t bar, uint32_t rank) 
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
                                                   unsigned long long limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
-  const unsigned long long t0 = globaltimer_ns();
+  WaitClock wc(limit_ns);
   while (true) {
 #pragma unroll 1
     for (int i = 0; i < 32; ++i)
       if (mbar_try_wait(bar, parity)) return true;
-    if (globaltimer_ns() - t0 > limit_ns) return false;
+    if (wc.expired()) return false;
   }
 }
 
