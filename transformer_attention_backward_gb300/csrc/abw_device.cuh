@@ -19,9 +19,22 @@ enum : unsigned int {
 
 // Everything a kernel needs to report a failed wait.
 struct WaitCtl {
-  unsigned int *err;              // device error word (library-owned symbol)
+  unsigned int *err;              // device error words (library-owned): [0] bits, [1] first timeout site
   unsigned long long limit_ns;    // time limit of one wait
 };
+
+// Where a wait ran out, for the report: kernel (bits 28-31), barrier slot
+// (bits 20-27), warp (bits 16-19) and the low 16 bits of the block index.
+enum : unsigned int { kSiteKv = 1u, kSiteDq = 2u, kSiteFwd = 3u, kSiteDecode = 4u };
+__device__ __forceinline__ unsigned int wait_site(unsigned int kernel, unsigned int slot) {
+  return (kernel << 28) | ((slot & 0xffu) << 20) | (((threadIdx.x >> 5) & 0xfu) << 16) | (blockIdx.x & 0xffffu);
+}
+// Records a timeout: the error bit, and the site if it is the first one.
+// Kept out of line: it runs only on the failure path.
+static __device__ __noinline__ void report_timeout(unsigned int *err, unsigned int kernel, unsigned int slot) {
+  atomicOr(err, kErrWaitTimeout);
+  atomicCAS(err + 1, 0u, wait_site(kernel, slot));
+}
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -144,7 +157,7 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
 // on or exits.  Returns true iff the first wait succeeded.
 __device__ __forceinline__ bool mbar_wait_or_flag(uint32_t bar, uint32_t parity, const WaitCtl &w) {
   if (mbar_wait_bounded(bar, parity, w.limit_ns)) return true;
-  atomicOr(w.err, kErrWaitTimeout);
+  report_timeout(w.err, kSiteDecode, bar >> 3);
   const unsigned long long drain = w.limit_ns < 2000000000ull ? 2000000000ull : w.limit_ns;
   mbar_wait_bounded(bar, parity, drain);
   return false;

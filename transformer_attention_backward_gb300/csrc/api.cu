@@ -18,7 +18,7 @@ std::atomic<unsigned long long> g_wait_limit_ns{2000000000ull};
 
 // The device error word.  Kernels receive its device address (resolved per
 // device with cudaGetSymbolAddress) and atomically OR failure bits into it.
-__device__ unsigned int g_abw_err_word;
+__device__ unsigned int g_abw_err_word[2];   // bits, first timeout site
 
 constexpr int kMaxDevices = 64;
 std::mutex g_dev_mu;
@@ -205,13 +205,20 @@ abw_status abw_device_check(abw_stream stream) {
   if (e != cudaSuccess) return from_cuda(e, "abw_device_check");
   abw::WaitCtl w = abw::wait_ctl();
   if (!w.err) return fail(ABW_ECUDA, "abw_device_check: device error word unavailable");
-  unsigned int word = 0;
-  e = cudaMemcpyAsync(&word, w.err, sizeof(word), cudaMemcpyDeviceToHost, st);
-  if (e == cudaSuccess) e = cudaMemsetAsync(w.err, 0, sizeof(word), st);
+  unsigned int words[2] = {0, 0};
+  e = cudaMemcpyAsync(words, w.err, sizeof(words), cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaMemsetAsync(w.err, 0, sizeof(words), st);
   if (e == cudaSuccess) e = cudaStreamSynchronize(st);
   if (e != cudaSuccess) return from_cuda(e, "abw_device_check");
-  if (word & (abw::kErrWaitTimeout | abw::kErrSelfTest))
-    return fail(ABW_ETIMEOUT, "a device-side bounded wait ran out (error word 0x%x)", word);
+  const unsigned int word = words[0], site = words[1];
+  if (word & (abw::kErrWaitTimeout | abw::kErrSelfTest)) {
+    static const char *const kernels[] = {"?", "causal kv", "causal dq", "causal forward", "decode"};
+    const unsigned int k = site >> 28;
+    return fail(ABW_ETIMEOUT,
+                "a device-side bounded wait ran out (error word 0x%x; first in the %s kernel, barrier slot %u, "
+                "warp %u, block %u)",
+                word, kernels[k < 5 ? k : 0], (site >> 20) & 0xffu, (site >> 16) & 0xfu, site & 0xffffu);
+  }
   if (word & abw::kErrSmemAlign)
     return fail(ABW_ECUDA, "a kernel's dynamic shared memory was not 1024-byte aligned; it did no work");
   return ABW_OK;

@@ -111,8 +111,13 @@ enum {
 };
 constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
 constexpr int kOffAbort = kOffTmemSlot + 4;
+// dO slot 1's two staged barriers (slot 0's are kBarStaged, kBarStaged + 1),
+// placed after the other words so that those keep their offsets (moving the
+// barrier block by 16 bytes measured 2 % slower)
+constexpr int kOffStaged1 = kOffAbort + 4;
+static_assert(kDOStages == 2, "one pair of staged barriers per dO slot");
 constexpr int kSmem = kOffBar + 256;
-static_assert(kOffAbort + 4 <= kSmem && kSmem <= 232448, "kv kernel shared memory");
+static_assert(kOffStaged1 % 8 == 0 && kOffStaged1 + 16 <= kSmem && kSmem <= 232448, "kv kernel shared memory");
 
 // kv kernel TMEM columns: S^T / P^T, dP^T / dS^T (one query block each), dV, dK.
 constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 384;
@@ -355,12 +360,21 @@ __global__ void __launch_bounds__(kThr, 1)
   const int N = p.gs * nq;               // iterations of this CTA
 
   auto bar = [&](int i) -> uint32_t { return sb + kOffBar + i * 8; };
+  // Block n's dS is staged in dO slot n % 2, and each slot has its own pair
+  // of staged barriers (query halves): the softmax warps can stage block
+  // n + 2 only after the copy warp has released the slot from block n, so a
+  // barrier is never two phases ahead of the copy warp's parity wait.  (One
+  // pair for all blocks could be, when the copy warp falls a block behind,
+  // and its wait would then be for a phase that needs the copy warp itself.)
+  auto staged_bar = [&](int slot, int half) -> uint32_t {
+    return slot == 0 ? bar(kBarStaged + half) : sb + kOffStaged1 + 8 * half;
+  };
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + kOffAbort);
   auto wt = [&](uint32_t br, uint32_t parity) -> bool {
     if (*abort_flag) return false;
     if (mbar_wait_bounded(br, parity, p.wait.limit_ns)) return true;
     *abort_flag = 1;
-    atomicOr(p.wait.err, kErrWaitTimeout);
+    report_timeout(p.wait.err, kSiteKv, (br - sb - kOffBar) / 8);
     return false;
   };
   // Whole-warp form: lane 0's outcome for every lane, so that a warp never
@@ -384,7 +398,8 @@ __global__ void __launch_bounds__(kThr, 1)
     mbar_init(bar(kBarDSFull), 256);   // ... and its dS row
     mbar_init(bar(kBarDVDone), 1);     // dV(n) has read dO(n) for the last time
     for (int s = 0; s < 2; ++s)
-      mbar_init(bar(kBarStaged + s), 128);   // every thread of query half s has staged its dS row
+      mbar_init(bar(kBarStaged + s), 128);   // slot 0: every thread of query half s has staged its dS row
+    for (int s = 0; s < 2; ++s) mbar_init(sb + kOffStaged1 + 8 * s, 128);   // ... slot 1
     mbar_init(bar(kBarRope), 1);       // the key block's RoPE rows landed
     mbar_init(bar(kBarDVFinal), 1);    // the last dV product has completed
     mbar_init(bar(kBarDKV), 1);
@@ -550,7 +565,7 @@ __global__ void __launch_bounds__(kThr, 1)
         // each query half's tile goes out as soon as its four warps staged it
         bool staged = true;
         for (int hf = 0; hf < 2 && staged; ++hf) {
-          staged = wt(bar(kBarStaged + hf), n & 1);
+          staged = wt(staged_bar(n % kDOStages, hf), (n / kDOStages) & 1);
           if (staged) bulk_store(dst + hf * (kTileBytes / 2), sb + kOffDO + (n % kDOStages) * kBlockBytes + hf * kTileBytes,
                                  kTileBytes);
         }
@@ -697,7 +712,7 @@ __global__ void __launch_bounds__(kThr, 1)
 #pragma unroll
         for (int u = 0; u < 8; ++u) *reinterpret_cast<uint4 *>(smem + stg + ((u ^ (lane & 7)) << 4)) = U[u];
         fence_proxy_async_smem();
-        mbar_arrive(bar(kBarStaged + ch));
+        mbar_arrive(staged_bar(n % kDOStages, ch));
       }
       blocks_done = n + 1;
     }
@@ -839,7 +854,7 @@ __global__ void __launch_bounds__(kThr, 1)
     if (*abort_flag) return false;
     if (mbar_wait_bounded(br, parity, p.wait.limit_ns)) return true;
     *abort_flag = 1;
-    atomicOr(p.wait.err, kErrWaitTimeout);
+    report_timeout(p.wait.err, kSiteDq, (br - sb - kQOffBar) / 8);
     return false;
   };
   // Whole-warp form: lane 0's outcome for every lane, so that a warp never

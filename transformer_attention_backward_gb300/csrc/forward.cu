@@ -109,7 +109,7 @@ __global__ void __launch_bounds__(kFThr, 1)
     if (*abort_flag) return false;
     if (mbar_wait_bounded(br, parity, p.wait.limit_ns)) return true;
     *abort_flag = 1;
-    atomicOr(p.wait.err, kErrWaitTimeout);
+    report_timeout(p.wait.err, kSiteFwd, (br - sb - kFOffBar) / 8);
     return false;
   };
   auto wtw = [&](uint32_t br, uint32_t parity) -> bool { return __shfl_sync(0xffffffffu, wt(br, parity), 0); };
