@@ -290,12 +290,19 @@ __global__ void __launch_bounds__(256) causal_prep_kernel(const __nv_bfloat16 *_
   }
 }
 
+constexpr int kMaxVarKb = 32;   // key blocks up to which the kv split may vary per key block
 struct TcParams {
   CausalWs ws;
   float *dq, *dk, *dv;
   const __nv_bfloat16 *pattn;   // saved probabilities [B][Hq][T][T] (row = query), or null: recompute from lse
   int B, T, Tp, Hq, Hkv, G, nkb, nqb;
   int hsplit, gs;  // kv kernel: each KV head's G query heads go to hsplit CTAs, gs = G / hsplit each
+  // kv kernel, small grids: the split chosen per key block instead (nsplit[kb]
+  // CTAs per (batch, KV head), kb_first[kb] the index of the key block's
+  // first CTA), so that a CTA's blocks (heads x query blocks) stay within
+  // one key block row's worth; var_split = 0 uses hsplit for every key block.
+  int var_split;
+  int nsplit[kMaxVarKb], kb_first[kMaxVarKb + 1];
   long long tph;   // dS^T tiles per head
   float scale;
   int rope;
@@ -346,18 +353,35 @@ __global__ void __launch_bounds__(kThr, 1)
   // key blocks come first.  The CTAs that run at one time then cover few
   // heads, whose Q and dO (every key block of a head re-reads them) stay in
   // L2 between the key blocks.
-  const int nh = p.Hkv * p.B * p.hsplit;
-  const int grp = blockIdx.x / (kHeadGroup * p.nkb);
-  const int gsz = min(kHeadGroup, nh - grp * kHeadGroup);
-  const int in_grp = blockIdx.x - grp * kHeadGroup * p.nkb;
-  const int kb = in_grp / gsz;
-  const int hb = grp * kHeadGroup + in_grp % gsz;   // (b * Hkv + kvh) * hsplit + split
-  const int split = hb % p.hsplit;
-  const int kvh = (hb / p.hsplit) % p.Hkv, b = hb / (p.hsplit * p.Hkv);
-  const int h_first = kvh * p.G + split * p.gs;     // query heads h_first .. h_first + gs - 1
+  int kb, b, kvh, h_first, gs;   // query heads h_first .. h_first + gs - 1
+  if (p.var_split) {
+    // key blocks in order (the heaviest first); within one, nsplit[kb] CTAs
+    // per (batch, KV head)
+    kb = 0;
+    while (kb + 1 < p.nkb && static_cast<int>(blockIdx.x) >= p.kb_first[kb + 1]) ++kb;
+    const int u = blockIdx.x - p.kb_first[kb], ns = p.nsplit[kb];
+    const int unit = u / ns;   // b * Hkv + kvh
+    kvh = unit % p.Hkv;
+    b = unit / p.Hkv;
+    gs = p.G / ns;
+    h_first = kvh * p.G + (u % ns) * gs;
+  } else {
+    const int nh = p.Hkv * p.B * p.hsplit;
+    const int grp = blockIdx.x / (kHeadGroup * p.nkb);
+    const int gsz = min(kHeadGroup, nh - grp * kHeadGroup);
+    const int in_grp = blockIdx.x - grp * kHeadGroup * p.nkb;
+    kb = in_grp / gsz;
+    const int hb = grp * kHeadGroup + in_grp % gsz;   // (b * Hkv + kvh) * hsplit + split
+    kvh = (hb / p.hsplit) % p.Hkv;
+    b = hb / (p.hsplit * p.Hkv);
+    gs = p.gs;
+    h_first = kvh * p.G + (hb % p.hsplit) * gs;
+  }
+  // with the group split over CTAs, dK / dV receive partial sums
+  const bool split_group = gs < p.G;
   const int k0 = kb * kBK;
   const int nq = p.nkb - kb;             // 128-query blocks at or after the key block, per head
-  const int N = p.gs * nq;               // iterations of this CTA
+  const int N = gs * nq;                 // iterations of this CTA
 
   auto bar = [&](int i) -> uint32_t { return sb + kOffBar + i * 8; };
   // Block n's dS is staged in dO slot n % 2, and each slot has its own pair
@@ -758,7 +782,7 @@ __global__ void __launch_bounds__(kThr, 1)
     eok = named_barrier_and(4, 256, eok);
     if (eok && warp == 4 && lane == 0) {
       for (int c = 0; c < 4; ++c) {
-        if (p.hsplit > 1)
+        if (split_group)
           tma_reduce_add_4d(&tmdV, sb + kOffK + c * 16384, 32 * c, kvh, k0, b);
         else
           tma_store_4d(&tmdV, sb + kOffK + c * 16384, 32 * c, kvh, k0, b);
@@ -796,7 +820,7 @@ __global__ void __launch_bounds__(kThr, 1)
     if (warp == 4 && lane == 0) {
       if (kok) {
         for (int c = 0; c < 4; ++c) {
-          if (p.hsplit > 1)
+          if (split_group)
             tma_reduce_add_4d(&tmdK, sb + kOffDO + c * 16384, 32 * c, kvh, k0, b);
           else
             tma_store_4d(&tmdK, sb + kOffDO + c * 16384, 32 * c, kvh, k0, b);
@@ -1108,7 +1132,27 @@ cudaError_t launch_attn_bwd_causal(const void *q, const void *k, const void *v, 
   const int G = Hq / Hkv;
   int hsplit = 1;
   while (hsplit < G && G % (2 * hsplit) == 0 && static_cast<long long>(nkb) * Hkv * B * hsplit < sms) hsplit *= 2;
-  const long long kv_ctas = static_cast<long long>(nkb) * Hkv * B * hsplit;
+  long long kv_ctas = static_cast<long long>(nkb) * Hkv * B * hsplit;
+  // When the group is split (the grid would not fill the GPU otherwise),
+  // choose the split per key block: key block kb gives each head nkb - kb
+  // query blocks, so it takes the largest share of the group (a divisor of
+  // G) whose blocks stay within nkb, the count of the heaviest key block
+  // with one head per CTA.  Every CTA then holds at most nkb blocks and the
+  // light key blocks use fewer CTAs: fewer CTAs and no second partial wave.
+  int nsplit[kMaxVarKb] = {}, kb_first[kMaxVarKb + 1] = {};
+  const bool var_split = hsplit > 1 && nkb <= kMaxVarKb;
+  if (var_split) {
+    kv_ctas = 0;
+    for (int kb = 0; kb < nkb; ++kb) {
+      int share = 1;   // heads per CTA
+      for (int d = 1; d <= G; ++d)
+        if (G % d == 0 && d * (nkb - kb) <= nkb) share = d;
+      nsplit[kb] = G / share;
+      kb_first[kb] = static_cast<int>(kv_ctas);
+      kv_ctas += static_cast<long long>(B) * Hkv * nsplit[kb];
+    }
+    kb_first[nkb] = static_cast<int>(kv_ctas);
+  }
   const long long dq_ctas = static_cast<long long>(nkb) * Hq * B;
   if (kv_ctas > 0x7fffffffLL || dq_ctas > 0x7fffffffLL) {
     *why = "grid too large";
@@ -1152,6 +1196,9 @@ cudaError_t launch_attn_bwd_causal(const void *q, const void *k, const void *v, 
   p.tph = tiles_per_head(nkb);
   p.hsplit = hsplit;
   p.gs = G / hsplit;
+  p.var_split = var_split;
+  for (int kb = 0; kb < kMaxVarKb; ++kb) p.nsplit[kb] = nsplit[kb];
+  for (int kb = 0; kb <= kMaxVarKb; ++kb) p.kb_first[kb] = kb_first[kb];
   p.scale = scale;
   p.rope = rope;
   p.wait = w;
