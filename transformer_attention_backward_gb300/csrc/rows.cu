@@ -185,26 +185,33 @@ __device__ __forceinline__ void store_dx4(void *dx, size_t idx4, float4 v) {
   }
 }
 
+// Rows of up to 2 x 1024 elements keep 8 blocks (2048 threads) resident per
+// SM and rows of up to 3 x 1024 keep 7, so a call of up to about 1,000 rows
+// runs in one wave (the row keeps x and dy * gamma in registers, not dy and
+// gamma apart; at 7 blocks a few values of the longer rows go to the stack).
+template <int NV>
+constexpr int rms_min_blocks() { return NV <= 2 ? 8 : NV == 3 ? 7 : 1; }
+
 template <bool XBF16, bool DXBF16, int NV>
-__global__ void __launch_bounds__(kRowThreads) rmsnorm_bwd_v4(const void *__restrict__ x,
+__global__ void __launch_bounds__(kRowThreads, rms_min_blocks<NV>()) rmsnorm_bwd_v4(const void *__restrict__ x,
                                                               const float *__restrict__ gamma,
                                                               const float *__restrict__ dy,
                                                               void *__restrict__ dx, int n, float eps) {
   __shared__ float2 red[kRowThreads / 32 + 1];
   const int n4 = n >> 2;
   const size_t rb = static_cast<size_t>(blockIdx.x) * n4;
-  float4 xv[NV], gv[NV], dv[NV];
+  float4 xv[NV], gv[NV];   // x and dy * gamma
   float ss = 0.f, cs = 0.f;
 #pragma unroll
   for (int k = 0; k < NV; ++k) {
     const int i = threadIdx.x + kRowThreads * k;
     if (i < n4) {
       xv[k] = load_x4<XBF16>(x, rb + i);
-      dv[k] = __ldg(reinterpret_cast<const float4 *>(dy) + rb + i);
-      gv[k] = __ldg(reinterpret_cast<const float4 *>(gamma) + i);
+      const float4 d = __ldg(reinterpret_cast<const float4 *>(dy) + rb + i);
+      const float4 g = __ldg(reinterpret_cast<const float4 *>(gamma) + i);
+      gv[k] = make_float4(d.x * g.x, d.y * g.y, d.z * g.z, d.w * g.w);
       ss += xv[k].x * xv[k].x + xv[k].y * xv[k].y + xv[k].z * xv[k].z + xv[k].w * xv[k].w;
-      cs += dv[k].x * gv[k].x * xv[k].x + dv[k].y * gv[k].y * xv[k].y + dv[k].z * gv[k].z * xv[k].z +
-            dv[k].w * gv[k].w * xv[k].w;
+      cs += gv[k].x * xv[k].x + gv[k].y * xv[k].y + gv[k].z * xv[k].z + gv[k].w * xv[k].w;
     }
   }
   const float2 sums = block_sum2(ss, cs, red);
@@ -216,10 +223,10 @@ __global__ void __launch_bounds__(kRowThreads) rmsnorm_bwd_v4(const void *__rest
     const int i = threadIdx.x + kRowThreads * k;
     if (i < n4) {
       float4 r;
-      r.x = (dv[k].x * gv[k].x - xv[k].x * coef) * inv_rms;
-      r.y = (dv[k].y * gv[k].y - xv[k].y * coef) * inv_rms;
-      r.z = (dv[k].z * gv[k].z - xv[k].z * coef) * inv_rms;
-      r.w = (dv[k].w * gv[k].w - xv[k].w * coef) * inv_rms;
+      r.x = (gv[k].x - xv[k].x * coef) * inv_rms;
+      r.y = (gv[k].y - xv[k].y * coef) * inv_rms;
+      r.z = (gv[k].z - xv[k].z * coef) * inv_rms;
+      r.w = (gv[k].w - xv[k].w * coef) * inv_rms;
       store_dx4<DXBF16>(dx, rb + i, r);
     }
   }
