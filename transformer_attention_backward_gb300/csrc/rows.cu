@@ -185,15 +185,17 @@ __device__ __forceinline__ void store_dx4(void *dx, size_t idx4, float4 v) {
   }
 }
 
-// Rows of up to 2 x 1024 elements keep 8 blocks (2048 threads) resident per
-// SM and rows of up to 3 x 1024 keep 7, so a call of up to about 1,000 rows
-// runs in one wave (the row keeps x and dy * gamma in registers, not dy and
-// gamma apart; at 7 blocks a few values of the longer rows go to the stack).
-template <int NV>
-constexpr int rms_min_blocks() { return NV <= 2 ? 8 : NV == 3 ? 7 : 1; }
+// For calls of many rows (kCap), rows of up to 2 x 1024 elements keep 8
+// blocks (2048 threads) resident per SM and rows of up to 3 x 1024 keep 7, so
+// about 1,000 rows run in one wave and long calls keep more rows in flight
+// (the row keeps x and dy * gamma in registers, not dy and gamma apart; at 7
+// blocks a few values of the longer rows go to the stack, which calls of few
+// rows, one wave anyway, do without).
+template <int NV, bool kCap>
+constexpr int rms_min_blocks() { return !kCap ? 1 : NV <= 2 ? 8 : NV == 3 ? 7 : 1; }
 
-template <bool XBF16, bool DXBF16, int NV>
-__global__ void __launch_bounds__(kRowThreads, rms_min_blocks<NV>()) rmsnorm_bwd_v4(const void *__restrict__ x,
+template <bool XBF16, bool DXBF16, int NV, bool kCap>
+__global__ void __launch_bounds__(kRowThreads, rms_min_blocks<NV, kCap>()) rmsnorm_bwd_v4(const void *__restrict__ x,
                                                               const float *__restrict__ gamma,
                                                               const float *__restrict__ dy,
                                                               void *__restrict__ dx, int n, float eps) {
@@ -263,6 +265,21 @@ __global__ void __launch_bounds__(kRowThreads) rmsnorm_bwd_any(const void *__res
   }
 }
 
+template <bool XB, bool DB, bool kCap>
+void rms_launch(int nv, const void *x, const float *g, const float *dy, void *dx, int rows, int n, float eps,
+                cudaStream_t st) {
+  if (nv <= 1)
+    rmsnorm_bwd_v4<XB, DB, 1, kCap><<<rows, kRowThreads, 0, st>>>(x, g, dy, dx, n, eps);
+  else if (nv <= 2)
+    rmsnorm_bwd_v4<XB, DB, 2, kCap><<<rows, kRowThreads, 0, st>>>(x, g, dy, dx, n, eps);
+  else if (nv <= 3)
+    rmsnorm_bwd_v4<XB, DB, 3, kCap><<<rows, kRowThreads, 0, st>>>(x, g, dy, dx, n, eps);
+  else if (nv <= 4)
+    rmsnorm_bwd_v4<XB, DB, 4, kCap><<<rows, kRowThreads, 0, st>>>(x, g, dy, dx, n, eps);
+  else
+    rmsnorm_bwd_v4<XB, DB, 8, kCap><<<rows, kRowThreads, 0, st>>>(x, g, dy, dx, n, eps);
+}
+
 template <bool XB, bool DB>
 cudaError_t rms_dispatch(const void *x, const float *g, const float *dy, void *dx, int rows, int n, float eps,
                          cudaStream_t st) {
@@ -270,17 +287,17 @@ cudaError_t rms_dispatch(const void *x, const float *g, const float *dy, void *d
   const int nv = (n4 + kRowThreads - 1) / kRowThreads;
   if (n % 4 != 0 || nv > 8) {
     rmsnorm_bwd_any<XB, DB><<<rows, kRowThreads, 0, st>>>(x, g, dy, dx, n, eps);
-  } else if (nv <= 1) {
-    rmsnorm_bwd_v4<XB, DB, 1><<<rows, kRowThreads, 0, st>>>(x, g, dy, dx, n, eps);
-  } else if (nv <= 2) {
-    rmsnorm_bwd_v4<XB, DB, 2><<<rows, kRowThreads, 0, st>>>(x, g, dy, dx, n, eps);
-  } else if (nv <= 3) {
-    rmsnorm_bwd_v4<XB, DB, 3><<<rows, kRowThreads, 0, st>>>(x, g, dy, dx, n, eps);
-  } else if (nv <= 4) {
-    rmsnorm_bwd_v4<XB, DB, 4><<<rows, kRowThreads, 0, st>>>(x, g, dy, dx, n, eps);
-  } else {
-    rmsnorm_bwd_v4<XB, DB, 8><<<rows, kRowThreads, 0, st>>>(x, g, dy, dx, n, eps);
+    return cudaGetLastError();
   }
+  // more rows than 4 blocks per SM hold: the register-capped form
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  if (rows > 4 * sms)
+    rms_launch<XB, DB, true>(nv, x, g, dy, dx, rows, n, eps, st);
+  else
+    rms_launch<XB, DB, false>(nv, x, g, dy, dx, rows, n, eps, st);
   return cudaGetLastError();
 }
 
@@ -291,8 +308,13 @@ cudaError_t rms_dispatch(const void *x, const float *g, const float *dy, void *d
 // block's rows and adds them into the zeroed output once, with 16-byte
 // vector reductions.
 // ---------------------------------------------------------------------------
+// The launch puts up to 4 blocks per SM; rows of up to 3 x 1024 elements are
+// held to the registers that lets all of them be resident at once.
+template <int NV>
+constexpr int rms_dg_min_blocks() { return NV <= 3 ? 4 : 1; }
+
 template <bool XBF16, bool DXBF16, int NV, bool DX>
-__global__ void __launch_bounds__(kRowThreads) rmsnorm_bwd_dgamma_v4(const void *__restrict__ x,
+__global__ void __launch_bounds__(kRowThreads, rms_dg_min_blocks<NV>()) rmsnorm_bwd_dgamma_v4(const void *__restrict__ x,
                                                                      const float *__restrict__ gamma,
                                                                      const float *__restrict__ dy,
                                                                      void *__restrict__ dx, float *__restrict__ dgamma,
