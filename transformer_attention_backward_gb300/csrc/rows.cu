@@ -106,6 +106,7 @@ struct RopeParams {
   double inv_freq[256];   // base^(-2i/D), formed on the host in double
 };
 
+constexpr int kRopeBatch = 8;
 __global__ void __launch_bounds__(128) rope_bwd_kernel(const __grid_constant__ RopeParams p) {
   __shared__ float2 cs[256];
   const int row = blockIdx.x;           // b * T + t
@@ -133,27 +134,55 @@ __global__ void __launch_bounds__(128) rope_bwd_kernel(const __grid_constant__ R
     float4 *dst = reinterpret_cast<float4 *>(p.dx + base);
     const int n4 = npairs >> 1;
     const int q4 = p.D >> 2;
-    for (int i = threadIdx.x; i < n4; i += blockDim.x) {
-      const int pi = (i % q4) * 2;   // pair index within the head
-      const float4 y = src[i];
-      const float2 a = cs[pi], b = cs[pi + 1];
-      float4 r;
-      r.x = y.x * a.x + y.y * a.y;
-      r.y = -y.x * a.y + y.y * a.x;
-      r.z = y.z * b.x + y.w * b.y;
-      r.w = -y.z * b.y + y.w * b.x;
-      dst[i] = r;
+    // kRopeBatch vectors per thread are loaded before the first is written,
+    // so a thread waits for one memory latency per batch, not per vector
+    // (each element is read before it is written, so dx may be dy)
+    for (int i0 = threadIdx.x; i0 < n4; i0 += kRopeBatch * blockDim.x) {
+      float4 y[kRopeBatch];
+#pragma unroll
+      for (int u = 0; u < kRopeBatch; ++u) {
+        const int i = i0 + u * blockDim.x;
+        if (i < n4) y[u] = src[i];
+      }
+#pragma unroll
+      for (int u = 0; u < kRopeBatch; ++u) {
+        const int i = i0 + u * blockDim.x;
+        if (i < n4) {
+          const int pi = (i % q4) * 2;   // pair index within the head
+          const float2 a = cs[pi], b = cs[pi + 1];
+          float4 r;
+          r.x = y[u].x * a.x + y[u].y * a.y;
+          r.y = -y[u].x * a.y + y[u].y * a.x;
+          r.z = y[u].z * b.x + y[u].w * b.y;
+          r.w = -y[u].z * b.y + y[u].w * b.x;
+          dst[i] = r;
+        }
+      }
     }
   } else {
-    for (int i = threadIdx.x; i < npairs; i += blockDim.x) {
-      const int h = i / half, pi = i % half;
-      const size_t o = base + static_cast<size_t>(h) * p.D;
-      const int i0 = p.interleaved ? 2 * pi : pi;
-      const int i1 = p.interleaved ? 2 * pi + 1 : pi + half;
-      const float y0 = p.dy[o + i0], y1 = p.dy[o + i1];
-      const float2 a = cs[pi];
-      p.dx[o + i0] = y0 * a.x + y1 * a.y;
-      p.dx[o + i1] = -y0 * a.y + y1 * a.x;
+    for (int i0 = threadIdx.x; i0 < npairs; i0 += kRopeBatch * blockDim.x) {
+      float y0[kRopeBatch], y1[kRopeBatch];
+#pragma unroll
+      for (int u = 0; u < kRopeBatch; ++u) {
+        const int i = i0 + u * blockDim.x;
+        if (i < npairs) {
+          const int h = i / half, pi = i % half;
+          const size_t o = base + static_cast<size_t>(h) * p.D;
+          y0[u] = p.dy[o + (p.interleaved ? 2 * pi : pi)];
+          y1[u] = p.dy[o + (p.interleaved ? 2 * pi + 1 : pi + half)];
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kRopeBatch; ++u) {
+        const int i = i0 + u * blockDim.x;
+        if (i < npairs) {
+          const int h = i / half, pi = i % half;
+          const size_t o = base + static_cast<size_t>(h) * p.D;
+          const float2 a = cs[pi];
+          p.dx[o + (p.interleaved ? 2 * pi : pi)] = y0[u] * a.x + y1[u] * a.y;
+          p.dx[o + (p.interleaved ? 2 * pi + 1 : pi + half)] = -y0[u] * a.y + y1[u] * a.x;
+        }
+      }
     }
   }
 }
