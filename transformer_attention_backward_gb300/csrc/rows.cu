@@ -117,9 +117,12 @@ __global__ void __launch_bounds__(128) rope_bwd_kernel(const __grid_constant__ R
     if (p.theta) {
       th = p.theta[static_cast<size_t>(row) * half + i];
     } else {
+      // reduced to [-pi, pi] in double (a multiply by 1 / 2 pi, not a divide:
+      // double division is slow on this GPU, and a last-bit difference in
+      // the quotient only picks another multiple of 2 pi)
       const double a = static_cast<double>(p.pos0 + t) * p.inv_freq[i];
-      const double twopi = 6.283185307179586476925286766559;
-      th = static_cast<float>(a - twopi * rint(a / twopi));
+      const double twopi = 6.283185307179586476925286766559, inv_twopi = 0.15915494309189533576888376337251;
+      th = static_cast<float>(fma(-twopi, rint(a * inv_twopi), a));
     }
     float sn, c;
     sincosf(th, &sn, &c);
