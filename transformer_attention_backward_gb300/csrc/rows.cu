@@ -112,6 +112,25 @@ __global__ void __launch_bounds__(128) rope_bwd_kernel(const __grid_constant__ R
   const int row = blockIdx.x;           // b * T + t
   const int t = row % p.T;
   const int half = p.D >> 1;
+  const size_t base = static_cast<size_t>(row) * p.H * p.D;
+  const int npairs = p.H * half;
+  const bool vec = p.interleaved && (p.D & 3) == 0;   // two pairs per float4
+  const float4 *src = reinterpret_cast<const float4 *>(p.dy + base);
+  float4 *dst = reinterpret_cast<float4 *>(p.dx + base);
+  const int n4 = npairs >> 1;
+  // The first batch of row values is requested before the angles are
+  // formed, so the angle arithmetic runs while the loads are in flight.
+  // kRopeBatch vectors per thread are loaded before the first is written,
+  // so a thread waits for one memory latency per batch, not per vector
+  // (each element is read before it is written, so dx may be dy).
+  float4 y[kRopeBatch];
+  if (vec) {
+#pragma unroll
+    for (int u = 0; u < kRopeBatch; ++u) {
+      const int i = threadIdx.x + u * blockDim.x;
+      if (i < n4) y[u] = src[i];
+    }
+  }
   for (int i = threadIdx.x; i < half; i += blockDim.x) {
     float th;
     if (p.theta) {
@@ -129,24 +148,9 @@ __global__ void __launch_bounds__(128) rope_bwd_kernel(const __grid_constant__ R
     cs[i] = make_float2(c, sn);
   }
   __syncthreads();
-  const size_t base = static_cast<size_t>(row) * p.H * p.D;
-  const int npairs = p.H * half;
-  if (p.interleaved && (p.D & 3) == 0) {
-    // two pairs per float4
-    const float4 *src = reinterpret_cast<const float4 *>(p.dy + base);
-    float4 *dst = reinterpret_cast<float4 *>(p.dx + base);
-    const int n4 = npairs >> 1;
+  if (vec) {
     const int q4 = p.D >> 2;
-    // kRopeBatch vectors per thread are loaded before the first is written,
-    // so a thread waits for one memory latency per batch, not per vector
-    // (each element is read before it is written, so dx may be dy)
-    for (int i0 = threadIdx.x; i0 < n4; i0 += kRopeBatch * blockDim.x) {
-      float4 y[kRopeBatch];
-#pragma unroll
-      for (int u = 0; u < kRopeBatch; ++u) {
-        const int i = i0 + u * blockDim.x;
-        if (i < n4) y[u] = src[i];
-      }
+    for (int i0 = threadIdx.x;;) {
 #pragma unroll
       for (int u = 0; u < kRopeBatch; ++u) {
         const int i = i0 + u * blockDim.x;
@@ -160,6 +164,13 @@ __global__ void __launch_bounds__(128) rope_bwd_kernel(const __grid_constant__ R
           r.w = -y[u].z * b.y + y[u].w * b.x;
           dst[i] = r;
         }
+      }
+      i0 += kRopeBatch * blockDim.x;
+      if (i0 >= n4) break;
+#pragma unroll
+      for (int u = 0; u < kRopeBatch; ++u) {
+        const int i = i0 + u * blockDim.x;
+        if (i < n4) y[u] = src[i];
       }
     }
   } else {
