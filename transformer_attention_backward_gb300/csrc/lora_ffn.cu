@@ -77,8 +77,6 @@ __global__ void __launch_bounds__(256, 4) relu2_mul_bwd_kernel(const void *__res
 
 // ----------------------------------------------------------------- LoRA
 constexpr int kLoraRows = 4;     // rows per block of the row pass
-constexpr int kLoraChunk = 32;   // rows per block of the column pass (a power of two)
-constexpr int kLoraBatch = 8;    // rows whose loads are in flight together
 
 template <bool XBF16>
 __device__ __forceinline__ float4 ldg_x4(const void *x, size_t i4) {
@@ -176,93 +174,97 @@ __global__ void __launch_bounds__(256) lora_rows_kernel(const void *__restrict__
   }
 }
 
-// Column pass: block (tile, chunk) covers 256 groups of four columns (of dA's
-// n_in, then of dB's n_out) over kLoraChunk rows and adds its partial sums
-//   dA[j][i] += sum_t dh[t][j] x[t][i],   dB[o][j] += s sum_t dy[t][o] h[t][j].
+// Column pass: block (column tile, row chunk) covers kLoraColG groups of four
+// columns (of dA's n_in, then of dB's n_out) over 32 or 64 rows and adds its
+// partial sums
+//   dA[j][i] += sum_t dh[t][j] x[t][i],   dB[o][j] += s sum_t dy[t][o] h[t][j]
+// with vector reductions.  Thread = (column group, row slice of kLoraColK
+// rows, all loaded before the first product); the row slices' sums meet in
+// shared memory, so one reduction per output group and rank leaves the
+// block, and many small blocks keep many rows in flight.
+constexpr int kLoraColG = 32;    // 4-column groups per block
+constexpr int kLoraColK = 8;     // rows per row slice
+// row slices per block (their partial sums share 37 KB of shared memory)
+template <int RK>
+constexpr int lora_col_slices() { return RK <= 8 ? 8 : 4; }
+template <int RK>
+constexpr int lora_col_rows() { return lora_col_slices<RK>() * kLoraColK; }
+
 template <bool XBF16, int RK>
-__global__ void __launch_bounds__(256) lora_cols_kernel(const void *__restrict__ x, const float *__restrict__ dy,
-                                                        const float *__restrict__ h, const float *__restrict__ dh,
-                                                        float *__restrict__ dA, float *__restrict__ dB, int rows,
-                                                        int n_in, int n_out, int r, float scale) {
-  __shared__ float hs[kLoraChunk][RK], dhs[kLoraChunk][RK];
-  const int tid = threadIdx.x;
-  const int r0 = blockIdx.y * kLoraChunk;
-  const int nr = min(kLoraChunk, rows - r0);
-  for (int e = tid; e < kLoraChunk * RK; e += 256) {
-    const int t = e / RK, j = e % RK;
-    const bool on = t < nr && j < r;
-    hs[t][j] = on ? h[static_cast<size_t>(r0 + t) * r + j] : 0.f;
-    dhs[t][j] = on ? dh[static_cast<size_t>(r0 + t) * r + j] : 0.f;
+__global__ void __launch_bounds__(lora_col_slices<RK>() * kLoraColG) lora_cols_kernel(
+    const void *__restrict__ x, const float *__restrict__ dy, const float *__restrict__ h,
+    const float *__restrict__ dh, float *__restrict__ dA, float *__restrict__ dB, int rows, int n_in, int n_out,
+    int r, float scale) {
+  constexpr int kS = lora_col_slices<RK>(), kR = lora_col_rows<RK>(), kT = kS * kLoraColG;
+  __shared__ float coef[kR][RK];
+  __shared__ __align__(16) float part[kS][kLoraColG][4 * RK + 4];   // +4: spread the banks
+  const int tid = threadIdx.x, cg = tid & (kLoraColG - 1), sl = tid / kLoraColG;
+  const int r0 = blockIdx.y * kR;
+  const int nr = min(kR, rows - r0);
+  const int in4 = n_in >> 2, out4 = n_out >> 2;
+  const int xtiles = (in4 + kLoraColG - 1) / kLoraColG;
+  const bool xcol = static_cast<int>(blockIdx.x) < xtiles;
+  const int c0 = (xcol ? blockIdx.x : blockIdx.x - xtiles) * kLoraColG;
+  const int c = c0 + cg;   // this thread's 4-column group
+  const bool on = c < (xcol ? in4 : out4);
+  float4 v[kLoraColK];
+#pragma unroll
+  for (int k = 0; k < kLoraColK; ++k) {
+    const int tt = sl * kLoraColK + k;
+    if (on && tt < nr)
+      v[k] = xcol ? ldg_x4<XBF16>(x, static_cast<size_t>(r0 + tt) * in4 + c)
+                  : __ldg(reinterpret_cast<const float4 *>(dy + static_cast<size_t>(r0 + tt) * n_out) + c);
+    else
+      v[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  {
+    const float *src = xcol ? dh : h;   // dA needs dh, dB needs h
+    for (int e = tid; e < kR * RK; e += kT) {
+      const int tt = e / RK, j = e % RK;
+      coef[tt][j] = (tt < nr && j < r) ? src[static_cast<size_t>(r0 + tt) * r + j] : 0.f;
+    }
   }
   __syncthreads();
-  const int in4 = n_in >> 2, out4 = n_out >> 2;
-  const int c = blockIdx.x * 256 + tid;
-  // Rows go in batches of kLoraBatch whose loads are all issued before the
-  // first use, so the batch waits for one memory latency rather than one per
-  // row.
-  if (c < in4) {
-    float4 acc[RK];
+  float4 acc[RK];
 #pragma unroll
-    for (int j = 0; j < RK; ++j) acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int t0 = 0; t0 < nr; t0 += kLoraBatch) {
-      float4 xv[kLoraBatch];
+  for (int j = 0; j < RK; ++j) acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-      for (int u = 0; u < kLoraBatch; ++u)
-        xv[u] = t0 + u < nr ? ldg_x4<XBF16>(x, static_cast<size_t>(r0 + t0 + u) * in4 + c)
-                            : make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int k = 0; k < kLoraColK; ++k)
 #pragma unroll
-      for (int u = 0; u < kLoraBatch; ++u)
-#pragma unroll
-        for (int j = 0; j < RK; ++j) {
-          const float w = dhs[(t0 + u) & (kLoraChunk - 1)][j];   // rows past nr have xv = 0
-          acc[j].x = fmaf(w, xv[u].x, acc[j].x);
-          acc[j].y = fmaf(w, xv[u].y, acc[j].y);
-          acc[j].z = fmaf(w, xv[u].z, acc[j].z);
-          acc[j].w = fmaf(w, xv[u].w, acc[j].w);
-        }
+    for (int j = 0; j < RK; ++j) {
+      const float w = coef[sl * kLoraColK + k][j];   // rows past nr have v = 0
+      acc[j].x = fmaf(w, v[k].x, acc[j].x);
+      acc[j].y = fmaf(w, v[k].y, acc[j].y);
+      acc[j].z = fmaf(w, v[k].z, acc[j].z);
+      acc[j].w = fmaf(w, v[k].w, acc[j].w);
     }
 #pragma unroll
-    for (int j = 0; j < RK; ++j)
-      if (j < r) red_add_f4(dA + static_cast<size_t>(j) * n_in + 4 * c, acc[j]);
-  } else if (c < in4 + out4) {
-    const int o4 = c - in4;
-    float acc[4][RK];
+  for (int j = 0; j < RK; ++j) *reinterpret_cast<float4 *>(&part[sl][cg][4 * j]) = acc[j];
+  __syncthreads();
+  // thread -> (group g, rank j): the slices' sums of columns 4 (c0 + g) ..
+  // + 3 for rank j
+  for (int e = tid; e < kLoraColG * RK; e += kT) {
+    const int g = e / RK, j = e % RK;
+    const int cc = c0 + g;
+    if (cc >= (xcol ? in4 : out4) || j >= r) continue;
+    float4 s4 = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-    for (int e = 0; e < 4; ++e)
-#pragma unroll
-      for (int j = 0; j < RK; ++j) acc[e][j] = 0.f;
-    for (int t0 = 0; t0 < nr; t0 += kLoraBatch) {
-      float4 dv[kLoraBatch];
-#pragma unroll
-      for (int u = 0; u < kLoraBatch; ++u)
-        dv[u] = t0 + u < nr
-                    ? __ldg(reinterpret_cast<const float4 *>(dy + static_cast<size_t>(r0 + t0 + u) * n_out) + o4)
-                    : make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-      for (int u = 0; u < kLoraBatch; ++u)
-#pragma unroll
-        for (int j = 0; j < RK; ++j) {
-          const float w = hs[(t0 + u) & (kLoraChunk - 1)][j];
-          acc[0][j] = fmaf(dv[u].x, w, acc[0][j]);
-          acc[1][j] = fmaf(dv[u].y, w, acc[1][j]);
-          acc[2][j] = fmaf(dv[u].z, w, acc[2][j]);
-          acc[3][j] = fmaf(dv[u].w, w, acc[3][j]);
-        }
+    for (int q = 0; q < kS; ++q) {
+      const float4 u = *reinterpret_cast<const float4 *>(&part[q][g][4 * j]);
+      s4.x += u.x;
+      s4.y += u.y;
+      s4.z += u.z;
+      s4.w += u.w;
     }
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      float *row = dB + static_cast<size_t>(4 * o4 + e) * r;
-      if ((r & 3) == 0) {
-#pragma unroll
-        for (int j = 0; j < RK; j += 4)
-          if (j < r)
-            red_add_f4(row + j, make_float4(scale * acc[e][j], scale * acc[e][j + 1], scale * acc[e][j + 2],
-                                            scale * acc[e][j + 3]));
-      } else {
-#pragma unroll
-        for (int j = 0; j < RK; ++j)
-          if (j < r) atomicAdd(row + j, scale * acc[e][j]);
-      }
+    if (xcol) {
+      red_add_f4(dA + static_cast<size_t>(j) * n_in + 4 * cc, s4);
+    } else {
+      // column 4 cc + e of dy is row 4 cc + e of dB
+      float *col = dB + static_cast<size_t>(4 * cc) * r + j;
+      atomicAdd(col, scale * s4.x);
+      atomicAdd(col + r, scale * s4.y);
+      atomicAdd(col + 2 * r, scale * s4.z);
+      atomicAdd(col + 3 * r, scale * s4.w);
     }
   }
 }
@@ -274,9 +276,10 @@ cudaError_t lora_launch(const void *x, const float *dy, const float *A, const fl
   lora_rows_kernel<XB, RK><<<rblocks, 256, 0, st>>>(x, dy, A, B, h, dh, dA, dB, rows, n_in, n_out, r, scale);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || rows == 0) return e;
-  const int tiles = ((n_in >> 2) + (n_out >> 2) + 255) / 256;
-  const dim3 grid(tiles, (rows + kLoraChunk - 1) / kLoraChunk);
-  lora_cols_kernel<XB, RK><<<grid, 256, 0, st>>>(x, dy, h, dh, dA, dB, rows, n_in, n_out, r, scale);
+  const int tiles = ((n_in >> 2) + kLoraColG - 1) / kLoraColG + ((n_out >> 2) + kLoraColG - 1) / kLoraColG;
+  const dim3 grid(tiles, (rows + lora_col_rows<RK>() - 1) / lora_col_rows<RK>());
+  lora_cols_kernel<XB, RK><<<grid, lora_col_slices<RK>() * kLoraColG, 0, st>>>(x, dy, h, dh, dA, dB, rows, n_in,
+                                                                              n_out, r, scale);
   return cudaGetLastError();
 }
 
