@@ -51,6 +51,8 @@ def compare_units(inp, shape, dq, dk, dv, units):
     W.CausalShape(B=1, T=192, Hq=2, Hkv=2, D=128, rope_base=0.0),
     W.CausalShape(B=1, T=300, Hq=3, Hkv=1, D=128, rope_base=500000.0, pos0=5),  # G = 3, offset positions
     W.CausalShape(B=1, T=257, Hq=2, Hkv=1, D=128, rope_base=0.0, qk_mult=4.0),  # saturated softmax
+    # 8 key blocks, G = 4 split per key block into 4, 2 and 1 CTAs; ragged tail
+    W.CausalShape(B=1, T=1000, Hq=8, Hkv=2, D=128, rope_base=10000.0),
 ])
 def test_causal_small(abw, shape):
     inp = W.causal_inputs(shape, seed=shape.T + shape.Hq)
