@@ -72,6 +72,37 @@ def test_causal_t2048_sampled(abw):
     assert all(torch.isfinite(t).all() for t in (dq, dk, dv))
 
 
+@pytest.mark.parametrize("shape,exact", [
+    (W.CAUSAL_2K, True),      # one CTA per (key block, head): every output written once
+    (W.CHAIN_LAYER, False),   # head groups split per key block: dK/dV added in arrival order
+])
+def test_causal_back_to_back_calls(abw, shape, exact):
+    """Hundreds of calls queued back to back on one stream (the pattern under
+    which a lagging copy warp once met a barrier phase too early): the device
+    error word stays clear and every call gives the first call's results."""
+    g = {k: v.cuda() for k, v in W.causal_inputs(shape, seed=W.SEED_BASE + 7).items()}
+    o, lse = abw.attn_fwd_causal(g["q"], g["k"], g["v"], shape.scale)
+    ws = torch.empty(abw.attn_bwd_causal_workspace_bytes(shape.B, shape.T, shape.Hq, shape.D),
+                     dtype=torch.uint8, device="cuda")
+    out = [torch.empty(g[n].shape, dtype=torch.float32, device="cuda") for n in ("q", "k", "k")]
+
+    def call():
+        abw.attn_bwd_causal(g["q"], g["k"], g["v"], o, g["dout"], lse, shape.scale, shape.rope_base,
+                            shape.pos0, dq=out[0], dk=out[1], dv=out[2], workspace=ws)
+
+    call()
+    abw.device_check()
+    first = [t.clone() for t in out]
+    for _ in range(500):
+        call()
+    abw.device_check()
+    for a, b in zip(out, first):
+        if exact:
+            assert torch.equal(a, b)
+        else:
+            assert float((a - b).abs().max()) <= 1e-5 * float(b.abs().max())
+
+
 def test_causal_t8192_saturated_sampled(abw):
     """B = 1, H = 32, T = 8192, Q and K x4 (softmax saturation), no RoPE."""
     shape = W.CAUSAL_8K
